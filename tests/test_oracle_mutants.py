@@ -1,0 +1,56 @@
+"""Planted mistakes in copies of the oracle: each must fail at least one pin.
+
+Every mutant is the oracle's C source with one plausible slip (a dropped term,
+a wrong sign, index or comparison, a swapped operand), compiled on the CPU into
+a temporary library and run through the same pins as the real oracle.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "scale_over_dk": ("1.0 / sqrt((double)d_k)", "1.0 / (double)d_k"),
+    "no_scale": ("scale > 0.0 ? scale : 1.0 / sqrt((double)d_k)", "scale > 0.0 ? scale : 1.0"),
+    "causal_hides_diagonal": ("!(causal && j > i)", "!(causal && j >= i)"),
+    "causal_reversed": ("!(causal && j > i)", "!(causal && j < i)"),
+    "padding_off_by_one": ("(j < len) &&", "(j <= len) &&"),
+    "no_normalisation": ("double w = scores[j] / l;", "double w = scores[j];"),
+    "max_shift_wrong_sign": ("exp(scores[j] - m)", "exp(m - scores[j])"),
+    "no_max_shift": ("exp(scores[j] - m)", "exp(scores[j])"),
+    "key_is_value": ("const float* kj = k + (int64_t)j * k_stride;",
+                     "const float* kj = v + (int64_t)j * v_stride;"),
+    "value_column_index": ("out[c] += w * (double)vj[c];", "out[c] += w * (double)vj[0];"),
+    "query_row_index": ("const float* q = c->q + flat * c->d_k;", "const float* q = c->q + (flat / c->n_q) * c->n_q * c->d_k;"),
+    "length_of_other_batch": ("int len = clamp_len(c->kv_lengths, c->mask_kind, bi, c->n_k);",
+                              "int len = clamp_len(c->kv_lengths, c->mask_kind, 0, c->n_k);"),
+    "masked_row_not_zero": ("if (!any) return;               /* every key masked: output row is 0 */",
+                            "if (!any) { for (int c = 0; c < d_v; ++c) out[c] = v[c]; return; }"),
+    "mha_heads_share_query": ("attention_row_f64(qp + hi * c->d_k,", "attention_row_f64(qp,"),
+    "mha_concat_reversed": ("concat + hi * c->d_v, hdk, hdv,", "concat + (c->h - 1 - hi) * c->d_v, hdk, hdv,"),
+    "mha_value_uses_key_weights": ("proj_ctx pv = {xkv + (int64_t)bi * n_k * d_model, wv, vp, d_model, hdv};",
+                                   "proj_ctx pv = {xkv + (int64_t)bi * n_k * d_model, wk, vp, d_model, hdv};"),
+    "mha_output_skips_wo": ("yr[o] += concat[t] * (double)wt[o];", "yr[o] += (o == t) ? concat[t] : 0.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation site not found: %r" % old
+    mutated = tmp_path / ("oracle_%s.c" % name)
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(mutated), str(tmp_path / ("lib_%s.so" % name)))
+    o = oracle.Oracle(lib)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(o)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, "mutant %s passed every pin" % name
