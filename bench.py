@@ -1,0 +1,393 @@
+"""Benchmark of the fused attention hot path on GB300.
+
+One step = one pass of the attention forward (scores, scale, causal mask,
+online softmax, P.V, normalisation and store) over the long-sequence causal
+workload: batch 4, 16 heads, n_q = n_k = 8192, d_k = d_v = 128, bf16 Q/K/V =
+0.5 N(0,1), lower-triangular mask, fp32 softmax statistics.  The metric is
+attention forward TFLOP/s with 4 b h n_q n_k d_k FLOP per pass, halved for the
+causal mask, whole job (all ranks).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(no data-path collective); the timed region is bracketed by a barrier and the
+maximum over ranks is reported.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+WORKLOAD = "long_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor peak (1 GPU)"
+KERNEL_SOURCE = os.path.join(ROOT, "transformer_scaled_dot_02_gb300", "csrc", "sdpa_tc.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def metric_flops(w: synthetic.Workload) -> float:
+    f = 4.0 * w.b * w.h * w.n_q * w.n_k * w.d_k
+    return f / 2 if w.causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, or
+    None when the kernel source changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+            0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+            0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Reads the SM clock and the clock-event reasons through NVML (read only)
+    on a background thread while the timed region runs."""
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self._period = period_s
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            handle = ctypes.c_void_p()
+            uuid = None
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = device_index
+            if vis:
+                parts = [p.strip() for p in vis.split(",") if p.strip()]
+                if device_index < len(parts):
+                    if parts[device_index].isdigit():
+                        idx = int(parts[device_index])
+                    else:
+                        uuid = parts[device_index]
+            if uuid is not None:
+                rc = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle))
+            else:
+                rc = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(handle))
+            if rc != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nv, self._h, self._ct = nv, handle, ctypes
+            self.ok = True
+        except OSError:
+            return
+
+    def _run(self):
+        ct, nv, h = self._ct, self._nv, self._h
+        clk = ct.c_uint()
+        reasons = ct.c_ulonglong()
+        while not self._stop.is_set():
+            r1 = nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk))
+            r2 = nv.nvmlDeviceGetCurrentClocksEventReasons(h, ct.byref(reasons))
+            if r1 == 0:
+                self.samples.append((clk.value, reasons.value if r2 == 0 else 0))
+            time.sleep(self._period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml" if self.ok else "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        names = [n for b, n in _REASONS.items() if bits & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": names,
+                "samples": len(mhz), "source": "nvml"}
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, world, rank, local):
+    import torch
+    import transformer_scaled_dot_02_gb300 as sd
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    sd.load_library()
+
+    w = synthetic.WORKLOADS[WORKLOAD]
+    q, k, v, lens = synthetic.sdpa_inputs(w)
+    dev = torch.device("cuda", local)
+    qd = torch.from_numpy(q).to(torch.bfloat16).to(dev)
+    kd = torch.from_numpy(k).to(torch.bfloat16).to(dev)
+    vd = torch.from_numpy(v).to(torch.bfloat16).to(dev)
+    od = torch.empty((w.b, w.h, w.n_q, w.d_v), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step():
+        sd.sdpa_forward(qd, kd, vd, od, w.b, w.h, w.n_q, w.n_k, w.d_k, w.d_v, w.mask_kind,
+                        None, 0.0, sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sd.sdpa_device_check()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    with sampler:
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    sd.sdpa_device_check()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the C ABI: pinned host inputs -> device -> attention -> host
+    e2e_steps = max(1, min(args.steps, 20))
+    qh = torch.from_numpy(q).to(torch.bfloat16).pin_memory()
+    kh = torch.from_numpy(k).to(torch.bfloat16).pin_memory()
+    vh = torch.from_numpy(v).to(torch.bfloat16).pin_memory()
+    oh = torch.empty(od.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(od, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    sd.sdpa_device_check()
+
+    flops = metric_flops(w)
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    mean_launch_ms = float(np.mean(launch_ms))
+    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = recorded_traffic(WORKLOAD)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "long-sequence causal self-attention b4 h16 n8192 d128 bf16",
+                   "b": w.b, "h": w.h, "n_q": w.n_q, "n_k": w.n_k, "d_k": w.d_k, "d_v": w.d_v,
+                   "mask": "causal", "values": "0.5*N(0,1) rounded to bf16",
+                   "accumulate": "fp32", "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (Q+K+V 403 MB, O 134 MB vs 129 MB L2)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "%s bf16_tflops (burst)" % peak_src,
+                     "frac_of_sustained": round(achieved / peak_sus, 4),
+                     "traffic": traffic, "kernel": "sdpa_fwd_bf16_tc<128>",
+                     "launch_ms_mean": round(mean_launch_ms, 4),
+                     "launch_ms_min": round(float(np.min(launch_ms)), 4)},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2),
+                "d2h_bytes_per_step": int(oh.numel() * 2), "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_baseline(w, q, k, v, args.cpu_rows)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------- oracle timing
+def _sample_rows(w, n_rows, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(w.b * w.h * w.n_q, size=n_rows, replace=False)).astype(np.int64)
+
+
+def _rows_flops(w, rows):
+    i = rows % w.n_q
+    visible = (i + 1) if w.causal else np.full_like(i, w.n_k)
+    return float(np.sum(4.0 * visible * w.d_k))
+
+
+def oracle_baseline(w, q, k, v, n_rows):
+    import oracle
+    threads = oracle.default_threads()
+    rows = _sample_rows(w, n_rows, 99)
+    t = time.perf_counter()
+    oracle.sdpa(q, k, v, w.mask_kind, None, rows=rows, threads=threads)
+    dt = time.perf_counter() - t
+    value = _rows_flops(w, rows) / dt / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d query rows drawn uniformly from the %d rows of the workload "
+                      "(fp64 C oracle, %.1f s)" % (len(rows), w.b * w.h * w.n_q, dt)}
+
+
+def run_reference(args, world, rank, local):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    w = synthetic.WORKLOADS[WORKLOAD]
+    q, k, v, _ = synthetic.sdpa_inputs(w)
+    threads = oracle.default_threads()
+    rows_per_step = args.ref_rows
+    for i in range(args.warmup):
+        oracle.sdpa(q, k, v, w.mask_kind, None, rows=_sample_rows(w, rows_per_step, 1000 + i),
+                    threads=threads)
+    flops = 0.0
+    t = time.perf_counter()
+    for i in range(args.steps):
+        rows = _sample_rows(w, rows_per_step, i)
+        oracle.sdpa(q, k, v, w.mask_kind, None, rows=rows, threads=threads)
+        flops += _rows_flops(w, rows)
+    dt = time.perf_counter() - t
+    value = flops / dt / 1e12
+    sample = ("each step: %d query rows drawn uniformly from the %d rows of the workload "
+              "(fp64 C oracle, %d threads)" % (rows_per_step, w.b * w.h * w.n_q, threads))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": "long-sequence causal self-attention b4 h16 n8192 d128 bf16",
+                   "b": w.b, "h": w.h, "n_q": w.n_q, "n_k": w.n_k, "d_k": w.d_k, "d_v": w.d_v,
+                   "mask": "causal"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=16384,
+                    help="query rows in the oracle's timed CPU sample")
+    ap.add_argument("--ref-rows", type=int, default=2048,
+                    help="query rows per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,132 @@
+/*
+ * libsdpa: fused scaled dot-product attention and multi-head attention on
+ * one GB300 GPU (sm_103a), behind a plain C ABI.
+ *
+ * The operations are those of "Attention Is All You Need":
+ *   section 3.2.1, Eq. (1):  Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k)) V
+ *   section 3.2.3:           illegal (future) connections of the decoder's
+ *                            self-attention are set to -infinity before the
+ *                            softmax, so position i sees keys j <= i
+ *   section 3.2.2:           MultiHead(Q, K, V) = Concat(head_1..head_h) W^O,
+ *                            head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V)
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named as device pointers are CUDA device addresses on the
+ *     current device, owned by the caller; the library keeps no reference
+ *     after the call returns and allocates no memory on the call path.
+ *   - Tensors are dense and row-major; every device pointer must be 16-byte
+ *     aligned (the kernels move tiles with the Tensor Memory Accelerator).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  A successful return means the work was
+ *     enqueued; errors detected on the host are returned before anything is
+ *     enqueued.
+ *   - Masks (`mask_kind`, bit flags): SDPA_MASK_CAUSAL hides keys j > i (it
+ *     requires n_q == n_k); SDPA_MASK_PADDING hides keys j >= kv_lengths[b]
+ *     (`kv_lengths`: device int32 [b], values clamped into [0, n_k] on the
+ *     device).  A query row with no visible key returns a row of zeros.
+ *   - `scale` multiplies Q K^T; 0.0f selects 1/sqrt(d_k) (Eq. (1)); 1.0f gives
+ *     the unscaled dot-product attention of section 3.2.1.  It must be >= 0
+ *     and finite.
+ */
+#ifndef LIBSDPA_SDPA_H
+#define LIBSDPA_SDPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,        /* null pointer, bad size, misalignment, bad mask */
+  SDPA_ERR_UNSUPPORTED = 2,        /* valid but outside what the kernels implement */
+  SDPA_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or not an sm_103 GPU */
+  SDPA_ERR_WORKSPACE = 4,          /* workspace null or smaller than mha_workspace_size() */
+  SDPA_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+  SDPA_ERR_DEVICE_TIMEOUT = 6      /* a kernel gave up on a bounded wait (sdpa_device_check) */
+} sdpa_status;
+
+enum { SDPA_MASK_NONE = 0, SDPA_MASK_CAUSAL = 1, SDPA_MASK_PADDING = 2 };
+
+/*
+ * Scaled dot-product attention, bf16 (Eq. (1) with the masks above).
+ *   q   [b, h, n_q, d_k]  bf16, device
+ *   k   [b, h, n_k, d_k]  bf16, device
+ *   v   [b, h, n_k, d_v]  bf16, device
+ *   out [b, h, n_q, d_v]  bf16, device, written (must not overlap the inputs)
+ * Scores, softmax statistics and the P.V accumulation are fp32; the
+ * softmax weights enter P.V rounded to bf16.  Supported: d_k == d_v, 64 or
+ * 128 (else SDPA_ERR_UNSUPPORTED).  b, h >= 1; n_q, n_k >= 0 (zero-sized
+ * work returns SDPA_OK with nothing enqueued; n_k == 0 writes zeros).
+ */
+sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
+                         int b, int h, int n_q, int n_k, int d_k, int d_v,
+                         int mask_kind, const int32_t* kv_lengths, float scale,
+                         void* stream);
+
+/*
+ * The same operation in fp32 throughout (fp32 inputs, exact fp32 exponentials
+ * and sums on the CUDA cores), for small fp32 problems and the worked
+ * examples.  Layouts as sdpa_forward with float elements; any
+ * 1 <= d_k, d_v <= 128.
+ */
+sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* out,
+                             int b, int h, int n_q, int n_k, int d_k, int d_v,
+                             int mask_kind, const int32_t* kv_lengths, float scale,
+                             void* stream);
+
+/*
+ * Bytes of device workspace mha_forward needs: the projected Q [b*n_q, h*d_k],
+ * K [b*n_k, h*d_k], V [b*n_k, h*d_v] and the concatenated heads
+ * [b*n_q, h*d_v], bf16, each rounded up to 256 bytes.  Returns 0 for
+ * negative sizes.
+ */
+size_t mha_workspace_size(int b, int n_q, int n_k, int h, int d_k, int d_v);
+
+/*
+ * Multi-head attention (section 3.2.2) without biases:
+ *   Q = X_q W^Q, K = X_kv W^K, V = X_kv W^V, head i = columns [i*d, (i+1)*d),
+ *   Y = Concat(head_1..head_h) W^O.
+ *   xq  [b, n_q, d_model]   bf16, device (decoder queries, or the sequence)
+ *   xkv [b, n_k, d_model]   bf16, device (encoder output for cross-attention;
+ *                           pass xkv == xq and n_k == n_q for self-attention)
+ *   wq, wk [d_model, h*d_k]; wv [d_model, h*d_v]; wo [h*d_v, d_model]  bf16, device
+ *   y   [b, n_q, d_model]   bf16, device, written
+ *   workspace: device buffer of ws_bytes >= mha_workspace_size(...), 16-byte
+ *   aligned, owned by the caller and reusable once the stream passes the call.
+ * Projections run on the tensor cores with fp32 accumulation and bf16
+ * outputs; the heads are written straight into the Concat layout.
+ * Supported: d_k == d_v in {64, 128}; d_model a multiple of 8.
+ */
+sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const void* wk,
+                        const void* wv, const void* wo, void* y, void* workspace,
+                        size_t ws_bytes, int b, int n_q, int n_k, int d_model, int h,
+                        int d_k, int d_v, int mask_kind, const int32_t* kv_lengths,
+                        float scale, void* stream);
+
+/*
+ * One projection of section 3.2.2 on its own: y[m, n] = sum_k x[m, k] w[k, n],
+ * x [m, k], w [k, n], y [m, n] bf16 row-major device tensors, fp32
+ * accumulation.  k and n must be multiples of 8; m, n, k >= 1.
+ */
+sdpa_status linear_forward(const void* x, const void* w, void* y, int m, int n, int k,
+                           void* stream);
+
+/*
+ * Waits for the current device to finish its queued work, then reads and
+ * clears the kernels' error word.  Returns SDPA_ERR_DEVICE_TIMEOUT if a
+ * kernel abandoned a bounded wait since the last check (its output is then
+ * undefined), SDPA_ERR_CUDA if the synchronisation failed, else SDPA_OK.
+ */
+sdpa_status sdpa_device_check(void);
+
+/* A static, human-readable name for a status code. */
+const char* sdpa_status_string(sdpa_status status);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* LIBSDPA_SDPA_H */

@@ -1,0 +1,175 @@
+"""bf16 tensor-core attention against the fp64 oracle on identical inputs.
+
+Bar: max|gpu - oracle| / max|oracle| <= 2e-2 (bf16 inputs, fp32
+accumulation).  Small and medium cases compare every output; the full-size
+long causal workload (the benchmark's launch) compares sampled rows that the
+oracle evaluates one by one.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import transformer_scaled_dot_02_gb300 as sd
+from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    sd.load_library()
+
+
+def _gpu(q, k, v, mask=0, lens=None, scale=0.0):
+    out = sd.attention(dev(q), dev(k), dev(v), mask, None if lens is None else dev_int(lens), scale)
+    sd.sdpa_device_check()
+    return host(out)
+
+
+def _rand(rng, shape, std=1.0):
+    return synthetic.round_to_bf16(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask", [0, 1, 2, 3])
+@pytest.mark.parametrize("n", [1, 17, 129, 300])
+def test_edge_shapes(d, mask, n):
+    """Ragged sequence lengths (inside one tile, just past one, several tiles
+    and a ragged tail) with every mask combination."""
+    rng = np.random.default_rng(1000 * d + 10 * mask + n)
+    b, h = 2, 3
+    n_q = n
+    n_k = n if mask & 1 else n + 45
+    q, k, v = _rand(rng, (b, h, n_q, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+    lens = np.array([n_k, max(1, n_k // 3)], np.int32) if mask & 2 else None
+    got = _gpu(q, k, v, mask, lens)
+    ref = oracle.sdpa(q, k, v, mask, lens)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_padding_degenerate_lengths(d):
+    """len 0 (no visible key: zeros), len 1 (value row 0), len > n_k (clamped)."""
+    rng = np.random.default_rng(7 + d)
+    q, k, v = _rand(rng, (4, 2, 200, d)), _rand(rng, (4, 2, 250, d)), _rand(rng, (4, 2, 250, d))
+    lens = np.array([0, 1, 250, 1000], np.int32)
+    got = _gpu(q, k, v, sd.SDPA_MASK_PADDING, lens)
+    ref = oracle.sdpa(q, k, v, sd.SDPA_MASK_PADDING, lens)
+    assert np.array_equal(got[0], np.zeros_like(got[0]))
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_no_keys(d):
+    rng = np.random.default_rng(3)
+    q = _rand(rng, (1, 2, 40, d))
+    kv = dev(np.ones((1, 2, 1, d), np.float32))   # a valid buffer; n_k = 0 reads none of it
+    t = __import__("torch")
+    out = t.full((1, 2, 40, d), 5.0, dtype=t.bfloat16, device="cuda")
+    sd.sdpa_forward(dev(q), kv, kv, out, 1, 2, 40, 0, d, d, 0)
+    sd.sdpa_device_check()
+    assert np.array_equal(host(out), np.zeros((1, 2, 40, d)))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_sharp_scores_move_the_running_max(d):
+    """Large, growing scores force the online softmax to rescale O many times."""
+    rng = np.random.default_rng(11 + d)
+    n = 700
+    q = _rand(rng, (1, 2, n, d), 3.0)
+    k = _rand(rng, (1, 2, n, d), 3.0)
+    # keys whose norm grows along the sequence: later tiles hold larger maxima
+    k = synthetic.round_to_bf16((k * np.linspace(0.2, 1.5, n, dtype=np.float32)[None, None, :, None]))
+    v = _rand(rng, (1, 2, n, d))
+    for mask in (0, 1):
+        got = _gpu(q, k, v, mask)
+        ref = oracle.sdpa(q, k, v, mask)
+        assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_unscaled_and_custom_scale():
+    rng = np.random.default_rng(12)
+    q, k, v = _rand(rng, (2, 2, 150, 64), 0.3), _rand(rng, (2, 2, 150, 64), 0.3), _rand(rng, (2, 2, 150, 64))
+    for scale in (1.0, 0.05):
+        got = _gpu(q, k, v, 1, None, scale)
+        ref = oracle.sdpa(q, k, v, 1, None, scale)
+        assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_single_head_many_tiles():
+    rng = np.random.default_rng(13)
+    q, k, v = _rand(rng, (1, 1, 1100, 128)), _rand(rng, (1, 1, 1100, 128)), _rand(rng, (1, 1, 1100, 128))
+    got = _gpu(q, k, v, sd.SDPA_MASK_CAUSAL)
+    ref = oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_deterministic():
+    rng = np.random.default_rng(14)
+    q, k, v = _rand(rng, (2, 4, 600, 128)), _rand(rng, (2, 4, 600, 128)), _rand(rng, (2, 4, 600, 128))
+    a = _gpu(q, k, v, 1)
+    b = _gpu(q, k, v, 1)
+    assert np.array_equal(a, b)
+
+
+def test_output_bounds_untouched():
+    """The kernel writes exactly its output tensor: guard bands stay intact."""
+    t = __import__("torch")
+    rng = np.random.default_rng(15)
+    b, h, n, d = 2, 3, 333, 64
+    q, k, v = _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n, d))
+    numel = b * h * n * d
+    guard = 4096
+    buf = t.full((numel + 2 * guard,), 7.0, dtype=t.bfloat16, device="cuda")
+    out = buf[guard:guard + numel]
+    sd.sdpa_forward(dev(q), dev(k), dev(v), out, b, h, n, n, d, d, sd.SDPA_MASK_CAUSAL)
+    sd.sdpa_device_check()
+    assert bool((buf[:guard] == 7.0).all()) and bool((buf[guard + numel:] == 7.0).all())
+    ref = oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)
+    assert rel_err(host(out).reshape(b, h, n, d), ref) <= TOL_BF16
+
+
+# ------------------------------------------------------------ the workloads
+@pytest.mark.parametrize("name", ["dec_causal_base", "enc_mha_base"])
+def test_workload_full_compare(name):
+    """Base-model decoder causal self-attention (b16 h8 n512 d64) and the
+    encoder's attention core (b32 h8 n128 d64, key padding 64..128)."""
+    w = synthetic.WORKLOADS[name]
+    q, k, v, lens = synthetic.sdpa_inputs(w)
+    got = _gpu(q, k, v, w.mask_kind, lens)
+    ref = oracle.sdpa(q, k, v, w.mask_kind, lens)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_cross_attention_workload():
+    """Big-model cross-attention core (b32 h16 n_q256 n_k384 d64, key padding
+    192..384): whole output of the first 6 batch entries, sampled rows of all."""
+    w = synthetic.WORKLOADS["cross_big"]
+    q, k, v, lens = synthetic.sdpa_inputs(w)
+    got = _gpu(q, k, v, w.mask_kind, lens)
+    ref = oracle.sdpa(q[:6], k[:6], v[:6], w.mask_kind, lens[:6])
+    assert rel_err(got[:6], ref) <= TOL_BF16
+    rng = np.random.default_rng(16)
+    rows = rng.choice(w.b * w.h * w.n_q, size=512, replace=False)
+    ref_rows = oracle.sdpa(q, k, v, w.mask_kind, lens, rows=rows)
+    assert rel_err(got.reshape(-1, w.d_v)[rows], ref_rows) <= TOL_BF16
+
+
+def test_long_causal_workload_sampled_rows():
+    """Long-sequence causal stress at full size (b4 h16 n8192 d128, values
+    0.5 N(0,1)), the benchmark's launch: rows at tile edges and at random."""
+    w = synthetic.WORKLOADS["long_causal"]
+    q, k, v, lens = synthetic.sdpa_inputs(w)
+    got = _gpu(q, k, v, w.mask_kind, lens)
+    rng = np.random.default_rng(17)
+    edges = [0, 1, 127, 128, 255, 256, 257, 4095, 4096, 8063, 8064, 8190, 8191]
+    rows = []
+    for bh in (0, 17, 63):
+        rows += [bh * w.n_q + i for i in edges]
+    rows += list(rng.choice(w.b * w.h * w.n_q, size=400, replace=False))
+    rows = np.array(rows, np.int64)
+    ref_rows = oracle.sdpa(q, k, v, w.mask_kind, lens, rows=rows)
+    assert rel_err(got.reshape(-1, w.d_v)[rows], ref_rows) <= TOL_BF16
+    # every row is a convex combination of value rows: bounded by max |V|
+    assert np.abs(got).max() <= np.abs(v).max() * 1.01

@@ -1,0 +1,167 @@
+"""Python binding of libsdpa: fused scaled dot-product and multi-head attention
+on one GB300 GPU.
+
+The functions below carry the names of the C entry points in include/sdpa.h
+and only marshal arguments: every step of the computation runs in the CUDA
+kernels of libsdpa.so.  Tensor arguments may be torch tensors (their
+``data_ptr()`` is passed) or raw device addresses as ints.  ``stream`` defaults
+to PyTorch's current CUDA stream.
+
+There is no fallback: if libsdpa.so is missing or fails to load, importing the
+functions raises, and every call returns the library's status as an exception.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdpa.so")
+
+SDPA_MASK_NONE = 0
+SDPA_MASK_CAUSAL = 1
+SDPA_MASK_PADDING = 2
+
+STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED",
+                3: "SDPA_ERR_UNSUPPORTED_DEVICE", 4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA",
+                6: "SDPA_ERR_DEVICE_TIMEOUT"}
+
+# Every symbol include/sdpa.h declares.
+EXPORTS = ("sdpa_forward", "sdpa_forward_f32", "mha_workspace_size", "mha_forward",
+           "linear_forward", "sdpa_device_check", "sdpa_status_string")
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, STATUS_NAMES.get(status, "status %d" % status)))
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads libsdpa.so (built by ``build.build()``) and declares its ABI."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError("libsdpa.so not built (%s); run transformer_scaled_dot_02_gb300.build" % p)
+    lib = ctypes.CDLL(p)
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    attn = [P, P, P, P, I, I, I, I, I, I, I, P, F, P]
+    lib.sdpa_forward.argtypes = attn
+    lib.sdpa_forward.restype = I
+    lib.sdpa_forward_f32.argtypes = attn
+    lib.sdpa_forward_f32.restype = I
+    lib.mha_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.mha_workspace_size.restype = SZ
+    lib.mha_forward.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, I, P, F, P]
+    lib.mha_forward.restype = I
+    lib.linear_forward.argtypes = [P, P, P, I, I, I, P]
+    lib.linear_forward.restype = I
+    lib.sdpa_device_check.argtypes = []
+    lib.sdpa_device_check.restype = I
+    lib.sdpa_status_string.argtypes = [I]
+    lib.sdpa_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise SdpaError(status, where)
+
+
+def sdpa_forward(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE,
+                 kv_lengths=None, scale=0.0, stream=None) -> None:
+    """bf16 attention, BHSD tensors (see include/sdpa.h)."""
+    _check(load_library().sdpa_forward(_addr(q), _addr(k), _addr(v), _addr(out), b, h, n_q, n_k,
+                                       d_k, d_v, mask_kind, _addr(kv_lengths), float(scale),
+                                       _stream(stream)), "sdpa_forward")
+
+
+def sdpa_forward_f32(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE,
+                     kv_lengths=None, scale=0.0, stream=None) -> None:
+    """fp32 attention, BHSD tensors (see include/sdpa.h)."""
+    _check(load_library().sdpa_forward_f32(_addr(q), _addr(k), _addr(v), _addr(out), b, h, n_q,
+                                           n_k, d_k, d_v, mask_kind, _addr(kv_lengths),
+                                           float(scale), _stream(stream)), "sdpa_forward_f32")
+
+
+def mha_workspace_size(b, n_q, n_k, h, d_k, d_v) -> int:
+    return int(load_library().mha_workspace_size(b, n_q, n_k, h, d_k, d_v))
+
+
+def mha_forward(xq, xkv, wq, wk, wv, wo, y, workspace, ws_bytes, b, n_q, n_k, d_model, h, d_k,
+                d_v, mask_kind=SDPA_MASK_NONE, kv_lengths=None, scale=0.0, stream=None) -> None:
+    """Multi-head attention with projections (see include/sdpa.h)."""
+    _check(load_library().mha_forward(_addr(xq), _addr(xkv), _addr(wq), _addr(wk), _addr(wv),
+                                      _addr(wo), _addr(y), _addr(workspace), int(ws_bytes), b, n_q,
+                                      n_k, d_model, h, d_k, d_v, mask_kind, _addr(kv_lengths),
+                                      float(scale), _stream(stream)), "mha_forward")
+
+
+def linear_forward(x, w, y, m, n, k, stream=None) -> None:
+    """y = x w for row-major bf16 matrices (see include/sdpa.h)."""
+    _check(load_library().linear_forward(_addr(x), _addr(w), _addr(y), m, n, k, _stream(stream)),
+           "linear_forward")
+
+
+def sdpa_device_check() -> None:
+    """Synchronises the device; raises if a kernel gave up on a bounded wait."""
+    _check(load_library().sdpa_device_check(), "sdpa_device_check")
+
+
+def sdpa_status_string(status: int) -> str:
+    return load_library().sdpa_status_string(status).decode()
+
+
+# ---------------------------------------------------------------- conveniences
+def attention(q, k, v, mask_kind=SDPA_MASK_NONE, kv_lengths=None, scale=0.0, stream=None):
+    """Allocates the output with torch and calls sdpa_forward (bf16) or
+    sdpa_forward_f32 (fp32) on BHSD tensors q [b,h,n_q,d_k], k, v."""
+    import torch
+    b, h, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    out = torch.empty((b, h, n_q, d_v), dtype=q.dtype, device=q.device)
+    fn = sdpa_forward if q.dtype == torch.bfloat16 else sdpa_forward_f32
+    fn(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths, scale, stream)
+    return out
+
+
+def multi_head_attention(xq, xkv, wq, wk, wv, wo, h, mask_kind=SDPA_MASK_NONE, kv_lengths=None,
+                         scale=0.0, workspace=None, stream=None):
+    """Allocates the output (and, if not given, the workspace) with torch and
+    calls mha_forward."""
+    import torch
+    b, n_q, d_model = xq.shape
+    n_k = xkv.shape[1]
+    d_k = wq.shape[1] // h
+    d_v = wv.shape[1] // h
+    need = mha_workspace_size(b, n_q, n_k, h, d_k, d_v)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=xq.device)
+    y = torch.empty((b, n_q, d_model), dtype=xq.dtype, device=xq.device)
+    mha_forward(xq, xkv, wq, wk, wv, wo, y, workspace, workspace.numel() * workspace.element_size(),
+                b, n_q, n_k, d_model, h, d_k, d_v, mask_kind, kv_lengths, scale, stream)
+    return y

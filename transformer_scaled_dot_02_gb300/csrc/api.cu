@@ -1,0 +1,354 @@
+// The C ABI of libsdpa (declared in include/sdpa.h): argument checks, tensor
+// maps for the TMA, and the launches of the attention and projection kernels.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "kernels.h"
+#include "sdpa.h"
+
+namespace {
+
+using sdpa::GemmParams;
+using sdpa::GemmProblem;
+using sdpa::SdpaF32Params;
+using sdpa::SdpaTcParams;
+
+// Error word the kernels raise bits in (bounded waits that gave up).
+__device__ unsigned g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  unsigned* status = nullptr;  // device address of g_device_status
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// Checks that the current device is a GB300-class (sm_103) GPU and returns its
+// status-word address.  The first call on a device does the probing.
+sdpa_status current_device(unsigned** status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SDPA_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return SDPA_ERR_UNSUPPORTED_DEVICE;
+    }
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
+        cudaGetLastError();
+        return SDPA_ERR_CUDA;
+      }
+      st.status = static_cast<unsigned*>(addr);
+    }
+    st.probed = true;
+  }
+  if (!st.supported) return SDPA_ERR_UNSUPPORTED_DEVICE;
+  *status = st.status;
+  return SDPA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
+// 64 x 128 boxes, 128-byte swizzle, zero fill outside the tensor.
+bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
+                 long long stride_n, long long stride_h, long long stride_b) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n > 0 ? n : 1),
+                              static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(b)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(stride_n) * 2,
+                                 static_cast<cuuint64_t>(stride_h) * 2,
+                                 static_cast<cuuint64_t>(stride_b) * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix: box (64 cols, box_rows).
+bool make_map_2d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared argument rules of the attention entry points (host-only checks).
+sdpa_status check_attention_args(const void* q, const void* k, const void* v, const void* out,
+                                 int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                                 const int32_t* kv_lengths, float scale) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return SDPA_ERR_INVALID_ARG;
+  if (b < 1 || h < 1 || n_q < 0 || n_k < 0 || d_k < 1 || d_v < 1) return SDPA_ERR_INVALID_ARG;
+  if (mask_kind < 0 || mask_kind > (SDPA_MASK_CAUSAL | SDPA_MASK_PADDING))
+    return SDPA_ERR_INVALID_ARG;
+  if ((mask_kind & SDPA_MASK_CAUSAL) && n_q != n_k) return SDPA_ERR_INVALID_ARG;
+  if ((mask_kind & SDPA_MASK_PADDING) &&
+      (kv_lengths == nullptr || (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0))
+    return SDPA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
+  // Sizes must stay addressable by the TMA (dimension <= 2^32, strides < 2^40 bytes).
+  const long long elems_q = 1ll * b * h * n_q * (d_k > d_v ? d_k : d_v);
+  const long long elems_k = 1ll * b * h * n_k * (d_k > d_v ? d_k : d_v);
+  if (elems_q > (1ll << 38) || elems_k > (1ll << 38)) return SDPA_ERR_UNSUPPORTED;
+  return SDPA_OK;
+}
+
+float effective_scale(float scale, int d_k) {
+  return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
+}
+
+// Launches the tensor-core attention over tensors with arbitrary (n, h, b)
+// element strides (BHSD for sdpa_forward, BSHD inside mha_forward).
+sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, void* out, int b,
+                                int h, int n_q, int n_k, int d, long long q_sn, long long q_sh,
+                                long long q_sb, long long kv_sn, long long kv_sh, long long kv_sb,
+                                long long o_sn, long long o_sh, long long o_sb, int mask_kind,
+                                const int32_t* kv_lengths, float scale, unsigned* status,
+                                cudaStream_t stream) {
+  SdpaTcParams p;
+  if (!make_map_4d(&p.tm_q, q, d, n_q, h, b, q_sn, q_sh, q_sb) ||
+      !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb) ||
+      !make_map_4d(&p.tm_v, v, d, n_k, h, b, kv_sn, kv_sh, kv_sb) ||
+      !make_map_4d(&p.tm_o, out, d, n_q, h, b, o_sn, o_sh, o_sb))
+    return SDPA_ERR_CUDA;
+  p.kv_lengths = (mask_kind & SDPA_MASK_PADDING) ? kv_lengths : nullptr;
+  p.status = status;
+  p.b = b;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.mask_kind = mask_kind;
+  p.num_q_blocks = (n_q + 255) / 256;
+  p.scale_log2 = effective_scale(scale, d) * 1.4426950408889634f;
+  return sdpa::launch_sdpa_tc(p, d, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+bool fill_gemm_problem(GemmProblem* pr, const void* x, const void* w, void* y, int m, int n,
+                       int k) {
+  pr->m = m;
+  pr->n = n;
+  pr->k = k;
+  return make_map_2d(&pr->tm_a, x, m, k, sdpa::kGemmBlockM) && make_map_2d(&pr->tm_b, w, k, n, 64) &&
+         make_map_2d(&pr->tm_c, y, m, n, sdpa::kGemmBlockM);
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out, int b, int h,
+                         int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                         const int32_t* kv_lengths, float scale, void* stream) {
+  sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
+                                        kv_lengths, scale);
+  if (st != SDPA_OK) return st;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return SDPA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0) return SDPA_OK;
+  const long long d = d_k;
+  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d, 1ll * n_q * d,
+                             1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
+                             1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* out, int b, int h,
+                             int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                             const int32_t* kv_lengths, float scale, void* stream) {
+  sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
+                                        kv_lengths, scale);
+  if (st != SDPA_OK) return st;
+  if (d_k > 128 || d_v > 128 || 1ll * b * h > 65535) return SDPA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0) return SDPA_OK;
+  SdpaF32Params p;
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.out = static_cast<float*>(out);
+  p.kv_lengths = (mask_kind & SDPA_MASK_PADDING) ? kv_lengths : nullptr;
+  p.b = b;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.d_k = d_k;
+  p.d_v = d_v;
+  p.mask_kind = mask_kind;
+  p.scale = effective_scale(scale, d_k);
+  return sdpa::launch_sdpa_f32(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
+}
+
+size_t mha_workspace_size(int b, int n_q, int n_k, int h, int d_k, int d_v) {
+  if (b < 0 || n_q < 0 || n_k < 0 || h < 0 || d_k < 0 || d_v < 0) return 0;
+  const size_t bq = static_cast<size_t>(b) * n_q, bk = static_cast<size_t>(b) * n_k;
+  return round256(bq * h * d_k * 2) + round256(bk * h * d_k * 2) + round256(bk * h * d_v * 2) +
+         round256(bq * h * d_v * 2);
+}
+
+sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const void* wk,
+                        const void* wv, const void* wo, void* y, void* workspace, size_t ws_bytes,
+                        int b, int n_q, int n_k, int d_model, int h, int d_k, int d_v,
+                        int mask_kind, const int32_t* kv_lengths, float scale, void* stream) {
+  if (xq == nullptr || xkv == nullptr || wq == nullptr || wk == nullptr || wv == nullptr ||
+      wo == nullptr || y == nullptr)
+    return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(xkv) || !aligned16(wq) || !aligned16(wk) || !aligned16(wv) ||
+      !aligned16(wo) || !aligned16(y))
+    return SDPA_ERR_INVALID_ARG;
+  if (b < 1 || h < 1 || n_q < 0 || n_k < 0 || d_model < 1 || d_k < 1 || d_v < 1)
+    return SDPA_ERR_INVALID_ARG;
+  if (mask_kind < 0 || mask_kind > (SDPA_MASK_CAUSAL | SDPA_MASK_PADDING))
+    return SDPA_ERR_INVALID_ARG;
+  if ((mask_kind & SDPA_MASK_CAUSAL) && n_q != n_k) return SDPA_ERR_INVALID_ARG;
+  if ((mask_kind & SDPA_MASK_PADDING) &&
+      (kv_lengths == nullptr || (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0))
+    return SDPA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
+  if (d_k != d_v || (d_k != 64 && d_k != 128) || d_model % 8 != 0) return SDPA_ERR_UNSUPPORTED;
+  if (1ll * b * (n_q > n_k ? n_q : n_k) > (1ll << 30) || 1ll * h * d_k > 65536)
+    return SDPA_ERR_UNSUPPORTED;
+  const size_t need = mha_workspace_size(b, n_q, n_k, h, d_k, d_v);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return SDPA_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  sdpa_status st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0) return SDPA_OK;
+
+  const size_t bq = static_cast<size_t>(b) * n_q, bk = static_cast<size_t>(b) * n_k;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qp = ws;
+  void* kp = ws + round256(bq * h * d_k * 2);
+  void* vp = static_cast<uint8_t*>(kp) + round256(bk * h * d_k * 2);
+  void* op = static_cast<uint8_t*>(vp) + round256(bk * h * d_v * 2);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int m_q = static_cast<int>(bq), m_k = static_cast<int>(bk);
+  const int hd = h * d_k;
+
+  // Q = X_q W^Q, K = X_kv W^K, V = X_kv W^V in one launch; outputs [b*n, h*d]
+  // row-major, which is the per-head layout [b, n, h, d] the attention reads.
+  GemmParams gp;
+  gp.status = status;
+  gp.num_problems = 0;
+  if (!fill_gemm_problem(&gp.prob[gp.num_problems++], xq, wq, qp, m_q, hd, d_model))
+    return SDPA_ERR_CUDA;
+  if (m_k > 0) {
+    if (!fill_gemm_problem(&gp.prob[gp.num_problems++], xkv, wk, kp, m_k, hd, d_model) ||
+        !fill_gemm_problem(&gp.prob[gp.num_problems++], xkv, wv, vp, m_k, hd, d_model))
+      return SDPA_ERR_CUDA;
+  }
+  if (sdpa::launch_gemm_tc(gp, m_q > m_k ? m_q : m_k, hd, s) != cudaSuccess) return SDPA_ERR_CUDA;
+
+  // Heads: strides of [b, n, h, d]; the output lands in Concat order.
+  const long long d = d_k;
+  st = launch_attention_tc(qp, kp, vp, op, b, h, n_q, n_k, d_k, 1ll * h * d, d, 1ll * n_q * h * d,
+                           1ll * h * d, d, 1ll * n_k * h * d, 1ll * h * d, d, 1ll * n_q * h * d,
+                           mask_kind, kv_lengths, scale, status, s);
+  if (st != SDPA_OK) return st;
+
+  // Y = Concat(heads) W^O
+  GemmParams go;
+  go.status = status;
+  go.num_problems = 1;
+  if (!fill_gemm_problem(&go.prob[0], op, wo, y, m_q, d_model, h * d_v)) return SDPA_ERR_CUDA;
+  return sdpa::launch_gemm_tc(go, m_q, d_model, s) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+sdpa_status linear_forward(const void* x, const void* w, void* y, int m, int n, int k,
+                           void* stream) {
+  if (x == nullptr || w == nullptr || y == nullptr) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return SDPA_ERR_INVALID_ARG;
+  if (m < 1 || n < 1 || k < 1) return SDPA_ERR_INVALID_ARG;
+  if (n % 8 != 0 || k % 8 != 0) return SDPA_ERR_UNSUPPORTED;
+  if (m > (1 << 30)) return SDPA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  sdpa_status st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  GemmParams gp;
+  gp.status = status;
+  gp.num_problems = 1;
+  if (!fill_gemm_problem(&gp.prob[0], x, w, y, m, n, k)) return SDPA_ERR_CUDA;
+  return sdpa::launch_gemm_tc(gp, m, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
+}
+
+sdpa_status sdpa_device_check(void) {
+  unsigned* status = nullptr;
+  sdpa_status st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return SDPA_ERR_CUDA;
+  }
+  unsigned word = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof(word)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return SDPA_ERR_CUDA;
+  }
+  return (word & sdpa::kStatusTimeout) ? SDPA_ERR_DEVICE_TIMEOUT : SDPA_OK;
+}
+
+const char* sdpa_status_string(sdpa_status status) {
+  switch (status) {
+    case SDPA_OK: return "SDPA_OK";
+    case SDPA_ERR_INVALID_ARG: return "SDPA_ERR_INVALID_ARG";
+    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED";
+    case SDPA_ERR_UNSUPPORTED_DEVICE: return "SDPA_ERR_UNSUPPORTED_DEVICE";
+    case SDPA_ERR_WORKSPACE: return "SDPA_ERR_WORKSPACE";
+    case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA";
+    case SDPA_ERR_DEVICE_TIMEOUT: return "SDPA_ERR_DEVICE_TIMEOUT";
+  }
+  return "SDPA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Host-side launch interfaces of the CUDA kernels (internal to libsdpa).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace sdpa {
+
+// Error bits of the device status word (read back by sdpa_device_check).
+constexpr unsigned kStatusTimeout = 1u;
+
+// Fused bf16 attention on the tensor cores.  The four tensor maps view
+// Q, K, V and O as 4-D (d, n, h, b) arrays with 64 x 128 boxes, 128-byte
+// swizzle; any strides for n, h, b (BHSD inputs, or BSHD inside the
+// multi-head path).
+struct SdpaTcParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  const int32_t* kv_lengths;  // device [b] or null
+  unsigned* status;           // device error word
+  int b, h, n_q, n_k;
+  int mask_kind;
+  int num_q_blocks;           // ceil(n_q / 256)
+  float scale_log2;           // scale * log2(e)
+};
+cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
+
+// Exact fp32 attention on the CUDA cores, BHSD contiguous.
+struct SdpaF32Params {
+  const float *q, *k, *v;
+  float* out;
+  const int32_t* kv_lengths;
+  int b, h, n_q, n_k, d_k, d_v;
+  int mask_kind;
+  float scale;
+};
+cudaError_t launch_sdpa_f32(const SdpaF32Params& p, cudaStream_t stream);
+
+// bf16 GEMM on the tensor cores, up to three independent problems per launch
+// (blockIdx.z): Y[m, n] = X[m, k] * W[k, n], all row-major.
+struct GemmProblem {
+  CUtensorMap tm_a;  // X: 2-D (k, m), box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_b;  // W: 2-D (n, k), box 64 x 64, 128-byte swizzle
+  CUtensorMap tm_c;  // Y: 2-D (n, m), box 64 x 128, 128-byte swizzle
+  int m, n, k;
+};
+struct GemmParams {
+  GemmProblem prob[3];
+  int num_problems;
+  unsigned* status;
+};
+constexpr int kGemmBlockM = 128;
+constexpr int kGemmBlockN = 256;
+cudaError_t launch_gemm_tc(const GemmParams& p, int max_m, int max_n, cudaStream_t stream);
+
+}  // namespace sdpa

@@ -1,0 +1,442 @@
+// Fused scaled dot-product attention, bf16 in/out, fp32 accumulation, on the
+// GB300 tensor cores (tcgen05 + TMA + tensor memory).
+//
+// Operation ("Attention Is All You Need", section 3.2.1, Eq. (1), with the
+// decoder's -infinity mask of section 3.2.3 and a key-padding mask):
+//   O[i, :] = sum_j softmax_j(scale * Q[i, :] . K[j, :]) V[j, :]
+// evaluated as an online (streaming) softmax over 128-key tiles, so the
+// n_q x n_k score matrix never leaves the SM.
+//
+// One CTA owns two 128-row query tiles of one (batch, head) and walks the
+// key/value tiles once for both:
+//   warp 8      TMA producer: Q tiles once, then K_j and V_j into a ring of
+//               shared-memory stages (128-byte swizzle, zero fill past n).
+//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
+//               then O_t += P_t V_j with P_t read from tensor memory.
+//   warps 0-7   two softmax warpgroups, one per query tile, one thread per
+//               score row (TMEM lane = row): scale, mask, running max and
+//               sum in fp32, exponentials with ex2, P written back to tensor
+//               memory as bf16 over the scores it replaces; they also rescale
+//               O when the running max grows and run the epilogue.
+// The issue order S0(j+1) / PV1(j) / S1(j+1) / PV0(j+1) keeps the tensor core
+// busy with one tile while the other tile's softmax runs.
+//
+// Tensor memory (512 columns): S_0 at 0, S_1 at 128 (fp32, 128 keys each;
+// P_t overwrites the first 64 columns of S_t as packed bf16 pairs), O_0 at 256
+// and O_1 at 256 + D (fp32, D columns each).
+//
+// Running max: the softmax keeps using a stale maximum m_used until a new
+// row maximum exceeds it by more than 8 (log2 units), so exp2(x - m_used) <=
+// 256 and O needs rescaling only when the maximum really moves.  Both O and
+// the running sum use the same m_used, so the final O / l is unchanged.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+namespace {
+
+constexpr int kBlockM = 128;     // query rows per tile (= tensor-memory lanes)
+constexpr int kBlockN = 128;     // keys per tile
+constexpr int kBoxBytes = 128 * 128;  // one 64-column (128-byte) box of 128 rows
+constexpr int kThreads = 320;    // 10 warps
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: a factor of 256
+
+template <int D>
+struct Cfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kBlockM * D * 2;
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
+};
+
+struct Bars {
+  uint64_t* q_full;
+  uint64_t* k_full;
+  uint64_t* k_empty;
+  uint64_t* v_full;
+  uint64_t* v_empty;
+  uint64_t* s_full;   // [2]
+  uint64_t* p_full;   // [2]
+  uint64_t* o_full;   // [2]
+  uint64_t* drain;
+};
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms.
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  const uint32_t smem_base = smem_u32(smem);
+
+  uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  Bars bars;
+  bars.q_full = bar_mem;
+  bars.k_full = bar_mem + 1;
+  bars.k_empty = bars.k_full + C::kStages;
+  bars.v_full = bars.k_empty + C::kStages;
+  bars.v_empty = bars.v_full + C::kStages;
+  bars.s_full = bars.v_empty + C::kStages;
+  bars.p_full = bars.s_full + 2;
+  bars.o_full = bars.p_full + 2;
+  bars.drain = bars.o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars.drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const AbortState ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work assignment: longest query blocks first (causal), all heads
+  const int bh_count = p.b * p.h;
+  const int qb = p.num_q_blocks - 1 - static_cast<int>(blockIdx.x) / bh_count;
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int bi = bh / p.h;
+  const int hi = bh % p.h;
+  const bool causal = (p.mask_kind & 1) != 0;
+  int kv_len = p.n_k;
+  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
+    kv_len = p.kv_lengths[bi];
+    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
+  }
+  // Query tile t covers rows [q0 + 128 t, q0 + 128 t + 128); it needs the key
+  // tiles holding at least one visible key.
+  const int q0 = qb * 2 * kBlockM;
+  auto tile_count = [&](int t) {
+    const int qs = q0 + t * kBlockM;
+    int key_end = kv_len;
+    if (causal) key_end = min(key_end, qs + kBlockM);
+    return (qs < p.n_q && key_end > 0) ? (key_end + kBlockN - 1) / kBlockN : 0;
+  };
+  const int n_tiles[2] = {tile_count(0), tile_count(1)};
+  const int n_kv = max(n_tiles[0], n_tiles[1]);
+
+  // ---- set-up: barriers (one thread), tensor memory (MMA warp)
+  if (threadIdx.x == 0) {
+    mbar_init(bars.q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bars.k_full + s, 1);
+      mbar_init(bars.k_empty + s, 1);
+      mbar_init(bars.v_full + s, 1);
+      mbar_init(bars.v_empty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_full + t, 1);
+      mbar_init(bars.p_full + t, kBlockM);
+      mbar_init(bars.o_full + t, 1);
+    }
+    mbar_init(bars.drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_o);
+      uint32_t q_bytes = 0;
+      for (int t = 0; t < 2; ++t) q_bytes += n_tiles[t] > 0 ? C::kTileBytes : 0;
+      if (q_bytes > 0) {
+        mbar_arrive_expect_tx(bars.q_full, q_bytes);
+        for (int t = 0; t < 2; ++t) {
+          if (n_tiles[t] == 0) continue;
+          for (int c = 0; c < C::kBoxes; ++c)
+            tma_load_4d(&p.tm_q, bars.q_full, smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes,
+                        c * 64, q0 + t * kBlockM, hi, bi);
+        }
+      }
+      int k_issued = 0, v_issued = 0;  // tiles whose K (V) copy was started
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t use = static_cast<uint32_t>(j / C::kStages);
+        if (j >= C::kStages && !mbar_wait(bars.k_empty + s, (use - 1) & 1u, ab)) break;
+        mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_4d(&p.tm_k, bars.k_full + s, smem + C::kKOff + s * C::kTileBytes + c * kBoxBytes,
+                      c * 64, j * kBlockN, hi, bi);
+        k_issued = j + 1;
+        if (j >= C::kStages && !mbar_wait(bars.v_empty + s, (use - 1) & 1u, ab)) break;
+        mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_4d(&p.tm_v, bars.v_full + s, smem + C::kVOff + s * C::kTileBytes + c * kBoxBytes,
+                      c * 64, j * kBlockN, hi, bi);
+        v_issued = j + 1;
+      }
+      // Let every copy this thread started land before the CTA can exit.
+      if (q_bytes > 0) mbar_wait_drain(bars.q_full, 0);
+      for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
+        mbar_wait_drain(bars.k_full + j % C::kStages, static_cast<uint32_t>(j / C::kStages) & 1u);
+      for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
+        mbar_wait_drain(bars.v_full + j % C::kStages, static_cast<uint32_t>(j / C::kStages) & 1u);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      const uint32_t q_smem = smem_base + C::kQOff;
+      const uint32_t k_smem = smem_base + C::kKOff;
+      const uint32_t v_smem = smem_base + C::kVOff;
+      auto issue_s = [&](int t, int stage) {
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = static_cast<uint32_t>((k >> 2) * kBoxBytes + (k & 3) * 32);
+          const uint64_t a = smem_desc_sw128(q_smem + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t b = smem_desc_sw128(k_smem + stage * C::kTileBytes + off, 16, 1024);
+          mma_bf16_ss(d_tmem, a, b, C::kIdescS, k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int stage, bool accumulate) {
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(256 + t * D);
+        const uint32_t p_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
+#pragma unroll
+        for (int k = 0; k < kBlockN / 16; ++k) {
+          const uint64_t b = smem_desc_sw128(v_smem + stage * C::kTileBytes + k * 16 * 128,
+                                             kBoxBytes, 1024);
+          mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(k * 8), b, C::kIdescPV,
+                      (accumulate || k > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = mbar_wait(bars.q_full, 0, ab) && mbar_wait(bars.k_full, 0, ab);
+      tc_fence_after();
+      if (ok) {
+        int last_t = n_tiles[1] > 0 ? 1 : 0;
+        for (int t = 0; t < 2; ++t) {
+          if (n_tiles[t] == 0) continue;
+          issue_s(t, 0);
+          mma_commit(bars.s_full + t);
+          if (t == last_t) mma_commit(bars.k_empty);
+        }
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % C::kStages;
+        ok = mbar_wait(bars.v_full + s, static_cast<uint32_t>(j / C::kStages) & 1u, ab);
+        if (!ok) break;
+        tc_fence_after();
+        const int last_pv_t = (j < n_tiles[1]) ? 1 : 0;
+        const int last_s_t = (j + 1 < n_tiles[1]) ? 1 : 0;
+        const int sn = (j + 1) % C::kStages;
+        bool k_next_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j < n_tiles[t]) {
+            ok = mbar_wait(bars.p_full + t, static_cast<uint32_t>(j) & 1u, ab);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            mma_commit(bars.o_full + t);
+            if (t == last_pv_t) mma_commit(bars.v_empty + s);
+          }
+          if (j + 1 < n_tiles[t]) {
+            if (!k_next_ready) {
+              ok = mbar_wait(bars.k_full + sn, static_cast<uint32_t>((j + 1) / C::kStages) & 1u, ab);
+              if (!ok) break;
+              tc_fence_after();
+              k_next_ready = true;
+            }
+            issue_s(t, sn);
+            mma_commit(bars.s_full + t);
+            if (t == last_s_t) mma_commit(bars.k_empty + sn);
+          }
+        }
+      }
+      // Every MMA issued above has finished once this barrier completes.
+      mma_commit(bars.drain);
+      mbar_wait_drain(bars.drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;           // query tile of this warpgroup
+    const int quarter = warp & 3;      // TMEM lane quarter of this warp
+    const int row_in_tile = quarter * 32 + lane;
+    const int q_start_t = q0 + t * kBlockM;
+    const int row = q_start_t + row_in_tile;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t s_col = static_cast<uint32_t>(t * kBlockN);
+    const uint32_t o_col = static_cast<uint32_t>(256 + t * D);
+    const float scale_log2 = p.scale_log2;
+    const int n_t = tile_count(t);
+    const int limit_base = causal ? min(row, kv_len - 1) : kv_len - 1;
+
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_t; ++j) {
+      ok = mbar_wait_warp(bars.s_full + t, static_cast<uint32_t>(j) & 1u, ab);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, sr[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int key0 = j * kBlockN;
+      const bool tile_masked =
+          (key0 + kBlockN > kv_len) || (causal && key0 + kBlockN - 1 > q_start_t);
+      if (tile_masked) {
+        const int lim = limit_base - key0;  // columns > lim are hidden
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_used, mx * scale_log2);
+      // Move the reference maximum only when it grew by more than the
+      // threshold (always on the first tile, where O holds nothing yet).
+      float alpha = 1.f;
+      bool rescale_warp = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        const bool need = m_new > m_used + kRescaleThreshold;
+        rescale_warp = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+          l *= alpha;
+        }
+      }
+      const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+      float rowsum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * e], scale_log2, -m_sub));
+          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * e + 1], scale_log2, -m_sub));
+          rowsum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(lane_base + s_col + half * 32, pk);
+      }
+      // O_t already holds P(j-1) V(j-1): the commit that signalled S_t(j)
+      // covers every MMA issued before it, PV_t(j-1) included.
+      if (rescale_warp) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + o_col + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(lane_base + o_col + c * 32, o);
+        }
+      }
+      l += rowsum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bars.p_full + t);
+    }
+
+    // ---- epilogue: O / l -> bf16 -> swizzled staging (Q_t's smem) -> TMA store.
+    // The branch is uniform over the warpgroup, so all 128 threads reach the
+    // named barrier; a warp whose waits failed skips only its own writes.
+    if (q_start_t < p.n_q) {
+      uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+      bool have_o = ok && n_t > 0;
+      if (have_o) {
+        have_o = mbar_wait_warp(bars.o_full + t, static_cast<uint32_t>(n_t - 1) & 1u, ab);
+        tc_fence_after();
+      }
+      if (have_o || (ok && n_t == 0)) {
+        const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (have_o) {
+            tmem_ld32(lane_base + o_col + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          uint8_t* box = stage + (c >> 1) * kBoxBytes;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+            const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
+            *reinterpret_cast<uint4*>(box + sw128_offset(static_cast<uint32_t>(row_in_tile), chunk)) = v;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1 + t, 128);
+      if (quarter == 0 && lane == 0 && !*abort_flag) {
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_store_4d(&p.tm_o, stage + c * kBoxBytes, c * 64, q_start_t, hi, bi);
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_impl(const SdpaTcParams& p, cudaStream_t stream) {
+  const int smem = Cfg<D>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_bf16_tc<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  sdpa_fwd_bf16_tc<D><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
+  if (head_dim == 64) return launch_impl<64>(p, stream);
+  if (head_dim == 128) return launch_impl<128>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sdpa
