@@ -374,7 +374,7 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=16384,
+    ap.add_argument("--cpu-rows", type=int, default=32768,
                     help="query rows in the oracle's timed CPU sample")
     ap.add_argument("--ref-rows", type=int, default=2048,
                     help="query rows per step of the reference (oracle) arm")

@@ -1,0 +1,74 @@
+"""Runs one attention (or multi-head attention) shape a few times through the
+C ABI, for profiling a single kernel launch under a profiler.
+
+    python -m transformer_scaled_dot_02_gb300.profile --b 4 --h 16 --n 8192 --d 128 --mask 1
+    python -m transformer_scaled_dot_02_gb300.profile --mha --b 32 --n 128 --d-model 512 --h 8
+
+Inputs are seeded N(0,1) bf16 values made on the device; nothing is checked.
+Prints the mean launch time measured with CUDA events.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+import transformer_scaled_dot_02_gb300 as sd
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--b", type=int, default=4)
+    ap.add_argument("--h", type=int, default=16)
+    ap.add_argument("--n", type=int, default=8192, help="query length (and key length)")
+    ap.add_argument("--nk", type=int, default=0, help="key length if different (not causal)")
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--mask", type=int, default=1)
+    ap.add_argument("--len-lo", type=int, default=0, help="padding lengths uniform in [lo, nk]")
+    ap.add_argument("--mha", action="store_true", help="multi-head attention with projections")
+    ap.add_argument("--d-model", type=int, default=512)
+    ap.add_argument("--iters", type=int, default=3)
+    a = ap.parse_args()
+
+    torch.manual_seed(0)
+    dev = torch.device("cuda", 0)
+    n_q = a.n
+    n_k = a.nk or a.n
+    lens = None
+    if a.mask & 2:
+        lo = a.len_lo or n_k // 2
+        lens = torch.randint(lo, n_k + 1, (a.b,), dtype=torch.int32, device=dev)
+    sd.load_library()
+    if a.mha:
+        dm = a.d_model
+        xq = torch.randn(a.b, n_q, dm, device=dev).to(torch.bfloat16)
+        xkv = xq if n_k == n_q else torch.randn(a.b, n_k, dm, device=dev).to(torch.bfloat16)
+        ws = [(torch.randn(*s, device=dev) / s[0] ** 0.5).to(torch.bfloat16)
+              for s in [(dm, a.h * a.d)] * 3 + [(a.h * a.d, dm)]]
+        work = torch.empty(sd.mha_workspace_size(a.b, n_q, n_k, a.h, a.d, a.d), dtype=torch.uint8,
+                           device=dev)
+
+        def run():
+            sd.multi_head_attention(xq, xkv, *ws, a.h, a.mask, lens, workspace=work)
+    else:
+        q = torch.randn(a.b, a.h, n_q, a.d, device=dev).to(torch.bfloat16)
+        k = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
+        v = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q[..., : a.d])
+
+        def run():
+            sd.sdpa_forward(q, k, v, out, a.b, a.h, n_q, n_k, a.d, a.d, a.mask, lens)
+
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(a.iters):
+        run()
+    e.record()
+    torch.cuda.synchronize()
+    sd.sdpa_device_check()
+    print("mean %.4f ms per call over %d calls" % (s.elapsed_time(e) / a.iters, a.iters))
+
+
+if __name__ == "__main__":
+    main()
