@@ -107,6 +107,35 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
                         float scale, void* stream);
 
 /*
+ * mha_forward for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this entry point exists for integration, not for the method.
+ *
+ * Some callers cannot call cudaMalloc, for example code inside a host
+ * framework that owns all device memory through its own pool, or code on a
+ * latency-critical path that must not risk the device-wide synchronisation an
+ * allocation can cause.  This variant takes no workspace: it uses a static
+ * device array of SDPA_MHA_NOALLOC_MAX_WORKSPACE bytes inside the library,
+ * which every GPU that loads the library holds until the process exits.  The
+ * caller still passes (and owns) the inputs and the output, with the same
+ * meaning, layouts and rules as mha_forward.
+ *   - Returns SDPA_ERR_WORKSPACE, before enqueuing anything, when
+ *     mha_workspace_size(b, n_q, n_k, h, d_k, d_v) exceeds
+ *     SDPA_MHA_NOALLOC_MAX_WORKSPACE.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - The first call on each device looks up the array's device address and
+ *     caches it; make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Calls that overlap on the GPU (e.g. on two streams, or from two host
+ *     threads) race on it: order them on one stream or synchronise.
+ */
+#define SDPA_MHA_NOALLOC_MAX_WORKSPACE (32u << 20) /* bytes: 32 MiB */
+
+sdpa_status mha_forward_noalloc(const void* xq, const void* xkv, const void* wq, const void* wk,
+                                const void* wv, const void* wo, void* y, int b, int n_q, int n_k,
+                                int d_model, int h, int d_k, int d_v, int mask_kind,
+                                const int32_t* kv_lengths, float scale, void* stream);
+
+/*
  * One projection of section 3.2.2 on its own: y[m, n] = sum_k x[m, k] w[k, n],
  * x [m, k], w [k, n], y [m, n] bf16 row-major device tensors, fp32
  * accumulation.  k and n must be multiples of 8; m, n, k >= 1.

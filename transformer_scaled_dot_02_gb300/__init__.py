@@ -28,7 +28,10 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
 
 # Every symbol include/sdpa.h declares.
 EXPORTS = ("sdpa_forward", "sdpa_forward_f32", "mha_workspace_size", "mha_forward",
-           "linear_forward", "sdpa_device_check", "sdpa_status_string")
+           "mha_forward_noalloc", "linear_forward", "sdpa_device_check", "sdpa_status_string")
+
+# Size of the static workspace behind mha_forward_noalloc (SDPA_MHA_NOALLOC_MAX_WORKSPACE).
+MHA_NOALLOC_MAX_WORKSPACE = 32 << 20
 
 
 class SdpaError(RuntimeError):
@@ -59,6 +62,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.mha_workspace_size.restype = SZ
     lib.mha_forward.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, I, P, F, P]
     lib.mha_forward.restype = I
+    lib.mha_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, F, P]
+    lib.mha_forward_noalloc.restype = I
     lib.linear_forward.argtypes = [P, P, P, I, I, I, P]
     lib.linear_forward.restype = I
     lib.sdpa_device_check.argtypes = []
@@ -119,6 +124,20 @@ def mha_forward(xq, xkv, wq, wk, wv, wo, y, workspace, ws_bytes, b, n_q, n_k, d_
                                       _addr(wo), _addr(y), _addr(workspace), int(ws_bytes), b, n_q,
                                       n_k, d_model, h, d_k, d_v, mask_kind, _addr(kv_lengths),
                                       float(scale), _stream(stream)), "mha_forward")
+
+
+def mha_forward_noalloc(xq, xkv, wq, wk, wv, wo, y, b, n_q, n_k, d_model, h, d_k, d_v,
+                        mask_kind=SDPA_MASK_NONE, kv_lengths=None, scale=0.0, stream=None) -> None:
+    """mha_forward without a workspace argument, for callers that cannot
+    allocate device memory: the library's static device workspace (at most
+    MHA_NOALLOC_MAX_WORKSPACE bytes) is used instead.  Calls that overlap on
+    the GPU share that workspace and must be ordered by the caller (see
+    include/sdpa.h)."""
+    _check(load_library().mha_forward_noalloc(_addr(xq), _addr(xkv), _addr(wq), _addr(wk),
+                                              _addr(wv), _addr(wo), _addr(y), b, n_q, n_k,
+                                              d_model, h, d_k, d_v, mask_kind, _addr(kv_lengths),
+                                              float(scale), _stream(stream)),
+           "mha_forward_noalloc")
 
 
 def linear_forward(x, w, y, m, n, k, stream=None) -> None:
