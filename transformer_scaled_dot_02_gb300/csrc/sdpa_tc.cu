@@ -13,6 +13,7 @@
 //               shared-memory stages (128-byte swizzle, zero fill past n).
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
 //               then O_t += P_t V_j with P_t read from tensor memory.
+//   warps 10-11 idle (they complete the third warpgroup for the register split).
 //   warps 0-7   two softmax warpgroups, one per query tile, one thread per
 //               score row (TMEM lane = row): scale, mask, running max and
 //               sum in fp32, exponentials with ex2, P written back to tensor
@@ -38,9 +39,15 @@ namespace {
 constexpr int kBlockM = 128;     // query rows per tile (= tensor-memory lanes)
 constexpr int kBlockN = 128;     // keys per tile
 constexpr int kBoxBytes = 128 * 128;  // one 64-column (128-byte) box of 128 rows
-constexpr int kThreads = 320;    // 10 warps
+constexpr int kThreads = 384;    // 12 warps: two softmax warpgroups + one for TMA/MMA
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split: 384 threads launch with 168 registers each; the TMA/MMA
+// warpgroup drops to 64 and the softmax warpgroups rise to 216
+// (128 * 64 + 256 * 216 = 63488 <= 384 * 168 = 64512).
+constexpr uint32_t kRegsControl = 64;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr int kHeadGroup = 8;    // heads whose K/V share L2 at a time
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: a factor of 256
 
@@ -105,10 +112,22 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work assignment: longest query blocks first (causal), all heads
+  // ---- work assignment.  CTAs take heads in groups of kHeadGroup so that the
+  // K/V of the heads in flight stay in L2; inside a group the longest query
+  // blocks (causal) go first.
   const int bh_count = p.b * p.h;
-  const int qb = p.num_q_blocks - 1 - static_cast<int>(blockIdx.x) / bh_count;
-  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int nqb = p.num_q_blocks;
+  const int group_ctas = kHeadGroup * nqb;
+  const int full_groups = bh_count / kHeadGroup;
+  const int idx = static_cast<int>(blockIdx.x);
+  int g = idx / group_ctas, r = idx % group_ctas, heads_in_group = kHeadGroup;
+  if (g >= full_groups) {
+    g = full_groups;
+    r = idx - full_groups * group_ctas;
+    heads_in_group = bh_count - full_groups * kHeadGroup;
+  }
+  const int qb = nqb - 1 - r / heads_in_group;
+  const int bh = g * kHeadGroup + r % heads_in_group;
   const int bi = bh / p.h;
   const int hi = bh % p.h;
   const bool causal = (p.mask_kind & 1) != 0;
@@ -153,7 +172,9 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducerWarp) {
+  if (warp >= 8) {
+   regs_decrease<kRegsControl>();
+   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -201,25 +222,34 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       const uint32_t q_smem = smem_base + C::kQOff;
       const uint32_t k_smem = smem_base + C::kKOff;
       const uint32_t v_smem = smem_base + C::kVOff;
+      // Descriptors split in halves: the high word is fixed by the layout, the
+      // low word holds (address >> 4) and the leading offset; a K step adds
+      // its byte offset >> 4 to the low word (no carry: smem < 256 KB).
+      const uint64_t kq = smem_desc_sw128(q_smem, 16, 1024);
+      const uint64_t kk = smem_desc_sw128(k_smem, 16, 1024);
+      const uint64_t kv = smem_desc_sw128(v_smem, kBoxBytes, 1024);
+      const uint32_t q_lo = static_cast<uint32_t>(kq), qk_hi = static_cast<uint32_t>(kq >> 32);
+      const uint32_t k_lo = static_cast<uint32_t>(kk);
+      const uint32_t v_lo = static_cast<uint32_t>(kv), v_hi = static_cast<uint32_t>(kv >> 32);
       auto issue_s = [&](int t, int stage) {
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
+        const uint32_t a0 = q_lo + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
+        const uint32_t b0 = k_lo + static_cast<uint32_t>((stage * C::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = static_cast<uint32_t>((k >> 2) * kBoxBytes + (k & 3) * 32);
-          const uint64_t a = smem_desc_sw128(q_smem + t * C::kTileBytes + off, 16, 1024);
-          const uint64_t b = smem_desc_sw128(k_smem + stage * C::kTileBytes + off, 16, 1024);
-          mma_bf16_ss(d_tmem, a, b, C::kIdescS, k > 0 ? 1u : 0u);
+          const uint32_t off = static_cast<uint32_t>(((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4);
+          mma_bf16_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int stage, bool accumulate) {
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(256 + t * D);
         const uint32_t p_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
+        const uint32_t b0 = v_lo + static_cast<uint32_t>((stage * C::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k) {
-          const uint64_t b = smem_desc_sw128(v_smem + stage * C::kTileBytes + k * 16 * 128,
-                                             kBoxBytes, 1024);
-          mma_bf16_ts(d_tmem, p_tmem + static_cast<uint32_t>(k * 8), b, C::kIdescPV,
-                      (accumulate || k > 0) ? 1u : 0u);
+          mma_bf16_ts_lohi(d_tmem, p_tmem + static_cast<uint32_t>(k * 8),
+                           b0 + static_cast<uint32_t>((k * 16 * 128) >> 4), v_hi, C::kIdescPV,
+                           (accumulate || k > 0) ? 1u : 0u);
         }
       };
 
@@ -269,7 +299,9 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       mma_commit(bars.drain);
       mbar_wait_drain(bars.drain, 0);
     }
+   }
   } else {
+    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;           // query tile of this warpgroup
     const int quarter = warp & 3;      // TMEM lane quarter of this warp
@@ -309,9 +341,18 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         for (int c = 0; c < 128; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // Row maximum: eight independent chains of three-input max.
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = fmax3(s[i], s[8 + i], s[16 + i]);
+#pragma unroll
+      for (int c = 24; c + 16 <= 120; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], s[120 + i]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float m_new = fmaxf(m_used, mx * scale_log2);
       // Move the reference maximum only when it grew by more than the
       // threshold (always on the first tile, where O holds nothing yet).
@@ -329,19 +370,30 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         }
       }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-      float rowsum = 0.f;
+      // p = exp2(s * scale * log2(e) - m): one packed FMA per pair of scores,
+      // four independent packed partial sums.
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 neg2 = make_float2(-m_sub, -m_sub);
+      float2 acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * e], scale_log2, -m_sub));
-          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * e + 1], scale_log2, -m_sub));
-          rowsum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          const int c = half * 64 + 2 * e;
+          const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, neg2);
+          const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[e & 3] = __fadd2_rn(acc[e & 3], pe);
+          pk[e] = pack_bf16x2(pe.x, pe.y);
         }
         tmem_st32(lane_base + s_col + half * 32, pk);
       }
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      const float rowsum = a.x + a.y;
       // O_t already holds P(j-1) V(j-1): the commit that signalled S_t(j)
       // covers every MMA issued before it, PV_t(j-1) included.
       if (rescale_warp) {
