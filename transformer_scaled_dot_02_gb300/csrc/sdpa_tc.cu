@@ -55,12 +55,14 @@ template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBlockM * D * 2;
-  static constexpr int kStages = (D == 128) ? 2 : 3;
+  // K/V ring depths: Q (2 tiles) + K + V stages fill the 227 KB of shared memory.
+  static constexpr int kKStages = (D == 128) ? 2 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6 + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
@@ -98,10 +100,10 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   Bars bars;
   bars.q_full = bar_mem;
   bars.k_full = bar_mem + 1;
-  bars.k_empty = bars.k_full + C::kStages;
-  bars.v_full = bars.k_empty + C::kStages;
-  bars.v_empty = bars.v_full + C::kStages;
-  bars.s_full = bars.v_empty + C::kStages;
+  bars.k_empty = bars.k_full + C::kKStages;
+  bars.v_full = bars.k_empty + C::kKStages;
+  bars.v_empty = bars.v_full + C::kVStages;
+  bars.s_full = bars.v_empty + C::kVStages;
   bars.p_full = bars.s_full + 2;
   bars.o_full = bars.p_full + 2;
   bars.drain = bars.o_full + 2;
@@ -151,9 +153,11 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   // ---- set-up: barriers (one thread), tensor memory (MMA warp)
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bars.k_full + s, 1);
       mbar_init(bars.k_empty + s, 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bars.v_full + s, 1);
       mbar_init(bars.v_empty + s, 1);
     }
@@ -194,27 +198,29 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K (V) copy was started
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t use = static_cast<uint32_t>(j / C::kStages);
-        if (j >= C::kStages && !mbar_wait(bars.k_empty + s, (use - 1) & 1u, ab)) break;
-        mbar_arrive_expect_tx(bars.k_full + s, C::kTileBytes);
+        const int sk = j % C::kKStages;
+        const uint32_t uk = static_cast<uint32_t>(j / C::kKStages);
+        if (j >= C::kKStages && !mbar_wait(bars.k_empty + sk, (uk - 1) & 1u, ab)) break;
+        mbar_arrive_expect_tx(bars.k_full + sk, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(&p.tm_k, bars.k_full + s, smem + C::kKOff + s * C::kTileBytes + c * kBoxBytes,
-                      c * 64, j * kBlockN, hi, bi);
+          tma_load_4d(&p.tm_k, bars.k_full + sk,
+                      smem + C::kKOff + sk * C::kTileBytes + c * kBoxBytes, c * 64, j * kBlockN, hi, bi);
         k_issued = j + 1;
-        if (j >= C::kStages && !mbar_wait(bars.v_empty + s, (use - 1) & 1u, ab)) break;
-        mbar_arrive_expect_tx(bars.v_full + s, C::kTileBytes);
+        const int sv = j % C::kVStages;
+        const uint32_t uv = static_cast<uint32_t>(j / C::kVStages);
+        if (j >= C::kVStages && !mbar_wait(bars.v_empty + sv, (uv - 1) & 1u, ab)) break;
+        mbar_arrive_expect_tx(bars.v_full + sv, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(&p.tm_v, bars.v_full + s, smem + C::kVOff + s * C::kTileBytes + c * kBoxBytes,
-                      c * 64, j * kBlockN, hi, bi);
+          tma_load_4d(&p.tm_v, bars.v_full + sv,
+                      smem + C::kVOff + sv * C::kTileBytes + c * kBoxBytes, c * 64, j * kBlockN, hi, bi);
         v_issued = j + 1;
       }
       // Let every copy this thread started land before the CTA can exit.
       if (q_bytes > 0) mbar_wait_drain(bars.q_full, 0);
-      for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
-        mbar_wait_drain(bars.k_full + j % C::kStages, static_cast<uint32_t>(j / C::kStages) & 1u);
-      for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
-        mbar_wait_drain(bars.v_full + j % C::kStages, static_cast<uint32_t>(j / C::kStages) & 1u);
+      for (int j = max(0, k_issued - C::kKStages); j < k_issued; ++j)
+        mbar_wait_drain(bars.k_full + j % C::kKStages, static_cast<uint32_t>(j / C::kKStages) & 1u);
+      for (int j = max(0, v_issued - C::kVStages); j < v_issued; ++j)
+        mbar_wait_drain(bars.v_full + j % C::kVStages, static_cast<uint32_t>(j / C::kVStages) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -265,13 +271,13 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         }
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % C::kStages;
-        ok = mbar_wait(bars.v_full + s, static_cast<uint32_t>(j / C::kStages) & 1u, ab);
+        const int s = j % C::kVStages;
+        ok = mbar_wait(bars.v_full + s, static_cast<uint32_t>(j / C::kVStages) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
         const int last_pv_t = (j < n_tiles[1]) ? 1 : 0;
         const int last_s_t = (j + 1 < n_tiles[1]) ? 1 : 0;
-        const int sn = (j + 1) % C::kStages;
+        const int sn = (j + 1) % C::kKStages;
         bool k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (j < n_tiles[t]) {
@@ -284,7 +290,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
           }
           if (j + 1 < n_tiles[t]) {
             if (!k_next_ready) {
-              ok = mbar_wait(bars.k_full + sn, static_cast<uint32_t>((j + 1) / C::kStages) & 1u, ab);
+              ok = mbar_wait(bars.k_full + sn, static_cast<uint32_t>((j + 1) / C::kKStages) & 1u, ab);
               if (!ok) break;
               tc_fence_after();
               k_next_ready = true;
