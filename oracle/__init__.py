@@ -49,6 +49,8 @@ class Oracle:
         lib.oracle_sdpa.restype = I
         lib.oracle_mha.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, D, P, I64, I]
         lib.oracle_mha.restype = I
+        lib.oracle_sdpa_restricted.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, I, D, P, I64, I]
+        lib.oracle_sdpa_restricted.restype = I
         self.lib = lib
         self.path = lib_path
 
@@ -94,11 +96,14 @@ def mha(*args, **kwargs):
     return default().mha(*args, **kwargs)
 
 
-def _sdpa(lib, q, k, v, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, rows=None, threads=None):
+def _sdpa(lib, q, k, v, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, rows=None, threads=None,
+          window=None):
     """Eq. (1) with masks on BHSD arrays q [b,h,n_q,d_k], k [b,h,n_k,d_k], v [b,h,n_k,d_v].
 
     Returns float64 [b,h,n_q,d_v], or [len(rows), d_v] when ``rows`` (flat ids
     (bi*h + hi)*n_q + i) is given.  ``scale`` <= 0 selects 1/sqrt(d_k).
+    ``window`` = r restricts query i to the r keys i - (r-1)//2 .. i + r//2
+    (restricted self-attention, section 4).
     """
     q, k, v = _f32(q), _f32(k), _f32(v)
     b, h, n_q, d_k = q.shape
@@ -112,9 +117,15 @@ def _sdpa(lib, q, k, v, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, rows=No
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         n_rows = rows_arr.size
         out = np.zeros((n_rows, d_v), dtype=np.float64)
-    rc = lib.oracle_sdpa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), b, h, n_q, n_k, d_k, d_v,
+    if window is None:
+        rc = lib.oracle_sdpa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), b, h, n_q, n_k, d_k, d_v,
                              int(mask_kind), _ptr(lens), float(scale), _ptr(rows_arr), n_rows,
                              threads or default_threads())
+    else:
+        rc = lib.oracle_sdpa_restricted(_ptr(q), _ptr(k), _ptr(v), _ptr(out), b, h, n_q, n_k,
+                                        d_k, d_v, int(mask_kind), _ptr(lens), int(window),
+                                        float(scale), _ptr(rows_arr), n_rows,
+                                        threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_sdpa rejected its arguments")
     return out

@@ -19,6 +19,11 @@
  *   sees keys j <= i (its own position included).  A key-padding mask is read
  *   the same way: keys j >= len_b of batch entry b get -infinity.
  *
+ *   Section 4 (restricted self-attention): each output position considers
+ *   only a neighbourhood of size r of the input sequence centred on it.  Read
+ *   here as keys i - floor((r-1)/2) <= j <= i + floor(r/2): exactly r
+ *   positions, symmetric for odd r; it combines with the other masks.
+ *
  *   Section 3.2.2, multi-head attention:
  *       MultiHead(Q, K, V) = Concat(head_1, ..., head_h) W^O,
  *       head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V),
@@ -85,15 +90,17 @@ static void parallel_for(int64_t n, int n_threads, range_fn fn, void* ctx) {
 
 /* ------------------------------------------------------------------------ */
 /* One output row of Eq. (1): q is the query (d_k), K rows at k + j*k_stride, */
-/* V rows at v + j*v_stride; keys j < n_visible_limit are candidates and the */
-/* causal rule (j <= i) is applied when causal != 0.  scores: scratch [n_k]. */
+/* V rows at v + j*v_stride; keys j < len are candidates, the causal rule     */
+/* (j <= i) applies when causal != 0, and keys outside [i - left, i + right] */
+/* are hidden (restricted attention).  scores: scratch [n_k].                */
 static void attention_row(const float* q, const float* k, const float* v, double* out,
                           int64_t k_stride, int64_t v_stride, int n_k, int d_k, int d_v,
-                          int i, int causal, int len, double scale, double* scores) {
+                          int i, int causal, int len, int64_t left, int64_t right,
+                          double scale, double* scores) {
   double m = -INFINITY;
   int any = 0;
   for (int j = 0; j < n_k; ++j) {
-    int visible = (j < len) && !(causal && j > i);
+    int visible = (j < len) && !(causal && j > i) && (j >= i - left) && (j <= i + right);
     if (!visible) { scores[j] = -INFINITY; continue; }
     double dot = 0.0;
     const float* kj = k + (int64_t)j * k_stride;
@@ -135,6 +142,7 @@ typedef struct {
   const int32_t* kv_lengths;
   double scale;
   const int64_t* rows;   /* flat row ids ((bi*h + hi)*n_q + i), or NULL = all */
+  int64_t left, right;    /* restricted-attention reach (unbounded by default) */
 } sdpa_ctx;
 
 static void sdpa_range(void* p, int64_t begin, int64_t end) {
@@ -150,9 +158,24 @@ static void sdpa_range(void* p, int64_t begin, int64_t end) {
     const float* v = c->v + bh * (int64_t)c->n_k * c->d_v;
     int len = clamp_len(c->kv_lengths, c->mask_kind, bi, c->n_k);
     attention_row(q, k, v, c->out + r * c->d_v, c->d_k, c->d_v, c->n_k, c->d_k, c->d_v, i,
-                  (c->mask_kind & ORACLE_MASK_CAUSAL) != 0, len, c->scale, scores);
+                  (c->mask_kind & ORACLE_MASK_CAUSAL) != 0, len, c->left, c->right, c->scale,
+                  scores);
   }
   free(scores);
+}
+
+static int sdpa_common(const float* q, const float* k, const float* v, double* out,
+                       int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                       const int32_t* kv_lengths, double scale, int64_t left, int64_t right,
+                       const int64_t* rows, int64_t n_rows, int n_threads) {
+  if (b < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k < 1 || d_v < 1) return -1;
+  if ((mask_kind & ORACLE_MASK_CAUSAL) && n_q != n_k) return -1;
+  if ((mask_kind & ORACLE_MASK_PADDING) && kv_lengths == NULL) return -1;
+  sdpa_ctx c = {q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths,
+                scale > 0.0 ? scale : 1.0 / sqrt((double)d_k), rows, left, right};
+  int64_t n = rows ? n_rows : (int64_t)b * h * n_q;
+  parallel_for(n, n_threads, sdpa_range, &c);
+  return 0;
 }
 
 /*
@@ -165,14 +188,21 @@ int oracle_sdpa(const float* q, const float* k, const float* v, double* out,
                 int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
                 const int32_t* kv_lengths, double scale,
                 const int64_t* rows, int64_t n_rows, int n_threads) {
-  if (b < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k < 1 || d_v < 1) return -1;
-  if ((mask_kind & ORACLE_MASK_CAUSAL) && n_q != n_k) return -1;
-  if ((mask_kind & ORACLE_MASK_PADDING) && kv_lengths == NULL) return -1;
-  sdpa_ctx c = {q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths,
-                scale > 0.0 ? scale : 1.0 / sqrt((double)d_k), rows};
-  int64_t n = rows ? n_rows : (int64_t)b * h * n_q;
-  parallel_for(n, n_threads, sdpa_range, &c);
-  return 0;
+  return sdpa_common(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths, scale,
+                     INT64_MAX / 4, INT64_MAX / 4, rows, n_rows, n_threads);
+}
+
+/*
+ * Restricted self-attention (section 4): as oracle_sdpa, with each query i
+ * limited to the r keys i - floor((r-1)/2) .. i + floor(r/2).  r >= 1.
+ */
+int oracle_sdpa_restricted(const float* q, const float* k, const float* v, double* out,
+                           int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                           const int32_t* kv_lengths, int r, double scale,
+                           const int64_t* rows, int64_t n_rows, int n_threads) {
+  if (r < 1) return -1;
+  return sdpa_common(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths, scale,
+                     (int64_t)((r - 1) / 2), (int64_t)(r / 2), rows, n_rows, n_threads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -225,9 +225,10 @@ def pin_permutation_equivariance(o):
     assert np.allclose(out_q, ref[:, :, pq], atol=0)
 
 
-def _decimal_attention(q, k, v, mask, lens, scale):
+def _decimal_attention(q, k, v, mask, lens, scale, window=None):
     """Independent brute force: explicit score matrix, softmax as
-    exp(s)/sum(exp(s)) without a max shift, all in 50-digit decimals."""
+    exp(s)/sum(exp(s)) without a max shift, all in 50-digit decimals.
+    ``window`` = r keeps keys i - (r-1)//2 .. i + r//2 (restricted attention)."""
     getcontext().prec = 50
     b, h, n_q, d_k = q.shape
     n_k, d_v = k.shape[2], v.shape[3]
@@ -240,6 +241,8 @@ def _decimal_attention(q, k, v, mask, lens, scale):
             for i in range(n_q):
                 for j in range(n_k):
                     if j >= L or ((mask & MASK_CAUSAL) and j > i):
+                        continue
+                    if window is not None and not (i - (window - 1) // 2 <= j <= i + window // 2):
                         continue
                     S[i][j] = sc * sum(Decimal(float(q[bi, hi, i, c])) * Decimal(float(k[bi, hi, j, c]))
                                        for c in range(d_k))
@@ -370,9 +373,64 @@ def pin_mha_rows_selection(o):
     assert np.array_equal(part, full.reshape(-1, dm)[rows])
 
 
+# ------------------------------------------------------ restricted attention
+def pin_restricted_worked_example(o):
+    """Section 4's neighbourhood of size r around position i, on the worked
+    example's numbers: with r = 2 position 0 sees keys 0 and 1 (weights 3/4,
+    1/4, output 3); with r = 3 and the causal mask position 1 sees keys 0 and
+    1 (output 3) and position 0 sees only itself (output 2)."""
+    g = _golden("worked_example_dk1.json")
+    keys = [_parse_key(s) for s in g["keys"]] + [5.0]
+    vals = g["values"] + [10.0]
+    q = np.ones((1, 1, 3, 1), np.float32)
+    k = _t([[x] for x in keys]).astype(np.float32)
+    v = _t([[x] for x in vals]).astype(np.float32)
+    out = o.sdpa(q, k, v, window=2)
+    assert abs(out[0, 0, 0, 0] - g["output"]) < 1e-6, out
+    w = o.sdpa(q, k, _t(np.eye(3)).astype(np.float32), window=2)
+    assert np.allclose(w[0, 0, 0], g["weights"] + [0.0], atol=1e-6), w
+    outc = o.sdpa(q, k, v, MASK_CAUSAL, window=3)
+    assert outc[0, 0, 0, 0] == g["masked_second_key"]["output"], outc
+    assert abs(outc[0, 0, 1, 0] - g["output"]) < 1e-6, outc
+    e = math.exp(5.0)
+    assert abs(outc[0, 0, 2, 0] - (6.0 + 10.0 * e) / (1.0 + e)) < 1e-5, outc
+
+
+def pin_restricted_extremes(o):
+    """r = 1 keeps only position i (output = V[i]); r covering the whole
+    sequence changes nothing."""
+    rng = np.random.default_rng(30)
+    n = 13
+    q = rng.standard_normal((2, 2, n, 4)).astype(np.float32)
+    k = rng.standard_normal((2, 2, n, 4)).astype(np.float32)
+    v = rng.standard_normal((2, 2, n, 3)).astype(np.float32)
+    one = o.sdpa(q, k, v, window=1)
+    assert np.array_equal(one, v.astype(np.float64))
+    lens = np.array([n, 6], np.int32)
+    for mask in (MASK_NONE, MASK_CAUSAL, MASK_PADDING, MASK_CAUSAL | MASK_PADDING):
+        ln = lens if mask & MASK_PADDING else None
+        assert np.array_equal(o.sdpa(q, k, v, mask, ln, window=2 * n + 1), o.sdpa(q, k, v, mask, ln))
+
+
+def pin_restricted_brute_force(o):
+    rng = np.random.default_rng(31)
+    for (n_q, n_k, d) in [(6, 6, 3), (5, 8, 2)]:
+        q = rng.standard_normal((2, 1, n_q, d)).astype(np.float32)
+        k = rng.standard_normal((2, 1, n_k, d)).astype(np.float32)
+        v = rng.standard_normal((2, 1, n_k, 2)).astype(np.float32)
+        lens = np.array([n_k, 3], np.int32)
+        masks = [MASK_NONE, MASK_PADDING] + ([MASK_CAUSAL, MASK_CAUSAL | MASK_PADDING] if n_q == n_k else [])
+        for mask in masks:
+            for r in (1, 2, 3, 4, 7):
+                ref = _decimal_attention(q, k, v, mask, lens, 0.0, window=r)
+                out = o.sdpa(q, k, v, mask, lens if mask & MASK_PADDING else None, window=r)
+                assert np.allclose(out, ref, rtol=0, atol=1e-13), (n_q, n_k, mask, r)
+
+
 PINS = [pin_worked_example, pin_worked_example_causal, pin_toy_rows, pin_scale_is_inverse_sqrt_dk,
         pin_rows_sum_to_one, pin_equal_scores_give_mean, pin_high_temperature_is_uniform,
         pin_shift_invariance, pin_causal_ignores_future, pin_padding_ignores_masked_keys,
         pin_permutation_equivariance, pin_brute_force, pin_rows_selection,
         pin_mha_single_head_identity, pin_mha_matches_matrix_form, pin_mha_concat_not_average,
-        pin_mha_rows_selection]
+        pin_mha_rows_selection, pin_restricted_worked_example, pin_restricted_extremes,
+        pin_restricted_brute_force]

@@ -34,6 +34,10 @@ MUTANTS = {
     "mha_concat_reversed": ("concat + hi * c->d_v, hdk, hdv,", "concat + (c->h - 1 - hi) * c->d_v, hdk, hdv,"),
     "mha_value_uses_key_weights": ("proj_ctx pv = {xkv + (int64_t)bi * n_k * d_model, wv, vp, d_model, hdv};",
                                    "proj_ctx pv = {xkv + (int64_t)bi * n_k * d_model, wk, vp, d_model, hdv};"),
+    "window_reach_swapped": ("(int64_t)((r - 1) / 2), (int64_t)(r / 2), rows",
+                             "(int64_t)(r / 2), (int64_t)((r - 1) / 2), rows"),
+    "window_left_exclusive": ("(j >= i - left)", "(j > i - left)"),
+    "window_right_exclusive": ("(j <= i + right)", "(j < i + right)"),
     "mha_output_skips_wo": ("yr[o] += concat[t] * (double)wt[o];", "yr[o] += (o == t) ? concat[t] : 0.0;"),
 }
 
