@@ -67,6 +67,21 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
                          void* stream);
 
 /*
+ * Restricted self-attention ("Attention Is All You Need", section 4): each
+ * output position i considers only a neighbourhood of size r of the input
+ * centred on it, read as the keys i - floor((r-1)/2) .. i + floor(r/2)
+ * (exactly r positions; symmetric for odd r).  Tensors, types, masks and
+ * rules as sdpa_forward; the window combines with SDPA_MASK_CAUSAL (which
+ * then leaves keys i - floor((r-1)/2) .. i) and SDPA_MASK_PADDING.  Key tiles
+ * outside every query's window are neither loaded nor multiplied, so the
+ * cost grows as n * r instead of n^2.  r >= 1 (else SDPA_ERR_INVALID_ARG).
+ */
+sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v, void* out,
+                                    int b, int h, int n_q, int n_k, int d_k, int d_v,
+                                    int mask_kind, const int32_t* kv_lengths, int r, float scale,
+                                    void* stream);
+
+/*
  * The same operation in fp32 throughout (fp32 inputs, exact fp32 exponentials
  * and sums on the CUDA cores), for small fp32 problems and the worked
  * examples.  Layouts as sdpa_forward with float elements; any

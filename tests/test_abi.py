@@ -99,6 +99,20 @@ def test_attention_argument_checks(lib, fn):
     assert _attn(lib, fn, scale=float("inf")) == INVALID
 
 
+def test_restricted_argument_checks(lib):
+    def call(**kw):
+        a = dict(q=A, out=A, n_q=16, n_k=16, d=64, mask=0, lens=None, r=3)
+        a.update(kw)
+        return lib.sdpa_forward_restricted(a["q"], A, A, a["out"], 1, 1, a["n_q"], a["n_k"], a["d"],
+                                           a["d"], a["mask"], a["lens"], a["r"], ctypes.c_float(0.0),
+                                           None)
+    assert call(r=0) == INVALID
+    assert call(r=-5) == INVALID
+    assert call(q=None) == INVALID
+    assert call(mask=1, n_k=17) == INVALID
+    assert call(d=32) == UNSUPPORTED
+
+
 def test_unsupported_shapes(lib):
     assert _attn(lib, "sdpa_forward", d_k=32, d_v=32) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=64, d_v=128) == UNSUPPORTED
@@ -144,6 +158,8 @@ def test_linear_argument_checks(lib):
 def test_valid_arguments_without_gpu_report_no_device(lib):
     assert _attn(lib, "sdpa_forward") == NODEV
     assert _attn(lib, "sdpa_forward_f32", d_k=1, d_v=1) == NODEV
+    assert lib.sdpa_forward_restricted(A, A, A, A, 1, 1, 16, 16, 64, 64, 0, None, 3,
+                                       ctypes.c_float(0.0), None) == NODEV
     assert _mha(lib) == NODEV
     assert lib.linear_forward(A, A, A, 4, 8, 8, None) == NODEV
     assert lib.sdpa_device_check() == NODEV

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
                 6: "SDPA_ERR_DEVICE_TIMEOUT"}
 
 # Every symbol include/sdpa.h declares.
-EXPORTS = ("sdpa_forward", "sdpa_forward_f32", "mha_workspace_size", "mha_forward",
+EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_f32", "mha_workspace_size",
+           "mha_forward",
            "mha_forward_noalloc", "linear_forward", "sdpa_device_check", "sdpa_status_string")
 
 # Size of the static workspace behind mha_forward_noalloc (SDPA_MHA_NOALLOC_MAX_WORKSPACE).
@@ -56,6 +57,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     attn = [P, P, P, P, I, I, I, I, I, I, I, P, F, P]
     lib.sdpa_forward.argtypes = attn
     lib.sdpa_forward.restype = I
+    lib.sdpa_forward_restricted.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, I, F, P]
+    lib.sdpa_forward_restricted.restype = I
     lib.sdpa_forward_f32.argtypes = attn
     lib.sdpa_forward_f32.restype = I
     lib.mha_workspace_size.argtypes = [I, I, I, I, I, I]
@@ -103,6 +106,15 @@ def sdpa_forward(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NON
     _check(load_library().sdpa_forward(_addr(q), _addr(k), _addr(v), _addr(out), b, h, n_q, n_k,
                                        d_k, d_v, mask_kind, _addr(kv_lengths), float(scale),
                                        _stream(stream)), "sdpa_forward")
+
+
+def sdpa_forward_restricted(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE,
+                            kv_lengths=None, r=1, scale=0.0, stream=None) -> None:
+    """bf16 restricted self-attention: query i sees keys i-(r-1)//2 .. i+r//2."""
+    _check(load_library().sdpa_forward_restricted(_addr(q), _addr(k), _addr(v), _addr(out), b, h,
+                                                  n_q, n_k, d_k, d_v, mask_kind,
+                                                  _addr(kv_lengths), int(r), float(scale),
+                                                  _stream(stream)), "sdpa_forward_restricted")
 
 
 def sdpa_forward_f32(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE,

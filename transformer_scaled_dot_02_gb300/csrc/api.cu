@@ -126,6 +126,7 @@ sdpa_status check_attention_args(const void* q, const void* k, const void* v, co
       (kv_lengths == nullptr || (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0))
     return SDPA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
+  if (n_q >= sdpa::kWindowUnbounded || n_k >= sdpa::kWindowUnbounded) return SDPA_ERR_UNSUPPORTED;
   // Sizes must stay addressable by the TMA (dimension <= 2^32, strides < 2^40 bytes).
   const long long elems_q = 1ll * b * h * n_q * (d_k > d_v ? d_k : d_v);
   const long long elems_k = 1ll * b * h * n_k * (d_k > d_v ? d_k : d_v);
@@ -144,7 +145,8 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
                                 long long q_sb, long long kv_sn, long long kv_sh, long long kv_sb,
                                 long long o_sn, long long o_sh, long long o_sb, int mask_kind,
                                 const int32_t* kv_lengths, float scale, unsigned* status,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int win_left = sdpa::kWindowUnbounded,
+                                int win_right = sdpa::kWindowUnbounded) {
   SdpaTcParams p;
   if (!make_map_4d(&p.tm_q, q, d, n_q, h, b, q_sn, q_sh, q_sb) ||
       !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb) ||
@@ -160,6 +162,8 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.mask_kind = mask_kind;
   p.num_q_blocks = (n_q + 255) / 256;
   p.scale_log2 = effective_scale(scale, d) * 1.4426950408889634f;
+  p.win_left = win_left;
+  p.win_right = win_right;
   return sdpa::launch_sdpa_tc(p, d, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -194,6 +198,28 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
                              1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
                              1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
                              static_cast<cudaStream_t>(stream));
+}
+
+sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v, void* out,
+                                    int b, int h, int n_q, int n_k, int d_k, int d_v,
+                                    int mask_kind, const int32_t* kv_lengths, int r, float scale,
+                                    void* stream) {
+  sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
+                                        kv_lengths, scale);
+  if (st != SDPA_OK) return st;
+  if (r < 1) return SDPA_ERR_INVALID_ARG;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return SDPA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0) return SDPA_OK;
+  const long long d = d_k;
+  // a neighbourhood of r positions: floor((r-1)/2) before i, floor(r/2) after
+  const int left = (r - 1) / 2, right = r / 2;
+  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d, 1ll * n_q * d,
+                             1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
+                             1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
+                             static_cast<cudaStream_t>(stream), left, right);
 }
 
 sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* out, int b, int h,

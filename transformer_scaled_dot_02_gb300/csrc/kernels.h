@@ -22,7 +22,11 @@ struct SdpaTcParams {
   int mask_kind;
   int num_q_blocks;           // ceil(n_q / 256)
   float scale_log2;           // scale * log2(e)
+  // Restricted attention: query i sees keys [i - win_left, i + win_right]
+  // (kWindowUnbounded for plain attention).
+  int win_left, win_right;
 };
+constexpr int kWindowUnbounded = 1 << 30;
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
 
 // Exact fp32 attention on the CUDA cores, BHSD contiguous.

@@ -138,17 +138,29 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
     kv_len = p.kv_lengths[bi];
     kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
   }
-  // Query tile t covers rows [q0 + 128 t, q0 + 128 t + 128); it needs the key
-  // tiles holding at least one visible key.
+  // Query tile t covers rows [q0 + 128 t, q0 + 128 t + 128).  It needs the key
+  // tiles [lo_of(t), hi_of(t)): those holding at least one key that some
+  // row of the tile can see (causal, padding and restricted-window limits).
   const int q0 = qb * 2 * kBlockM;
-  auto tile_count = [&](int t) {
+  auto tile_range = [&](int t) -> int2 {
     const int qs = q0 + t * kBlockM;
-    int key_end = kv_len;
-    if (causal) key_end = min(key_end, qs + kBlockM);
-    return (qs < p.n_q && key_end > 0) ? (key_end + kBlockN - 1) / kBlockN : 0;
+    if (qs >= p.n_q) return make_int2(0, 0);
+    const int row_hi = min(qs + kBlockM, p.n_q) - 1;
+    int key_lo = max(0, qs - p.win_left);
+    int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
+    if (causal) key_hi = min(key_hi, row_hi + 1);
+    if (key_hi <= key_lo) return make_int2(0, 0);
+    return make_int2(key_lo / kBlockN, (key_hi + kBlockN - 1) / kBlockN);
   };
-  const int n_tiles[2] = {tile_count(0), tile_count(1)};
-  const int n_kv = max(n_tiles[0], n_tiles[1]);
+  const int2 range0 = tile_range(0), range1 = tile_range(1);
+  auto lo_of = [&](int t) { return t ? range1.x : range0.x; };
+  auto hi_of = [&](int t) { return t ? range1.y : range0.y; };
+  const bool has0 = range0.y > range0.x, has1 = range1.y > range1.x;
+  // the CTA walks key tiles [j_first, j_first + n_kv)
+  const int j_first = has0 ? (has1 ? min(range0.x, range1.x) : range0.x) : (has1 ? range1.x : 0);
+  const int j_end = has0 ? (has1 ? max(range0.y, range1.y) : range0.y) : (has1 ? range1.y : 0);
+  const int n_kv = j_end - j_first;
+  auto active = [&](int t, int j) { return j >= lo_of(t) && j < hi_of(t); };
 
   // ---- set-up: barriers (one thread), tensor memory (MMA warp)
   if (threadIdx.x == 0) {
@@ -186,34 +198,36 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_o);
       uint32_t q_bytes = 0;
-      for (int t = 0; t < 2; ++t) q_bytes += n_tiles[t] > 0 ? C::kTileBytes : 0;
+      q_bytes += has0 ? C::kTileBytes : 0;
+      q_bytes += has1 ? C::kTileBytes : 0;
       if (q_bytes > 0) {
         mbar_arrive_expect_tx(bars.q_full, q_bytes);
         for (int t = 0; t < 2; ++t) {
-          if (n_tiles[t] == 0) continue;
+          if (hi_of(t) <= lo_of(t)) continue;
           for (int c = 0; c < C::kBoxes; ++c)
             tma_load_4d(&p.tm_q, bars.q_full, smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes,
                         c * 64, q0 + t * kBlockM, hi, bi);
         }
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K (V) copy was started
-      for (int j = 0; j < n_kv; ++j) {
-        const int sk = j % C::kKStages;
-        const uint32_t uk = static_cast<uint32_t>(j / C::kKStages);
-        if (j >= C::kKStages && !mbar_wait(bars.k_empty + sk, (uk - 1) & 1u, ab)) break;
+      for (int u = 0; u < n_kv; ++u) {
+        const int j = j_first + u;
+        const int sk = u % C::kKStages;
+        const uint32_t uk = static_cast<uint32_t>(u / C::kKStages);
+        if (u >= C::kKStages && !mbar_wait(bars.k_empty + sk, (uk - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(bars.k_full + sk, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(&p.tm_k, bars.k_full + sk,
                       smem + C::kKOff + sk * C::kTileBytes + c * kBoxBytes, c * 64, j * kBlockN, hi, bi);
-        k_issued = j + 1;
-        const int sv = j % C::kVStages;
-        const uint32_t uv = static_cast<uint32_t>(j / C::kVStages);
-        if (j >= C::kVStages && !mbar_wait(bars.v_empty + sv, (uv - 1) & 1u, ab)) break;
+        k_issued = u + 1;
+        const int sv = u % C::kVStages;
+        const uint32_t uv = static_cast<uint32_t>(u / C::kVStages);
+        if (u >= C::kVStages && !mbar_wait(bars.v_empty + sv, (uv - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(bars.v_full + sv, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(&p.tm_v, bars.v_full + sv,
                       smem + C::kVOff + sv * C::kTileBytes + c * kBoxBytes, c * 64, j * kBlockN, hi, bi);
-        v_issued = j + 1;
+        v_issued = u + 1;
       }
       // Let every copy this thread started land before the CTA can exit.
       if (q_bytes > 0) mbar_wait_drain(bars.q_full, 0);
@@ -262,35 +276,39 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       bool ok = mbar_wait(bars.q_full, 0, ab) && mbar_wait(bars.k_full, 0, ab);
       tc_fence_after();
       if (ok) {
-        int last_t = n_tiles[1] > 0 ? 1 : 0;
+        const int last_t = active(1, j_first) ? 1 : 0;
         for (int t = 0; t < 2; ++t) {
-          if (n_tiles[t] == 0) continue;
+          if (!active(t, j_first)) continue;
           issue_s(t, 0);
           mma_commit(bars.s_full + t);
           if (t == last_t) mma_commit(bars.k_empty);
         }
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % C::kVStages;
-        ok = mbar_wait(bars.v_full + s, static_cast<uint32_t>(j / C::kVStages) & 1u, ab);
+      for (int u = 0; ok && u < n_kv; ++u) {
+        const int j = j_first + u;
+        const int s = u % C::kVStages;
+        ok = mbar_wait(bars.v_full + s, static_cast<uint32_t>(u / C::kVStages) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
-        const int last_pv_t = (j < n_tiles[1]) ? 1 : 0;
-        const int last_s_t = (j + 1 < n_tiles[1]) ? 1 : 0;
-        const int sn = (j + 1) % C::kKStages;
+        const bool pv_any = active(0, j) || active(1, j);
+        const bool s_any = active(0, j + 1) || active(1, j + 1);
+        const int last_pv_t = active(1, j) ? 1 : 0;
+        const int last_s_t = active(1, j + 1) ? 1 : 0;
+        const int sn = (u + 1) % C::kKStages;
+        const uint32_t kn_phase = static_cast<uint32_t>((u + 1) / C::kKStages) & 1u;
         bool k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j < n_tiles[t]) {
-            ok = mbar_wait(bars.p_full + t, static_cast<uint32_t>(j) & 1u, ab);
+          if (active(t, j)) {
+            ok = mbar_wait(bars.p_full + t, static_cast<uint32_t>(j - lo_of(t)) & 1u, ab);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, s, j > 0);
+            issue_pv(t, s, j > lo_of(t));
             mma_commit(bars.o_full + t);
             if (t == last_pv_t) mma_commit(bars.v_empty + s);
           }
-          if (j + 1 < n_tiles[t]) {
+          if (active(t, j + 1)) {
             if (!k_next_ready) {
-              ok = mbar_wait(bars.k_full + sn, static_cast<uint32_t>((j + 1) / C::kKStages) & 1u, ab);
+              ok = mbar_wait(bars.k_full + sn, kn_phase, ab);
               if (!ok) break;
               tc_fence_after();
               k_next_ready = true;
@@ -299,6 +317,13 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
             mma_commit(bars.s_full + t);
             if (t == last_s_t) mma_commit(bars.k_empty + sn);
           }
+        }
+        // A key tile inside the walked range that no query tile uses is still
+        // released, so the producer's ring keeps turning.
+        if (ok && !pv_any) mma_commit(bars.v_empty + s);
+        if (ok && !s_any && u + 1 < n_kv) {
+          ok = mbar_wait(bars.k_full + sn, kn_phase, ab);
+          if (ok) mma_commit(bars.k_empty + sn);
         }
       }
       // Every MMA issued above has finished once this barrier completes.
@@ -318,14 +343,18 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
     const uint32_t s_col = static_cast<uint32_t>(t * kBlockN);
     const uint32_t o_col = static_cast<uint32_t>(256 + t * D);
     const float scale_log2 = p.scale_log2;
-    const int n_t = tile_count(t);
-    const int limit_base = causal ? min(row, kv_len - 1) : kv_len - 1;
+    const int t_lo = lo_of(t), t_hi = hi_of(t);
+    const int n_t = t_hi - t_lo;
+    // visible keys of this row: [lo_lim, hi_lim]
+    const int lo_lim = row - p.win_left;
+    const int hi_lim = min(kv_len - 1, causal ? row : row + min(p.win_right, p.n_k));
 
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_t; ++j) {
-      ok = mbar_wait_warp(bars.s_full + t, static_cast<uint32_t>(j) & 1u, ab);
+    for (int j = t_lo; j < t_hi; ++j) {
+      const uint32_t it = static_cast<uint32_t>(j - t_lo);   // this tile's iteration
+      ok = mbar_wait_warp(bars.s_full + t, it & 1u, ab);
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
@@ -339,13 +368,15 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
       const int key0 = j * kBlockN;
-      const bool tile_masked =
-          (key0 + kBlockN > kv_len) || (causal && key0 + kBlockN - 1 > q_start_t);
+      const bool tile_masked = (key0 + kBlockN > kv_len) ||
+                               (causal && key0 + kBlockN - 1 > q_start_t) ||
+                               (key0 + kBlockN - 1 > q_start_t + p.win_right) ||
+                               (key0 < q_start_t + kBlockM - 1 - p.win_left);
       if (tile_masked) {
-        const int lim = limit_base - key0;  // columns > lim are hidden
+        const int lo = lo_lim - key0, hi_c = hi_lim - key0;  // visible columns [lo, hi_c]
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (c > lim) s[c] = -INFINITY;
+          if (c < lo || c > hi_c) s[c] = -INFINITY;
       }
       // Row maximum: eight independent chains of three-input max.
       float mx8[8];
@@ -364,7 +395,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       // threshold (always on the first tile, where O holds nothing yet).
       float alpha = 1.f;
       bool rescale_warp = false;
-      if (j == 0) {
+      if (it == 0) {
         m_used = m_new;
       } else {
         const bool need = m_new > m_used + kRescaleThreshold;
