@@ -51,6 +51,8 @@ class Oracle:
         lib.oracle_mha.restype = I
         lib.oracle_sdpa_restricted.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, I, D, P, I64, I]
         lib.oracle_sdpa_restricted.restype = I
+        lib.oracle_sdpa_decode.argtypes = [P, P, P, P, I, I, I, I, I, I, P, D, P, I64, I]
+        lib.oracle_sdpa_decode.restype = I
         self.lib = lib
         self.path = lib_path
 
@@ -59,6 +61,9 @@ class Oracle:
 
     def mha(self, *args, **kwargs):
         return _mha(self.lib, *args, **kwargs)
+
+    def decode(self, *args, **kwargs):
+        return _decode(self.lib, *args, **kwargs)
 
 
 _default: Oracle | None = None
@@ -94,6 +99,34 @@ def sdpa(*args, **kwargs):
 def mha(*args, **kwargs):
     """Multi-head attention; see ``_mha``.  Uses the library built from oracle.c."""
     return default().mha(*args, **kwargs)
+
+
+def decode(*args, **kwargs):
+    """One decoding step over a cache; see ``_decode``."""
+    return default().decode(*args, **kwargs)
+
+
+def _decode(lib, q, k, v, kv_lengths=None, scale=0.0, rows=None, threads=None):
+    """n_q new queries q [b,h,n_q,d_k] against caches k [b,h,n_k,d_k], v [b,h,n_k,d_v]
+    of lengths kv_lengths [b] (None: n_k).  Query i sees keys j <= len_b - n_q + i.
+    Returns float64 [b,h,n_q,d_v] (or [len(rows), d_v])."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    b, h, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    lens = None if kv_lengths is None else np.ascontiguousarray(kv_lengths, dtype=np.int32)
+    if rows is None:
+        out = np.zeros((b, h, n_q, d_v), dtype=np.float64)
+        rows_arr, n_rows = None, 0
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows = rows_arr.size
+        out = np.zeros((n_rows, d_v), dtype=np.float64)
+    rc = lib.oracle_sdpa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(out), b, h, n_q, n_k, d_k, d_v,
+                                _ptr(lens), float(scale), _ptr(rows_arr), n_rows,
+                                threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_sdpa_decode rejected its arguments")
+    return out
 
 
 def _sdpa(lib, q, k, v, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, rows=None, threads=None,

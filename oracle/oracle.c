@@ -24,6 +24,13 @@
  *   here as keys i - floor((r-1)/2) <= j <= i + floor(r/2): exactly r
  *   positions, symmetric for odd r; it combines with the other masks.
  *
+ *   Autoregressive decoding (section 3.1: the decoder generates one symbol at
+ *   a time, consuming the symbols generated so far): a decoding step attends
+ *   n_q new queries to the cached keys and values.  Read here as: the new
+ *   queries are the last n_q positions of each sequence's cache of length
+ *   len_b, so query i sits at position len_b - n_q + i and, by the causal
+ *   rule, sees keys j <= len_b - n_q + i.
+ *
  *   Section 3.2.2, multi-head attention:
  *       MultiHead(Q, K, V) = Concat(head_1, ..., head_h) W^O,
  *       head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V),
@@ -203,6 +210,63 @@ int oracle_sdpa_restricted(const float* q, const float* k, const float* v, doubl
   if (r < 1) return -1;
   return sdpa_common(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths, scale,
                      (int64_t)((r - 1) / 2), (int64_t)(r / 2), rows, n_rows, n_threads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* One decoding step over a key/value cache.                                  */
+typedef struct {
+  const float *q, *k, *v;
+  double* out;
+  int h, n_q, n_k, d_k, d_v;
+  const int32_t* kv_lengths;
+  double scale;
+  const int64_t* rows;
+} decode_ctx;
+
+static void decode_range(void* p, int64_t begin, int64_t end) {
+  decode_ctx* c = (decode_ctx*)p;
+  double* scores = (double*)malloc(sizeof(double) * (size_t)(c->n_k > 0 ? c->n_k : 1));
+  for (int64_t r = begin; r < end; ++r) {
+    int64_t flat = c->rows ? c->rows[r] : r;
+    int i = (int)(flat % c->n_q);
+    int64_t bh = flat / c->n_q;
+    int bi = (int)(bh / c->h);
+    int len = clamp_len(c->kv_lengths, ORACLE_MASK_PADDING, bi, c->n_k);
+    int pos = len - c->n_q + i;   /* position of this query in its sequence */
+    const float* q = c->q + flat * c->d_k;
+    const float* k = c->k + bh * (int64_t)c->n_k * c->d_k;
+    const float* v = c->v + bh * (int64_t)c->n_k * c->d_v;
+    if (pos < 0) {                 /* the query lies before the cache: nothing visible */
+      for (int cc = 0; cc < c->d_v; ++cc) c->out[r * c->d_v + cc] = 0.0;
+      continue;
+    }
+    attention_row(q, k, v, c->out + r * c->d_v, c->d_k, c->d_v, c->n_k, c->d_k, c->d_v, pos,
+                  1, len, INT64_MAX / 4, INT64_MAX / 4, c->scale, scores);
+  }
+  free(scores);
+}
+
+/*
+ * Decoding step: q [b,h,n_q,d_k] new queries, k [b,h,n_k,d_k] and
+ * v [b,h,n_k,d_v] caches, kv_lengths int32 [b] cache lengths (NULL: all
+ * n_k).  Query i sees keys j <= len_b - n_q + i.  Output as oracle_sdpa.
+ */
+int oracle_sdpa_decode(const float* q, const float* k, const float* v, double* out,
+                       int b, int h, int n_q, int n_k, int d_k, int d_v,
+                       const int32_t* kv_lengths, double scale,
+                       const int64_t* rows, int64_t n_rows, int n_threads) {
+  if (b < 0 || h < 0 || n_q < 1 || n_k < 0 || d_k < 1 || d_v < 1) return -1;
+  int32_t* lens = NULL;
+  if (kv_lengths == NULL) {
+    lens = (int32_t*)malloc(sizeof(int32_t) * (size_t)(b > 0 ? b : 1));
+    for (int i = 0; i < b; ++i) lens[i] = n_k;
+  }
+  decode_ctx c = {q, k, v, out, h, n_q, n_k, d_k, d_v, kv_lengths ? kv_lengths : lens,
+                  scale > 0.0 ? scale : 1.0 / sqrt((double)d_k), rows};
+  int64_t n = rows ? n_rows : (int64_t)b * h * n_q;
+  parallel_for(n, n_threads, decode_range, &c);
+  free(lens);
+  return 0;
 }
 
 /* ------------------------------------------------------------------------ */

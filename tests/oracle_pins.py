@@ -427,10 +427,53 @@ def pin_restricted_brute_force(o):
                 assert np.allclose(out, ref, rtol=0, atol=1e-13), (n_q, n_k, mask, r)
 
 
+# ---------------------------------------------------------------- decoding
+def pin_decode_matches_causal_rows(o):
+    """A decoding step of n_q queries over a cache of length n equals the last
+    n_q rows of causal self-attention over the full sequence; one query over
+    the whole cache equals unmasked attention of that query."""
+    rng = np.random.default_rng(40)
+    n, d = 11, 4
+    q = rng.standard_normal((2, 2, n, d)).astype(np.float32)
+    k = rng.standard_normal((2, 2, n, d)).astype(np.float32)
+    v = rng.standard_normal((2, 2, n, 3)).astype(np.float32)
+    full = o.sdpa(q, k, v, MASK_CAUSAL)
+    for n_q in (1, 3, n):
+        dec = o.decode(q[:, :, n - n_q:], k, v)
+        assert np.array_equal(dec, full[:, :, n - n_q:]), n_q
+    one = o.decode(q[:, :, 4:5], k, v)
+    assert np.array_equal(one, o.sdpa(q[:, :, 4:5], k, v))
+
+
+def pin_decode_cache_lengths(o):
+    """Per-sequence cache lengths: keys past len_b are ignored; a query placed
+    before the cache start sees nothing (zeros); the worked example as a
+    one-query step over a two-entry cache gives 3."""
+    rng = np.random.default_rng(41)
+    n, d = 9, 3
+    q = rng.standard_normal((3, 1, 2, d)).astype(np.float32)
+    k = rng.standard_normal((3, 1, n, d)).astype(np.float32)
+    v = rng.standard_normal((3, 1, n, 2)).astype(np.float32)
+    lens = np.array([5, 1, 0], np.int32)
+    dec = o.decode(q, k, v, lens)
+    ref0 = o.sdpa(q[:1], k[:1, :, :5], v[:1, :, :5], MASK_NONE)    # both queries see keys < 5 ...
+    ref0c = o.decode(q[:1], k[:1, :, :5], v[:1, :, :5])            # ... with the causal shift
+    assert np.array_equal(dec[0], ref0c[0])
+    assert np.array_equal(dec[0, :, 1], ref0[0, :, 1])             # last query sees the whole cache
+    assert np.array_equal(dec[1, :, 0], np.zeros((1, 2)))          # position -1: nothing
+    assert np.allclose(dec[1, :, 1], v[1, :, 0], atol=0)           # position 0: key 0 only
+    assert np.array_equal(dec[2], np.zeros_like(dec[2]))
+    g = _golden("worked_example_dk1.json")
+    kk = _t([[_parse_key(x)] for x in g["keys"]]).astype(np.float32)
+    vv = _t([[x] for x in g["values"]]).astype(np.float32)
+    w = o.decode(_t([g["q"]]).astype(np.float32), kk, vv)
+    assert abs(w[0, 0, 0, 0] - g["output"]) < 1e-6
+
+
 PINS = [pin_worked_example, pin_worked_example_causal, pin_toy_rows, pin_scale_is_inverse_sqrt_dk,
         pin_rows_sum_to_one, pin_equal_scores_give_mean, pin_high_temperature_is_uniform,
         pin_shift_invariance, pin_causal_ignores_future, pin_padding_ignores_masked_keys,
         pin_permutation_equivariance, pin_brute_force, pin_rows_selection,
         pin_mha_single_head_identity, pin_mha_matches_matrix_form, pin_mha_concat_not_average,
         pin_mha_rows_selection, pin_restricted_worked_example, pin_restricted_extremes,
-        pin_restricted_brute_force]
+        pin_restricted_brute_force, pin_decode_matches_causal_rows, pin_decode_cache_lengths]

@@ -38,6 +38,8 @@ MUTANTS = {
                              "(int64_t)(r / 2), (int64_t)((r - 1) / 2), rows"),
     "window_left_exclusive": ("(j >= i - left)", "(j > i - left)"),
     "window_right_exclusive": ("(j <= i + right)", "(j < i + right)"),
+    "decode_position_unshifted": ("int pos = len - c->n_q + i;", "int pos = i;"),
+    "decode_position_off_by_one": ("int pos = len - c->n_q + i;", "int pos = len - c->n_q + i + 1;"),
     "mha_output_skips_wo": ("yr[o] += concat[t] * (double)wt[o];", "yr[o] += (o == t) ? concat[t] : 0.0;"),
 }
 
