@@ -93,6 +93,30 @@ sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* 
                              void* stream);
 
 /*
+ * One autoregressive decoding step ("Attention Is All You Need", section 3.1:
+ * the decoder generates one symbol at a time): 1 <= n_q <= 8 new queries per
+ * (batch, head) against cached keys and values.
+ *   q   [b, h, n_q, d_k]  bf16, device (the new queries)
+ *   k   [b, h, n_k, d_k]  bf16, device (key cache, capacity n_k)
+ *   v   [b, h, n_k, d_v]  bf16, device (value cache)
+ *   out [b, h, n_q, d_v]  bf16, device, written
+ *   kv_lengths: device int32 [b], the filled length len_b of each cache
+ *   (clamped into [0, n_k]), or NULL for n_k.  The new queries are the last
+ *   n_q positions of each sequence, so query i sees keys j <= len_b - n_q + i
+ *   (the causal rule of section 3.2.3); a query with no visible key gives 0.
+ *   workspace: device buffer of ws_bytes >= sdpa_decode_workspace_size(...)
+ *   (may be NULL when that size is 0), 16-byte aligned, caller-owned.
+ * The step is bound by reading the caches once from HBM; it runs on the CUDA
+ * cores with the cache split across CTAs and a merge of the partial softmax
+ * states.  Supported: d_k == d_v in {64, 128}, b * h <= 65535.
+ */
+size_t sdpa_decode_workspace_size(int b, int h, int n_q, int n_k, int d_v);
+
+sdpa_status sdpa_decode(const void* q, const void* k, const void* v, void* out, void* workspace,
+                        size_t ws_bytes, int b, int h, int n_q, int n_k, int d_k, int d_v,
+                        const int32_t* kv_lengths, float scale, void* stream);
+
+/*
  * Bytes of device workspace mha_forward needs: the projected Q [b*n_q, h*d_k],
  * K [b*n_k, h*d_k], V [b*n_k, h*d_v] and the concatenated heads
  * [b*n_q, h*d_v], bf16, each rounded up to 256 bytes.  Returns 0 for

@@ -113,6 +113,27 @@ def test_restricted_argument_checks(lib):
     assert call(d=32) == UNSUPPORTED
 
 
+def test_decode_argument_checks(lib):
+    def call(**kw):
+        a = dict(q=A, out=A, ws=A, ws_bytes=1 << 30, b=2, h=2, n_q=1, n_k=4096, d=128, lens=None)
+        a.update(kw)
+        return lib.sdpa_decode(a["q"], A, A, a["out"], a["ws"], a["ws_bytes"], a["b"], a["h"],
+                               a["n_q"], a["n_k"], a["d"], a["d"], a["lens"], ctypes.c_float(0.0),
+                               None)
+    assert call(q=None) == INVALID
+    assert call(out=MIS) == INVALID
+    assert call(n_q=0) == INVALID
+    assert call(lens=A + 2) == INVALID
+    assert call(n_q=9) == UNSUPPORTED
+    assert call(d=96) == UNSUPPORTED
+    need = sd.sdpa_decode_workspace_size(2, 2, 1, 4096, 128)
+    assert need > 0
+    assert call(ws=None) == WORKSPACE
+    assert call(ws_bytes=need - 1) == WORKSPACE
+    # a short cache needs no workspace: one split
+    assert sd.sdpa_decode_workspace_size(1024, 16, 1, 256, 128) == 0
+
+
 def test_unsupported_shapes(lib):
     assert _attn(lib, "sdpa_forward", d_k=32, d_v=32) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=64, d_v=128) == UNSUPPORTED
@@ -162,4 +183,6 @@ def test_valid_arguments_without_gpu_report_no_device(lib):
                                        ctypes.c_float(0.0), None) == NODEV
     assert _mha(lib) == NODEV
     assert lib.linear_forward(A, A, A, 4, 8, 8, None) == NODEV
+    assert lib.sdpa_decode(A, A, A, A, A, 1 << 30, 2, 2, 1, 4096, 128, 128, None,
+                           ctypes.c_float(0.0), None) == NODEV
     assert lib.sdpa_device_check() == NODEV

@@ -1,0 +1,73 @@
+"""One decoding step over a K/V cache (split across CTAs on the CUDA cores)
+against the oracle, tolerance 2e-2 of the output scale."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import transformer_scaled_dot_02_gb300 as sd
+from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(rng, shape, std=1.0):
+    return synthetic.round_to_bf16(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+def _gpu(q, k, v, lens=None, scale=0.0):
+    out = sd.decode_step(dev(q), dev(k), dev(v), None if lens is None else dev_int(lens), scale)
+    sd.sdpa_device_check()
+    return host(out)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n_q", [1, 2, 4, 5, 8])
+@pytest.mark.parametrize("b,h,n_k", [(1, 1, 1), (2, 3, 37), (4, 2, 1000), (1, 4, 5000)])
+def test_decode_shapes(d, n_q, b, h, n_k):
+    rng = np.random.default_rng(9000 + d + 10 * n_q + n_k)
+    q, k, v = _rand(rng, (b, h, n_q, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+    lens = rng.integers(0, n_k + 1, size=b).astype(np.int32)
+    lens[0] = n_k
+    got = _gpu(q, k, v, lens)
+    ref = oracle.decode(q, k, v, lens)
+    assert rel_err(got, ref) <= TOL_BF16
+    got_full = _gpu(q, k, v, None)
+    assert rel_err(got_full, oracle.decode(q, k, v)) <= TOL_BF16
+
+
+def test_decode_edge_lengths():
+    """Cache lengths 0 (nothing visible), shorter than n_q (early queries see
+    nothing), one, and beyond n_k (clamped)."""
+    rng = np.random.default_rng(91)
+    b, h, n_q, n_k, d = 5, 2, 4, 700, 128
+    q, k, v = _rand(rng, (b, h, n_q, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+    lens = np.array([0, 2, 1, 699, 5000], np.int32)
+    got = _gpu(q, k, v, lens)
+    ref = oracle.decode(q, k, v, lens)
+    assert np.array_equal(got[0], np.zeros_like(got[0]))
+    assert np.array_equal(got[1, :, :2], np.zeros_like(got[1, :, :2]))
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_decode_matches_causal_attention_rows():
+    """The last n_q rows of causal self-attention equal a decoding step."""
+    rng = np.random.default_rng(92)
+    b, h, n, d, n_q = 2, 4, 640, 64, 3
+    q, k, v = _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n, d))
+    full = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL))
+    step = _gpu(q[:, :, n - n_q:], k, v)
+    assert rel_err(step, full[:, :, n - n_q:]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("n_q", [1, 4])
+def test_decode_workload(n_q):
+    """Decoding step at serving size: 32 sequences, 16 heads, d=128, caches of
+    8192 positions filled to lengths in [4096, 8192]."""
+    rng = np.random.default_rng(93 + n_q)
+    b, h, n_k, d = 32, 16, 8192, 128
+    q, k, v = _rand(rng, (b, h, n_q, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+    lens = rng.integers(4096, n_k + 1, size=b).astype(np.int32)
+    got = _gpu(q, k, v, lens)
+    ref = oracle.decode(q, k, v, lens)
+    assert rel_err(got, ref) <= TOL_BF16

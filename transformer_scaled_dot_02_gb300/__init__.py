@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
                 6: "SDPA_ERR_DEVICE_TIMEOUT"}
 
 # Every symbol include/sdpa.h declares.
-EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_f32", "mha_workspace_size",
+EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_f32",
+           "sdpa_decode_workspace_size", "sdpa_decode", "mha_workspace_size",
            "mha_forward",
            "mha_forward_noalloc", "linear_forward", "sdpa_device_check", "sdpa_status_string")
 
@@ -61,6 +62,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sdpa_forward_restricted.restype = I
     lib.sdpa_forward_f32.argtypes = attn
     lib.sdpa_forward_f32.restype = I
+    lib.sdpa_decode_workspace_size.argtypes = [I, I, I, I, I]
+    lib.sdpa_decode_workspace_size.restype = SZ
+    lib.sdpa_decode.argtypes = [P, P, P, P, P, SZ, I, I, I, I, I, I, P, F, P]
+    lib.sdpa_decode.restype = I
     lib.mha_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.mha_workspace_size.restype = SZ
     lib.mha_forward.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, I, P, F, P]
@@ -123,6 +128,33 @@ def sdpa_forward_f32(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK
     _check(load_library().sdpa_forward_f32(_addr(q), _addr(k), _addr(v), _addr(out), b, h, n_q,
                                            n_k, d_k, d_v, mask_kind, _addr(kv_lengths),
                                            float(scale), _stream(stream)), "sdpa_forward_f32")
+
+
+def sdpa_decode_workspace_size(b, h, n_q, n_k, d_v) -> int:
+    return int(load_library().sdpa_decode_workspace_size(b, h, n_q, n_k, d_v))
+
+
+def sdpa_decode(q, k, v, out, workspace, ws_bytes, b, h, n_q, n_k, d_k, d_v, kv_lengths=None,
+                scale=0.0, stream=None) -> None:
+    """One decoding step over bf16 K/V caches (see include/sdpa.h)."""
+    _check(load_library().sdpa_decode(_addr(q), _addr(k), _addr(v), _addr(out), _addr(workspace),
+                                      int(ws_bytes), b, h, n_q, n_k, d_k, d_v, _addr(kv_lengths),
+                                      float(scale), _stream(stream)), "sdpa_decode")
+
+
+def decode_step(q, k, v, kv_lengths=None, scale=0.0, workspace=None, stream=None):
+    """Allocates the output (and, if needed, the workspace) with torch and
+    calls sdpa_decode on q [b,h,n_q,d], k/v [b,h,n_k,d] bf16 tensors."""
+    import torch
+    b, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    need = sdpa_decode_workspace_size(b, h, n_q, n_k, d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    out = torch.empty((b, h, n_q, d), dtype=q.dtype, device=q.device)
+    sdpa_decode(q, k, v, out, workspace, 0 if workspace is None else workspace.numel(), b, h, n_q,
+                n_k, d, d, kv_lengths, scale, stream)
+    return out
 
 
 def mha_workspace_size(b, n_q, n_k, h, d_k, d_v) -> int:

@@ -252,6 +252,59 @@ sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* 
              : SDPA_ERR_CUDA;
 }
 
+size_t sdpa_decode_workspace_size(int b, int h, int n_q, int n_k, int d_v) {
+  if (b < 1 || h < 1 || n_q < 1 || n_k < 0 || d_v < 1) return 0;
+  const int splits = sdpa::decode_splits(b, h, n_k);
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(b) * h * n_q;
+  return round256(static_cast<size_t>(splits) * rows * d_v * 4) +
+         round256(static_cast<size_t>(splits) * rows * 2 * 4);
+}
+
+sdpa_status sdpa_decode(const void* q, const void* k, const void* v, void* out, void* workspace,
+                        size_t ws_bytes, int b, int h, int n_q, int n_k, int d_k, int d_v,
+                        const int32_t* kv_lengths, float scale, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return SDPA_ERR_INVALID_ARG;
+  if (b < 1 || h < 1 || n_q < 1 || n_k < 0 || d_k < 1 || d_v < 1) return SDPA_ERR_INVALID_ARG;
+  if (kv_lengths != nullptr && (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0)
+    return SDPA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
+  if (d_k != d_v || (d_k != 64 && d_k != 128) || n_q > sdpa::kDecodeMaxQueries ||
+      1ll * b * h > 65535 || n_k >= sdpa::kWindowUnbounded)
+    return SDPA_ERR_UNSUPPORTED;
+  const size_t need = sdpa_decode_workspace_size(b, h, n_q, n_k, d_v);
+  if (need > 0 && (workspace == nullptr || !aligned16(workspace) || ws_bytes < need))
+    return SDPA_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  sdpa_status st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  sdpa::DecodeParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.out = static_cast<uint16_t*>(out);
+  p.kv_lengths = kv_lengths;
+  p.b = b;
+  p.h = h;
+  p.n_q = n_q;
+  p.n_k = n_k;
+  p.splits = sdpa::decode_splits(b, h, n_k);
+  const int per = (n_k + p.splits - 1) / p.splits;
+  p.keys_per_split = ((per + 7) / 8) * 8;
+  const size_t rows = static_cast<size_t>(b) * h * n_q;
+  p.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
+  p.part_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                  round256(static_cast<size_t>(p.splits) * rows *
+                                                           d_v * 4))
+                       : nullptr;
+  p.scale_log2 = effective_scale(scale, d_k) * 1.4426950408889634f;
+  return sdpa::launch_sdpa_decode(p, d_k, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
+}
+
 size_t mha_workspace_size(int b, int n_q, int n_k, int h, int d_k, int d_v) {
   if (b < 0 || n_q < 0 || n_k < 0 || h < 0 || d_k < 0 || d_v < 0) return 0;
   const size_t bq = static_cast<size_t>(b) * n_q, bk = static_cast<size_t>(b) * n_k;

@@ -29,6 +29,24 @@ struct SdpaTcParams {
 constexpr int kWindowUnbounded = 1 << 30;
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
 
+// One decoding step over a K/V cache on the CUDA cores, split across CTAs.
+struct DecodeParams {
+  const uint16_t *q, *k, *v;  // bf16 BHSD: q [b,h,n_q,d], k/v [b,h,n_k,d]
+  uint16_t* out;              // bf16 [b,h,n_q,d]
+  float* part_o;              // [splits][b*h*n_q][d]  (splits > 1)
+  float* part_ml;             // [splits][b*h*n_q][2]  (splits > 1)
+  const int32_t* kv_lengths;  // device [b] or null
+  int b, h, n_q, n_k;
+  int splits, keys_per_split;
+  float scale_log2;
+};
+constexpr int kDecodeMaxQueries = 8;
+constexpr int kDecodeTargetCtas = 152 * 4;   // four CTAs per SM of a GB300
+constexpr int kDecodeMinKeysPerSplit = 256;
+constexpr int kDecodeMaxSplits = 256;
+int decode_splits(int b, int h, int n_k);
+cudaError_t launch_sdpa_decode(const DecodeParams& p, int head_dim, cudaStream_t stream);
+
 // Exact fp32 attention on the CUDA cores, BHSD contiguous.
 struct SdpaF32Params {
   const float *q, *k, *v;
