@@ -1,0 +1,67 @@
+"""Failure detection without a GPU fault: a bounded wait that runs out.
+
+A test-only copy of the attention kernel, compiled here with
+SDPA_TEST_WITHHOLD_FIRST_S_COMMIT, never signals the first score tile of a
+query tile.  The softmax warps' wait on it gives up after its limit (about a
+second), the CTA aborts cleanly (copies and MMAs in flight are drained, tensor
+memory is freed) and sdpa_device_check() reports SDPA_ERR_DEVICE_TIMEOUT.  The
+context stays usable: the same library then returns to normal operation and
+the product library computes correct results.
+"""
+import os
+import subprocess
+import tempfile
+import time
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import transformer_scaled_dot_02_gb300 as sd
+from transformer_scaled_dot_02_gb300 import build as sd_build
+from gpu_util import TOL_BF16, dev, host, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def faulty_lib():
+    sd_build.build()
+    d = tempfile.mkdtemp(prefix="sdpa_timeout_")
+    obj = os.path.join(d, "sdpa_tc_withhold.o")
+    nvcc = sd_build._nvcc()
+    subprocess.check_call([nvcc] + sd_build._flags() + ["-DSDPA_TEST_WITHHOLD_FIRST_S_COMMIT", "-c",
+                          os.path.join(sd_build.CSRC, "sdpa_tc.cu"), "-o", obj])
+    others = [os.path.join(sd_build.BUILD_DIR, s.replace(".cu", ".o"))
+              for s in sd_build.SOURCES if s != "sdpa_tc.cu"]
+    lib_path = os.path.join(d, "libsdpa_withhold.so")
+    subprocess.check_call([nvcc] + sd_build.ARCH + ["-shared", "-cudart", "static", "-o", lib_path,
+                                                   obj] + others)
+    return sd.load_library(lib_path)
+
+
+def test_bounded_wait_times_out_and_reports(faulty_lib):
+    import torch
+    rng = np.random.default_rng(1)
+    b, h, n, d = 1, 1, 128, 64   # one CTA, one query tile
+    q = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
+    qd = dev(q)
+    out = torch.zeros((b, h, n, d), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    t0 = time.time()
+    rc = faulty_lib.sdpa_forward(qd.data_ptr(), qd.data_ptr(), qd.data_ptr(), out.data_ptr(), b, h,
+                                 n, n, d, d, 0, None, __import__("ctypes").c_float(0.0), stream)
+    assert rc == 0
+    st = faulty_lib.sdpa_device_check()
+    elapsed = time.time() - t0
+    assert st == 6, sd.STATUS_NAMES.get(st, st)   # SDPA_ERR_DEVICE_TIMEOUT
+    assert elapsed < 30.0
+    # the word was cleared by the check
+    assert faulty_lib.sdpa_device_check() == 0
+    # the context still works: the product library computes the right answer
+    k = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
+    v = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
+    got = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL))
+    sd.sdpa_device_check()
+    assert rel_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
