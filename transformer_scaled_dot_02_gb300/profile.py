@@ -3,6 +3,8 @@ C ABI, for profiling a single kernel launch under a profiler.
 
     python -m transformer_scaled_dot_02_gb300.profile --b 4 --h 16 --n 8192 --d 128 --mask 1
     python -m transformer_scaled_dot_02_gb300.profile --mha --b 32 --n 128 --d-model 512 --h 8
+    python -m transformer_scaled_dot_02_gb300.profile --decode --b 32 --h 16 --n 1 --nk 8192 --d 128
+    python -m transformer_scaled_dot_02_gb300.profile --restricted 1024 --b 4 --h 16 --n 8192 --mask 1
 
 Inputs are seeded N(0,1) bf16 values made on the device; nothing is checked.
 Prints the mean launch time measured with CUDA events.
@@ -26,6 +28,8 @@ def main():
     ap.add_argument("--mask", type=int, default=1)
     ap.add_argument("--len-lo", type=int, default=0, help="padding lengths uniform in [lo, nk]")
     ap.add_argument("--mha", action="store_true", help="multi-head attention with projections")
+    ap.add_argument("--decode", action="store_true", help="one decoding step: --n new queries, --nk cache")
+    ap.add_argument("--restricted", type=int, default=0, help="neighbourhood size r (restricted)")
     ap.add_argument("--d-model", type=int, default=512)
     ap.add_argument("--iters", type=int, default=3)
     a = ap.parse_args()
@@ -35,11 +39,21 @@ def main():
     n_q = a.n
     n_k = a.nk or a.n
     lens = None
-    if a.mask & 2:
+    if (a.mask & 2) or (a.decode and a.len_lo):
         lo = a.len_lo or n_k // 2
         lens = torch.randint(lo, n_k + 1, (a.b,), dtype=torch.int32, device=dev)
     sd.load_library()
-    if a.mha:
+    if a.decode:
+        q = torch.randn(a.b, a.h, n_q, a.d, device=dev).to(torch.bfloat16)
+        k = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
+        v = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        work = torch.empty(max(1, sd.sdpa_decode_workspace_size(a.b, a.h, n_q, n_k, a.d)),
+                           dtype=torch.uint8, device=dev)
+
+        def run():
+            sd.sdpa_decode(q, k, v, out, work, work.numel(), a.b, a.h, n_q, n_k, a.d, a.d, lens)
+    elif a.mha:
         dm = a.d_model
         xq = torch.randn(a.b, n_q, dm, device=dev).to(torch.bfloat16)
         xkv = xq if n_k == n_q else torch.randn(a.b, n_k, dm, device=dev).to(torch.bfloat16)
@@ -57,7 +71,11 @@ def main():
         out = torch.empty_like(q[..., : a.d])
 
         def run():
-            sd.sdpa_forward(q, k, v, out, a.b, a.h, n_q, n_k, a.d, a.d, a.mask, lens)
+            if a.restricted:
+                sd.sdpa_forward_restricted(q, k, v, out, a.b, a.h, n_q, n_k, a.d, a.d, a.mask, lens,
+                                           a.restricted)
+            else:
+                sd.sdpa_forward(q, k, v, out, a.b, a.h, n_q, n_k, a.d, a.d, a.mask, lens)
 
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
