@@ -110,7 +110,7 @@ def test_restricted_argument_checks(lib):
     assert call(r=-5) == INVALID
     assert call(q=None) == INVALID
     assert call(mask=1, n_k=17) == INVALID
-    assert call(d=32) == UNSUPPORTED
+    assert call(d=48) == UNSUPPORTED
 
 
 def test_decode_argument_checks(lib):
@@ -135,7 +135,8 @@ def test_decode_argument_checks(lib):
 
 
 def test_unsupported_shapes(lib):
-    assert _attn(lib, "sdpa_forward", d_k=32, d_v=32) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=48, d_v=48) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=8, d_v=8) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=64, d_v=128) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=256, d_v=256) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward_f32", d_k=129, d_v=64) == UNSUPPORTED
@@ -159,7 +160,7 @@ def test_mha_argument_checks(lib):
     assert _mha(lib, h=0) == INVALID
     assert _mha(lib, mask=1, n_k=9) == INVALID
     assert _mha(lib, mask=2) == INVALID
-    assert _mha(lib, d_k=32, d_v=32) == UNSUPPORTED
+    assert _mha(lib, d_k=48, d_v=48) == UNSUPPORTED
     assert _mha(lib, d_model=60) == UNSUPPORTED
     assert _mha(lib, ws=None) == WORKSPACE
     assert _mha(lib, ws=MIS) == WORKSPACE

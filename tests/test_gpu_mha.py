@@ -61,7 +61,7 @@ def test_cross_mha_workload_sampled():
     assert rel_err(got.reshape(-1, w.d_model)[rows], ref) <= TOL_BF16
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 def test_mha_ragged_causal(d):
     rng = np.random.default_rng(22 + d)
     b, n, dm, h = 2, 300, 256, 2

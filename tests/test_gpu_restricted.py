@@ -26,7 +26,7 @@ def _gpu(q, k, v, mask, lens, r, scale=0.0):
     return host(out)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("mask", [0, 1, 2, 3])
 @pytest.mark.parametrize("r", [1, 2, 3, 64, 127, 128, 129, 300, 5000])
 def test_restricted_shapes(d, mask, r):

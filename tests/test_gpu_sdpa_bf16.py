@@ -31,7 +31,7 @@ def _rand(rng, shape, std=1.0):
     return synthetic.round_to_bf16(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("mask", [0, 1, 2, 3])
 @pytest.mark.parametrize("n", [1, 17, 129, 300])
 def test_edge_shapes(d, mask, n):
@@ -48,7 +48,7 @@ def test_edge_shapes(d, mask, n):
     assert rel_err(got, ref) <= TOL_BF16
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 def test_padding_degenerate_lengths(d):
     """len 0 (no visible key: zeros), len 1 (value row 0), len > n_k (clamped)."""
     rng = np.random.default_rng(7 + d)
@@ -72,7 +72,7 @@ def test_no_keys(d):
     assert np.array_equal(host(out), np.zeros((1, 2, 40, d)))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 def test_sharp_scores_move_the_running_max(d):
     """Large, growing scores force the online softmax to rescale O many times."""
     rng = np.random.default_rng(11 + d)
@@ -173,3 +173,14 @@ def test_long_causal_workload_sampled_rows():
     assert rel_err(got.reshape(-1, w.d_v)[rows], ref_rows) <= TOL_BF16
     # every row is a convex combination of value rows: bounded by max |V|
     assert np.abs(got).max() <= np.abs(v).max() * 1.01
+
+
+@pytest.mark.parametrize("h,d", [(16, 32), (32, 16)])
+def test_table3_head_sizes(h, d):
+    """Table 3, row (A): d_model 512 split as 16 heads of 32 or 32 heads of 16,
+    causal self-attention over 600 positions."""
+    rng = np.random.default_rng(17 + d)
+    q, k, v = _rand(rng, (2, h, 600, d)), _rand(rng, (2, h, 600, d)), _rand(rng, (2, h, 600, d))
+    got = _gpu(q, k, v, sd.SDPA_MASK_CAUSAL)
+    ref = oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)
+    assert rel_err(got, ref) <= TOL_BF16

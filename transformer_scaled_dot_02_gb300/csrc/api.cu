@@ -81,7 +81,7 @@ sdpa_status current_device(unsigned** status) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
-// 64 x 128 boxes, 128-byte swizzle, zero fill outside the tensor.
+// boxes of min(d, 64) x 128, swizzled at the row width, zero fill outside.
 bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
                  long long stride_n, long long stride_h, long long stride_b) {
   auto enc = encode_fn();
@@ -91,10 +91,14 @@ bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(stride_n) * 2,
                                  static_cast<cuuint64_t>(stride_h) * 2,
                                  static_cast<cuuint64_t>(stride_b) * 2};
-  const cuuint32_t box[4] = {64, 128, 1, 1};
+  // boxes of min(d, 64) columns: rows of 128, 64 or 32 bytes, swizzled at that width
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 128, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle swz = d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                         : (d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                    : CU_TENSOR_MAP_SWIZZLE_32B);
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -133,6 +137,9 @@ sdpa_status check_attention_args(const void* q, const void* k, const void* v, co
   if (elems_q > (1ll << 38) || elems_k > (1ll << 38)) return SDPA_ERR_UNSUPPORTED;
   return SDPA_OK;
 }
+
+// head sizes the tensor-core attention kernel is built for
+bool tc_head_size(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 float effective_scale(float scale, int d_k) {
   return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
@@ -188,7 +195,7 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
   sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
                                         kv_lengths, scale);
   if (st != SDPA_OK) return st;
-  if (d_k != d_v || (d_k != 64 && d_k != 128)) return SDPA_ERR_UNSUPPORTED;
+  if (d_k != d_v || !tc_head_size(d_k)) return SDPA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = current_device(&status);
   if (st != SDPA_OK) return st;
@@ -208,7 +215,7 @@ sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v,
                                         kv_lengths, scale);
   if (st != SDPA_OK) return st;
   if (r < 1) return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || (d_k != 64 && d_k != 128)) return SDPA_ERR_UNSUPPORTED;
+  if (d_k != d_v || !tc_head_size(d_k)) return SDPA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = current_device(&status);
   if (st != SDPA_OK) return st;
@@ -331,7 +338,7 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
       (kv_lengths == nullptr || (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0))
     return SDPA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || (d_k != 64 && d_k != 128) || d_model % 8 != 0) return SDPA_ERR_UNSUPPORTED;
+  if (d_k != d_v || !tc_head_size(d_k) || d_model % 8 != 0) return SDPA_ERR_UNSUPPORTED;
   if (1ll * b * (n_q > n_k ? n_q : n_k) > (1ll << 30) || 1ll * h * d_k > 65536)
     return SDPA_ERR_UNSUPPORTED;
   const size_t need = mha_workspace_size(b, n_q, n_k, h, d_k, d_v);

@@ -248,14 +248,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 // K-major tiles: rows of 128 bytes, 8-row groups 1024 bytes apart (SBO); the
 // leading offset is unused.  MN-major tiles: LBO = distance between 64-element
 // column blocks, SBO = distance between 8-row groups along K.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// `layout` selects the swizzle: 2 = 128-byte, 4 = 64-byte, 6 = 32-byte rows.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
   return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo, 2);
 }
 
 // tcgen05.ld / st, shape 32x32b: lane i of the warp reads/writes TMEM lane
@@ -283,6 +289,26 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       SDPA_W8(r, 0), SDPA_W8(r, 8), SDPA_W8(r, 16), SDPA_W8(r, 24)
       : "memory");
 }
+
+#define SDPA_R4(p, o) "=r"(p[o + 0]), "=r"(p[o + 1]), "=r"(p[o + 2]), "=r"(p[o + 3])
+#define SDPA_W4(p, o) "r"(p[o + 0]), "r"(p[o + 1]), "r"(p[o + 2]), "r"(p[o + 3])
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : SDPA_R4(r, 0), SDPA_R4(r, 4), SDPA_R4(r, 8), SDPA_R4(r, 12)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      SDPA_W4(r, 0), SDPA_W4(r, 4), SDPA_W4(r, 8), SDPA_W4(r, 12)
+      : "memory");
+}
+#undef SDPA_R4
+#undef SDPA_W4
 
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -330,6 +356,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // 128-byte rows written with the 128-byte swizzle (the TMA's SWIZZLE_128B).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// Same for rows of RowBytes (128, 64 or 32) under the matching swizzle: the
+// 16-byte chunk index is XORed with address bits 7.. of the row start.
+template <int RowBytes>
+__device__ __forceinline__ uint32_t swizzle_offset(uint32_t row, uint32_t chunk) {
+  if constexpr (RowBytes == 128) return row * 128u + ((chunk ^ (row & 7u)) << 4);
+  else if constexpr (RowBytes == 64) return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
+  else return row * 32u + ((chunk ^ ((row >> 2) & 1u)) << 4);
 }
 
 }  // namespace sdpa

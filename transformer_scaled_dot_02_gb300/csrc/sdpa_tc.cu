@@ -38,7 +38,6 @@ namespace {
 
 constexpr int kBlockM = 128;     // query rows per tile (= tensor-memory lanes)
 constexpr int kBlockN = 128;     // keys per tile
-constexpr int kBoxBytes = 128 * 128;  // one 64-column (128-byte) box of 128 rows
 constexpr int kThreads = 384;    // 12 warps: two softmax warpgroups + one for TMA/MMA
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -53,11 +52,21 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: a factor of 256
 
 template <int D>
 struct Cfg {
-  static constexpr int kBoxes = D / 64;
+  // Tiles move as boxes of kBoxCols columns x 128 rows, rows of kRowBytes
+  // swizzled at that width (128-, 64- or 32-byte swizzle for d >= 64, 32, 16).
+  static constexpr int kBoxCols = D < 64 ? D : 64;
+  static constexpr int kRowBytes = kBoxCols * 2;
+  static constexpr int kBoxBytes = 128 * kRowBytes;
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr uint32_t kLayout = kRowBytes == 128 ? 2u : (kRowBytes == 64 ? 4u : 6u);
+  static constexpr uint32_t kSBO = 8 * kRowBytes;          // 8-row group stride
+  static constexpr int kStepsPerRow = kRowBytes / 32;      // K=16 steps per swizzled row
+  static constexpr int kOChunk = D < 32 ? D : 32;          // O columns per TMEM load
   static constexpr int kTileBytes = kBlockM * D * 2;
   // K/V ring depths: Q (2 tiles) + K + V stages fill the 227 KB of shared memory.
   static constexpr int kKStages = (D == 128) ? 2 : 4;
   static constexpr int kVStages = (D == 128) ? 2 : 4;
+  static_assert(D == 16 || D == 32 || D == 64 || D == 128, "head size");
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
@@ -79,6 +88,12 @@ struct Bars {
   uint64_t* o_full;   // [2]
   uint64_t* drain;
 };
+
+// TMEM loads / stores of 32 or 16 columns (32x32b shape).
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
+__device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
 
 template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
@@ -205,8 +220,8 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         for (int t = 0; t < 2; ++t) {
           if (hi_of(t) <= lo_of(t)) continue;
           for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_4d(&p.tm_q, bars.q_full, smem + C::kQOff + t * C::kTileBytes + c * kBoxBytes,
-                        c * 64, q0 + t * kBlockM, hi, bi);
+            tma_load_4d(&p.tm_q, bars.q_full, smem + C::kQOff + t * C::kTileBytes + c * C::kBoxBytes,
+                        c * C::kBoxCols, q0 + t * kBlockM, hi, bi);
         }
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K (V) copy was started
@@ -218,7 +233,8 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         mbar_arrive_expect_tx(bars.k_full + sk, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(&p.tm_k, bars.k_full + sk,
-                      smem + C::kKOff + sk * C::kTileBytes + c * kBoxBytes, c * 64, j * kBlockN, hi, bi);
+                      smem + C::kKOff + sk * C::kTileBytes + c * C::kBoxBytes, c * C::kBoxCols,
+                      j * kBlockN, hi, bi);
         k_issued = u + 1;
         const int sv = u % C::kVStages;
         const uint32_t uv = static_cast<uint32_t>(u / C::kVStages);
@@ -226,7 +242,8 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         mbar_arrive_expect_tx(bars.v_full + sv, C::kTileBytes);
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(&p.tm_v, bars.v_full + sv,
-                      smem + C::kVOff + sv * C::kTileBytes + c * kBoxBytes, c * 64, j * kBlockN, hi, bi);
+                      smem + C::kVOff + sv * C::kTileBytes + c * C::kBoxBytes, c * C::kBoxCols,
+                      j * kBlockN, hi, bi);
         v_issued = u + 1;
       }
       // Let every copy this thread started land before the CTA can exit.
@@ -245,9 +262,9 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       // Descriptors split in halves: the high word is fixed by the layout, the
       // low word holds (address >> 4) and the leading offset; a K step adds
       // its byte offset >> 4 to the low word (no carry: smem < 256 KB).
-      const uint64_t kq = smem_desc_sw128(q_smem, 16, 1024);
-      const uint64_t kk = smem_desc_sw128(k_smem, 16, 1024);
-      const uint64_t kv = smem_desc_sw128(v_smem, kBoxBytes, 1024);
+      const uint64_t kq = smem_desc(q_smem, 16, C::kSBO, C::kLayout);
+      const uint64_t kk = smem_desc(k_smem, 16, C::kSBO, C::kLayout);
+      const uint64_t kv = smem_desc(v_smem, C::kBoxBytes, C::kSBO, C::kLayout);
       const uint32_t q_lo = static_cast<uint32_t>(kq), qk_hi = static_cast<uint32_t>(kq >> 32);
       const uint32_t k_lo = static_cast<uint32_t>(kk);
       const uint32_t v_lo = static_cast<uint32_t>(kv), v_hi = static_cast<uint32_t>(kv >> 32);
@@ -257,7 +274,8 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         const uint32_t b0 = k_lo + static_cast<uint32_t>((stage * C::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = static_cast<uint32_t>(((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4);
+          const uint32_t off = static_cast<uint32_t>(
+              ((k / C::kStepsPerRow) * C::kBoxBytes + (k % C::kStepsPerRow) * 32) >> 4);
           mma_bf16_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
@@ -268,7 +286,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
 #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k) {
           mma_bf16_ts_lohi(d_tmem, p_tmem + static_cast<uint32_t>(k * 8),
-                           b0 + static_cast<uint32_t>((k * 16 * 128) >> 4), v_hi, C::kIdescPV,
+                           b0 + static_cast<uint32_t>((k * 16 * C::kRowBytes) >> 4), v_hi, C::kIdescPV,
                            (accumulate || k > 0) ? 1u : 0u);
         }
       };
@@ -442,14 +460,14 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       // covers every MMA issued before it, PV_t(j-1) included.
       if (rescale_warp) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + o_col + c * 32, o);
+        for (int c = 0; c < D / C::kOChunk; ++c) {
+          uint32_t o[C::kOChunk];
+          tmem_ld_chunk(lane_base + o_col + c * C::kOChunk, o);
           tmem_ld_wait();
           reg_fence(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_base + o_col + c * 32, o);
+          for (int e = 0; e < C::kOChunk; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_chunk(lane_base + o_col + c * C::kOChunk, o);
         }
       }
       l += rowsum;
@@ -471,26 +489,28 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       if (have_o || (ok && n_t == 0)) {
         const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
+        for (int c = 0; c < D / C::kOChunk; ++c) {
+          uint32_t o[C::kOChunk];
           if (have_o) {
-            tmem_ld32(lane_base + o_col + c * 32, o);
+            tmem_ld_chunk(lane_base + o_col + c * C::kOChunk, o);
             tmem_ld_wait();
             reg_fence(o);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
+            for (int e = 0; e < C::kOChunk; ++e) o[e] = 0u;
           }
-          uint8_t* box = stage + (c >> 1) * kBoxBytes;
+          const int col0 = c * C::kOChunk;                 // first O column of this chunk
+          uint8_t* box = stage + (col0 / C::kBoxCols) * C::kBoxBytes;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q4 = 0; q4 < C::kOChunk / 8; ++q4) {
             uint4 v;
             v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
             v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
             v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
             v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-            const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
-            *reinterpret_cast<uint4*>(box + sw128_offset(static_cast<uint32_t>(row_in_tile), chunk)) = v;
+            const uint32_t chunk = static_cast<uint32_t>((col0 % C::kBoxCols) / 8 + q4);
+            *reinterpret_cast<uint4*>(
+                box + swizzle_offset<C::kRowBytes>(static_cast<uint32_t>(row_in_tile), chunk)) = v;
           }
         }
         fence_proxy_async_smem();
@@ -498,7 +518,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       named_bar_sync(1 + t, 128);
       if (quarter == 0 && lane == 0 && !*abort_flag) {
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_store_4d(&p.tm_o, stage + c * kBoxBytes, c * 64, q_start_t, hi, bi);
+          tma_store_4d(&p.tm_o, stage + c * C::kBoxBytes, c * C::kBoxCols, q_start_t, hi, bi);
         tma_store_commit();
         tma_store_wait_read();
       }
@@ -530,6 +550,8 @@ cudaError_t launch_impl(const SdpaTcParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
+  if (head_dim == 16) return launch_impl<16>(p, stream);
+  if (head_dim == 32) return launch_impl<32>(p, stream);
   if (head_dim == 64) return launch_impl<64>(p, stream);
   if (head_dim == 128) return launch_impl<128>(p, stream);
   return cudaErrorInvalidValue;
