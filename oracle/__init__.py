@@ -53,6 +53,8 @@ class Oracle:
         lib.oracle_sdpa_restricted.restype = I
         lib.oracle_sdpa_decode.argtypes = [P, P, P, P, I, I, I, I, I, I, P, D, P, I64, I]
         lib.oracle_sdpa_decode.restype = I
+        lib.oracle_sdpa_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, D, I, I]
+        lib.oracle_sdpa_backward.restype = I
         self.lib = lib
         self.path = lib_path
 
@@ -64,6 +66,9 @@ class Oracle:
 
     def decode(self, *args, **kwargs):
         return _decode(self.lib, *args, **kwargs)
+
+    def backward(self, *args, **kwargs):
+        return _backward(self.lib, *args, **kwargs)
 
 
 _default: Oracle | None = None
@@ -99,6 +104,29 @@ def sdpa(*args, **kwargs):
 def mha(*args, **kwargs):
     """Multi-head attention; see ``_mha``.  Uses the library built from oracle.c."""
     return default().mha(*args, **kwargs)
+
+
+def backward(*args, **kwargs):
+    """Gradients of Eq. (1); see ``_backward``."""
+    return default().backward(*args, **kwargs)
+
+
+def _backward(lib, q, k, v, dout, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, window=None,
+              threads=None):
+    """dq, dk, dv (float64, shapes of q, k, v) of sum(dout * attention(q, k, v))."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    b, h, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    lens = None if kv_lengths is None else np.ascontiguousarray(kv_lengths, dtype=np.int32)
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    rc = lib.oracle_sdpa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), b, h, n_q, n_k, d_k, d_v, int(mask_kind), _ptr(lens),
+                                  float(scale), int(window or 0), threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_sdpa_backward rejected its arguments")
+    return dq, dk, dv
 
 
 def decode(*args, **kwargs):

@@ -31,6 +31,13 @@
  *   len_b, so query i sits at position len_b - n_q + i and, by the causal
  *   rule, sees keys j <= len_b - n_q + i.
  *
+ *   Training (section 5) needs the gradients of Eq. (1).  With P = softmax(S),
+ *   S = scale * Q K^T, O = P V and an upstream gradient dO of O, the chain rule
+ *   gives, per head:
+ *       dV = P^T dO,   dP = dO V^T,   D_i = sum_j P_ij dP_ij (= dO_i . O_i),
+ *       dS = P o (dP - D),   dQ = scale * dS K,   dK = scale * dS^T Q,
+ *   the softmax Jacobian written out row by row; masked entries have P = 0.
+ *
  *   Section 3.2.2, multi-head attention:
  *       MultiHead(Q, K, V) = Concat(head_1, ..., head_h) W^O,
  *       head_i = Attention(Q W_i^Q, K W_i^K, V W_i^V),
@@ -210,6 +217,107 @@ int oracle_sdpa_restricted(const float* q, const float* k, const float* v, doubl
   if (r < 1) return -1;
   return sdpa_common(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths, scale,
                      (int64_t)((r - 1) / 2), (int64_t)(r / 2), rows, n_rows, n_threads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gradients of Eq. (1) for one (batch, head): plain loops over rows.         */
+typedef struct {
+  const float *q, *k, *v, *dout;
+  double *dq, *dk, *dv;
+  int h, n_q, n_k, d_k, d_v, mask_kind;
+  const int32_t* kv_lengths;
+  double scale;
+  int64_t left, right;
+} bwd_ctx;
+
+static void bwd_range(void* p, int64_t begin, int64_t end) {
+  bwd_ctx* c = (bwd_ctx*)p;
+  double* prow = (double*)malloc(sizeof(double) * (size_t)(c->n_k > 0 ? c->n_k : 1));
+  double* dprow = (double*)malloc(sizeof(double) * (size_t)(c->n_k > 0 ? c->n_k : 1));
+  for (int64_t bh = begin; bh < end; ++bh) {
+    int bi = (int)(bh / c->h);
+    int len = clamp_len(c->kv_lengths, c->mask_kind, bi, c->n_k);
+    int causal = (c->mask_kind & ORACLE_MASK_CAUSAL) != 0;
+    const float* q = c->q + bh * (int64_t)c->n_q * c->d_k;
+    const float* k = c->k + bh * (int64_t)c->n_k * c->d_k;
+    const float* v = c->v + bh * (int64_t)c->n_k * c->d_v;
+    const float* dout = c->dout + bh * (int64_t)c->n_q * c->d_v;
+    double* dq = c->dq + bh * (int64_t)c->n_q * c->d_k;
+    double* dk = c->dk + bh * (int64_t)c->n_k * c->d_k;
+    double* dv = c->dv + bh * (int64_t)c->n_k * c->d_v;
+    for (int64_t x = 0; x < (int64_t)c->n_k * c->d_k; ++x) dk[x] = 0.0;
+    for (int64_t x = 0; x < (int64_t)c->n_k * c->d_v; ++x) dv[x] = 0.0;
+    for (int i = 0; i < c->n_q; ++i) {
+      const float* qi = q + (int64_t)i * c->d_k;
+      const float* doi = dout + (int64_t)i * c->d_v;
+      double* dqi = dq + (int64_t)i * c->d_k;
+      for (int x = 0; x < c->d_k; ++x) dqi[x] = 0.0;
+      /* P row (softmax with the max shift; masked entries 0) */
+      double m = -INFINITY;
+      int any = 0;
+      for (int j = 0; j < c->n_k; ++j) {
+        int visible = (j < len) && !(causal && j > i) && (j >= i - c->left) && (j <= i + c->right);
+        if (!visible) { prow[j] = -INFINITY; continue; }
+        double dot = 0.0;
+        const float* kj = k + (int64_t)j * c->d_k;
+        for (int x = 0; x < c->d_k; ++x) dot += (double)qi[x] * (double)kj[x];
+        prow[j] = c->scale * dot;
+        if (prow[j] > m) m = prow[j];
+        any = 1;
+      }
+      if (!any) continue;            /* no visible key: output 0, gradients 0 */
+      double l = 0.0;
+      for (int j = 0; j < c->n_k; ++j) {
+        prow[j] = (prow[j] == -INFINITY) ? 0.0 : exp(prow[j] - m);
+        l += prow[j];
+      }
+      for (int j = 0; j < c->n_k; ++j) prow[j] /= l;
+      /* dP row = dO_i . v_j, and D_i = sum_j P_ij dP_ij */
+      double Di = 0.0;
+      for (int j = 0; j < c->n_k; ++j) {
+        if (prow[j] == 0.0) { dprow[j] = 0.0; continue; }
+        double dot = 0.0;
+        const float* vj = v + (int64_t)j * c->d_v;
+        for (int x = 0; x < c->d_v; ++x) dot += (double)doi[x] * (double)vj[x];
+        dprow[j] = dot;
+        Di += prow[j] * dot;
+      }
+      for (int j = 0; j < c->n_k; ++j) {
+        if (prow[j] == 0.0) continue;
+        double ds = prow[j] * (dprow[j] - Di);
+        const float* kj = k + (int64_t)j * c->d_k;
+        double* dkj = dk + (int64_t)j * c->d_k;
+        double* dvj = dv + (int64_t)j * c->d_v;
+        for (int x = 0; x < c->d_k; ++x) {
+          dqi[x] += c->scale * ds * (double)kj[x];
+          dkj[x] += c->scale * ds * (double)qi[x];
+        }
+        for (int x = 0; x < c->d_v; ++x) dvj[x] += prow[j] * (double)doi[x];
+      }
+    }
+  }
+  free(prow);
+  free(dprow);
+}
+
+/*
+ * Gradients of Eq. (1) with masks: given q, k, v (BHSD float32) and dout
+ * [b,h,n_q,d_v], writes dq [b,h,n_q,d_k], dk [b,h,n_k,d_k], dv [b,h,n_k,d_v]
+ * (fp64).  Parallel over (batch, head).  Returns 0, or -1 on bad arguments.
+ */
+int oracle_sdpa_backward(const float* q, const float* k, const float* v, const float* dout,
+                         double* dq, double* dk, double* dv, int b, int h, int n_q, int n_k,
+                         int d_k, int d_v, int mask_kind, const int32_t* kv_lengths,
+                         double scale, int r, int n_threads) {
+  if (b < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k < 1 || d_v < 1) return -1;
+  if ((mask_kind & ORACLE_MASK_CAUSAL) && n_q != n_k) return -1;
+  if ((mask_kind & ORACLE_MASK_PADDING) && kv_lengths == NULL) return -1;
+  bwd_ctx c = {q, k, v, dout, dq, dk, dv, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths,
+               scale > 0.0 ? scale : 1.0 / sqrt((double)d_k),
+               r > 0 ? (int64_t)((r - 1) / 2) : INT64_MAX / 4,
+               r > 0 ? (int64_t)(r / 2) : INT64_MAX / 4};
+  parallel_for((int64_t)b * h, n_threads, bwd_range, &c);
+  return 0;
 }
 
 /* ------------------------------------------------------------------------ */

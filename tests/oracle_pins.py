@@ -470,10 +470,63 @@ def pin_decode_cache_lengths(o):
     assert abs(w[0, 0, 0, 0] - g["output"]) < 1e-6
 
 
+# ---------------------------------------------------------------- gradients
+def pin_backward_finite_differences(o):
+    """The gradients are those of L = sum(dO * Attention(Q, K, V)): central
+    differences of the oracle's own forward along random directions agree."""
+    rng = np.random.default_rng(50)
+    cases = [(2, 2, 5, 5, 3, 2, MASK_CAUSAL, None), (1, 2, 4, 7, 4, 3, MASK_PADDING, None),
+             (2, 1, 6, 6, 2, 2, MASK_NONE, 3), (1, 1, 6, 6, 3, 3, MASK_CAUSAL | MASK_PADDING, 4)]
+    for (b, h, n_q, n_k, d_k, d_v, mask, r) in cases:
+        q = rng.standard_normal((b, h, n_q, d_k))
+        k = rng.standard_normal((b, h, n_k, d_k))
+        v = rng.standard_normal((b, h, n_k, d_v))
+        do = rng.standard_normal((b, h, n_q, d_v))
+        lens = np.array([n_k, max(1, n_k // 2)][:b], np.int32) if mask & MASK_PADDING else None
+        # float32 storage: keep the inputs exactly representable
+        q, k, v, do = (x.astype(np.float32).astype(np.float64) for x in (q, k, v, do))
+        dq, dk, dv = o.backward(q, k, v, do, mask, lens, window=r)
+
+        def loss(qq, kk, vv):
+            return float(np.sum(do * o.sdpa(qq, kk, vv, mask, lens, window=r)))
+        eps = 1e-3
+        for (x, g, which) in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+            direction = rng.standard_normal(x.shape)
+            args_p = [q, k, v]
+            args_m = [q, k, v]
+            args_p[which] = x + eps * direction
+            args_m[which] = x - eps * direction
+            # the oracle reads float32: central differences on float64 copies
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(fd - float(np.sum(g * direction))) < 2e-4 * (1 + abs(fd)), (which, mask, fd)
+
+
+def pin_backward_closed_forms(o):
+    """Identical keys give dQ = 0 (softmax rows sum to one, so the rows of dS
+    sum to zero); the dV rows sum to the dO rows; keys hidden by padding get
+    zero gradient."""
+    rng = np.random.default_rng(51)
+    n, d = 6, 3
+    q = rng.standard_normal((1, 1, n, d)).astype(np.float32)
+    key = rng.standard_normal(d).astype(np.float32)
+    k = np.broadcast_to(key, (1, 1, n, d)).copy()
+    v = rng.standard_normal((1, 1, n, d)).astype(np.float32)
+    do = rng.standard_normal((1, 1, n, d)).astype(np.float32)
+    dq, dk, dv = o.backward(q, k, v, do)
+    assert np.allclose(dq, 0.0, atol=1e-12)
+    assert np.allclose(dv.sum(2), do.astype(np.float64).sum(2), atol=1e-12)
+    k2 = rng.standard_normal((1, 1, n, d)).astype(np.float32)
+    lens = np.array([4], np.int32)
+    dq, dk, dv = o.backward(q, k2, v, do, MASK_PADDING, lens)
+    assert np.array_equal(dk[0, 0, 4:], np.zeros((2, d))) and np.array_equal(dv[0, 0, 4:], np.zeros((2, d)))
+    assert np.allclose(dv.sum(2), do.astype(np.float64).sum(2), atol=1e-12)
+
+
 PINS = [pin_worked_example, pin_worked_example_causal, pin_toy_rows, pin_scale_is_inverse_sqrt_dk,
         pin_rows_sum_to_one, pin_equal_scores_give_mean, pin_high_temperature_is_uniform,
         pin_shift_invariance, pin_causal_ignores_future, pin_padding_ignores_masked_keys,
         pin_permutation_equivariance, pin_brute_force, pin_rows_selection,
         pin_mha_single_head_identity, pin_mha_matches_matrix_form, pin_mha_concat_not_average,
         pin_mha_rows_selection, pin_restricted_worked_example, pin_restricted_extremes,
-        pin_restricted_brute_force, pin_decode_matches_causal_rows, pin_decode_cache_lengths]
+        pin_restricted_brute_force, pin_decode_matches_causal_rows, pin_decode_cache_lengths,
+        pin_backward_finite_differences, pin_backward_closed_forms]

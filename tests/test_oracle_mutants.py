@@ -40,6 +40,9 @@ MUTANTS = {
     "window_right_exclusive": ("(j <= i + right)", "(j < i + right)"),
     "decode_position_unshifted": ("int pos = len - c->n_q + i;", "int pos = i;"),
     "decode_position_off_by_one": ("int pos = len - c->n_q + i;", "int pos = len - c->n_q + i + 1;"),
+    "backward_ds_sign": ("double ds = prow[j] * (dprow[j] - Di);", "double ds = prow[j] * (dprow[j] + Di);"),
+    "backward_dk_unscaled": ("dkj[x] += c->scale * ds * (double)qi[x];", "dkj[x] += ds * (double)qi[x];"),
+    "backward_dv_uses_dp": ("dvj[x] += prow[j] * (double)doi[x];", "dvj[x] += dprow[j] * (double)doi[x];"),
     "mha_output_skips_wo": ("yr[o] += concat[t] * (double)wt[o];", "yr[o] += (o == t) ? concat[t] : 0.0;"),
 }
 
