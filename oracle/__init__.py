@@ -55,6 +55,8 @@ class Oracle:
         lib.oracle_sdpa_decode.restype = I
         lib.oracle_sdpa_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, D, I, I]
         lib.oracle_sdpa_backward.restype = I
+        lib.oracle_sdpa_lse.argtypes = [P, P, P, I, I, I, I, I, I, P, I, D, I]
+        lib.oracle_sdpa_lse.restype = I
         self.lib = lib
         self.path = lib_path
 
@@ -69,6 +71,9 @@ class Oracle:
 
     def backward(self, *args, **kwargs):
         return _backward(self.lib, *args, **kwargs)
+
+    def lse(self, *args, **kwargs):
+        return _lse(self.lib, *args, **kwargs)
 
 
 _default: Oracle | None = None
@@ -109,6 +114,27 @@ def mha(*args, **kwargs):
 def backward(*args, **kwargs):
     """Gradients of Eq. (1); see ``_backward``."""
     return default().backward(*args, **kwargs)
+
+
+def lse(*args, **kwargs):
+    """Per-row log of the softmax denominator; see ``_lse``."""
+    return default().lse(*args, **kwargs)
+
+
+def _lse(lib, q, k, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, window=None, threads=None):
+    """lse [b,h,n_q] float64: ln sum over visible keys of exp(scale q.k), -inf
+    for a row that sees no key (window=None: plain attention)."""
+    q, k = _f32(q), _f32(k)
+    b, h, n_q, d_k = q.shape
+    n_k = k.shape[2]
+    lens = None if kv_lengths is None else np.ascontiguousarray(kv_lengths, dtype=np.int32)
+    out = np.zeros((b, h, n_q), dtype=np.float64)
+    rc = lib.oracle_sdpa_lse(_ptr(q), _ptr(k), _ptr(out), b, h, n_q, n_k, d_k, int(mask_kind),
+                             _ptr(lens), int(window or 0), float(scale),
+                             threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_sdpa_lse: bad arguments")
+    return out
 
 
 def _backward(lib, q, k, v, dout, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, window=None,

@@ -220,6 +220,69 @@ int oracle_sdpa_restricted(const float* q, const float* k, const float* v, doubl
 }
 
 /* ------------------------------------------------------------------------ */
+/* Log of the softmax denominator of Eq. (1) for every query row:             */
+/*   lse_i = ln sum_{j visible} exp(scale q_i . k_j)                          */
+/* (-inf when no key is visible), taken as m + ln sum exp(s_j - m) with m the */
+/* row maximum.  The visibility rule is attention_row's.  This is the value a */
+/* backward pass needs to rebuild the softmax weights exp(s_ij - lse_i).      */
+typedef struct {
+  const float *q, *k;
+  double* lse;
+  int h, n_q, n_k, d_k, mask_kind;
+  const int32_t* kv_lengths;
+  double scale;
+  int64_t left, right;
+} lse_ctx;
+
+static void lse_range(void* p, int64_t begin, int64_t end) {
+  lse_ctx* c = (lse_ctx*)p;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(c->n_k > 0 ? c->n_k : 1));
+  for (int64_t r = begin; r < end; ++r) {
+    int i = (int)(r % c->n_q);
+    int64_t bh = r / c->n_q;
+    int bi = (int)(bh / c->h);
+    int len = clamp_len(c->kv_lengths, c->mask_kind, bi, c->n_k);
+    int causal = (c->mask_kind & ORACLE_MASK_CAUSAL) != 0;
+    const float* q = c->q + r * c->d_k;
+    const float* k = c->k + bh * (int64_t)c->n_k * c->d_k;
+    double m = -INFINITY;
+    for (int j = 0; j < c->n_k; ++j) {
+      int visible = (j < len) && !(causal && j > i) && (j >= i - c->left) && (j <= i + c->right);
+      s[j] = -INFINITY;
+      if (!visible) continue;
+      double dot = 0.0;
+      for (int e = 0; e < c->d_k; ++e) dot += (double)q[e] * (double)k[(int64_t)j * c->d_k + e];
+      s[j] = c->scale * dot;
+      if (s[j] > m) m = s[j];
+    }
+    if (m == -INFINITY) { c->lse[r] = -INFINITY; continue; }
+    double l = 0.0;
+    for (int j = 0; j < c->n_k; ++j)
+      if (s[j] != -INFINITY) l += exp(s[j] - m);
+    c->lse[r] = m + log(l);
+  }
+  free(s);
+}
+
+/*
+ * lse [b,h,n_q] of the rows of oracle_sdpa (r == 0) or oracle_sdpa_restricted
+ * (r >= 1) on the same arguments.  Returns 0, or -1 on bad arguments.
+ */
+int oracle_sdpa_lse(const float* q, const float* k, double* lse, int b, int h, int n_q, int n_k,
+                    int d_k, int mask_kind, const int32_t* kv_lengths, int r, double scale,
+                    int n_threads) {
+  if (b < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k < 1 || r < 0) return -1;
+  if ((mask_kind & ORACLE_MASK_CAUSAL) && n_q != n_k) return -1;
+  if ((mask_kind & ORACLE_MASK_PADDING) && kv_lengths == NULL) return -1;
+  lse_ctx c = {q, k, lse, h, n_q, n_k, d_k, mask_kind, kv_lengths,
+               scale > 0.0 ? scale : 1.0 / sqrt((double)d_k),
+               r > 0 ? (int64_t)((r - 1) / 2) : INT64_MAX / 4,
+               r > 0 ? (int64_t)(r / 2) : INT64_MAX / 4};
+  parallel_for((int64_t)b * h * n_q, n_threads, lse_range, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gradients of Eq. (1) for one (batch, head): plain loops over rows.         */
 typedef struct {
   const float *q, *k, *v, *dout;

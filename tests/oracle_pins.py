@@ -522,6 +522,47 @@ def pin_backward_closed_forms(o):
     assert np.allclose(dv.sum(2), do.astype(np.float64).sum(2), atol=1e-12)
 
 
+def pin_lse_closed_forms(o):
+    """The per-row log-sum-exp: zero keys give ln(number of visible keys)
+    under every mask; a row that sees nothing gives -inf; one query 1 against
+    keys 0 and t (d_k = 1, scale 1) gives ln(1 + e^t)."""
+    n, d = 9, 4
+    zeros_q = np.ones((2, 1, n, d), np.float32)
+    zeros_k = np.zeros((2, 1, n, d), np.float32)
+    lens = np.array([n, 3], np.int32)
+    lse = o.lse(zeros_q, zeros_k, MASK_CAUSAL | MASK_PADDING, lens, window=5)
+    for bi in range(2):
+        for i in range(n):
+            # visible: j <= i, j < len, i - 2 <= j <= i + 2
+            count = sum(1 for j in range(n) if j <= i and j < lens[bi] and i - 2 <= j <= i + 2)
+            want = np.log(count) if count else -np.inf
+            assert lse[bi, 0, i] == want or abs(lse[bi, 0, i] - want) < 1e-12, (bi, i)
+    assert np.all(np.isneginf(o.lse(zeros_q[:1], zeros_k[:1], MASK_PADDING,
+                                    np.array([0], np.int32))))
+    t = np.float32(1.0986123)
+    q = np.ones((1, 1, 1, 1), np.float32)
+    k = np.array([0.0, t], np.float32).reshape(1, 1, 2, 1)
+    got = o.lse(q, k, scale=1.0)[0, 0, 0]
+    assert abs(got - np.log1p(np.exp(np.float64(t)))) < 1e-12
+
+
+def pin_lse_rebuilds_softmax(o):
+    """exp(scale q_i.k_j - lse_i) are the softmax weights: with V the identity
+    (one value row per key) the attention output is exactly those weights."""
+    rng = np.random.default_rng(52)
+    b, h, n, d = 2, 2, 11, 5
+    q = (rng.standard_normal((b, h, n, d)) * 2).astype(np.float32)
+    k = rng.standard_normal((b, h, n, d)).astype(np.float32)
+    v = np.broadcast_to(np.eye(n, dtype=np.float32), (b, h, n, n)).copy()
+    lens = np.array([n, 6], np.int32)
+    for mask, r in ((MASK_NONE, None), (MASK_CAUSAL | MASK_PADDING, None), (MASK_PADDING, 4)):
+        weights = o.sdpa(q, k, v, mask, lens, window=r)
+        lse = o.lse(q, k, mask, lens, window=r)
+        s = np.einsum("bhid,bhjd->bhij", q.astype(np.float64), k.astype(np.float64)) / np.sqrt(d)
+        rebuilt = np.where(weights > 0, np.exp(s - lse[..., None]), 0.0)
+        assert np.allclose(rebuilt, weights, rtol=1e-12, atol=1e-15), mask
+
+
 PINS = [pin_worked_example, pin_worked_example_causal, pin_toy_rows, pin_scale_is_inverse_sqrt_dk,
         pin_rows_sum_to_one, pin_equal_scores_give_mean, pin_high_temperature_is_uniform,
         pin_shift_invariance, pin_causal_ignores_future, pin_padding_ignores_masked_keys,
@@ -529,4 +570,5 @@ PINS = [pin_worked_example, pin_worked_example_causal, pin_toy_rows, pin_scale_i
         pin_mha_single_head_identity, pin_mha_matches_matrix_form, pin_mha_concat_not_average,
         pin_mha_rows_selection, pin_restricted_worked_example, pin_restricted_extremes,
         pin_restricted_brute_force, pin_decode_matches_causal_rows, pin_decode_cache_lengths,
-        pin_backward_finite_differences, pin_backward_closed_forms]
+        pin_backward_finite_differences, pin_backward_closed_forms, pin_lse_closed_forms,
+        pin_lse_rebuilds_softmax]

@@ -43,6 +43,11 @@ MUTANTS = {
     "backward_ds_sign": ("double ds = prow[j] * (dprow[j] - Di);", "double ds = prow[j] * (dprow[j] + Di);"),
     "backward_dk_unscaled": ("dkj[x] += c->scale * ds * (double)qi[x];", "dkj[x] += ds * (double)qi[x];"),
     "backward_dv_uses_dp": ("dvj[x] += prow[j] * (double)doi[x];", "dvj[x] += dprow[j] * (double)doi[x];"),
+    "lse_drops_max": ("c->lse[r] = m + log(l);", "c->lse[r] = log(l);"),
+    "lse_log2": ("c->lse[r] = m + log(l);", "c->lse[r] = m + log2(l);"),
+    "lse_unscaled": ("s[j] = c->scale * dot;", "s[j] = dot;"),
+    "lse_causal_reversed": ("int visible = (j < len) && !(causal && j > i) && (j >= i - c->left)",
+                            "int visible = (j < len) && !(causal && j < i) && (j >= i - c->left)"),
     "mha_output_skips_wo": ("yr[o] += concat[t] * (double)wt[o];", "yr[o] += (o == t) ? concat[t] : 0.0;"),
 }
 
