@@ -83,6 +83,47 @@ sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v,
                                     void* stream);
 
 /*
+ * sdpa_forward that also returns, for the backward pass, each query row's
+ * natural log-sum-exp of its scaled, masked scores:
+ *   lse [b, h, n_q] fp32, device, written: lse_i = ln sum_{j visible} exp(scale q_i . k_j)
+ *   (-INFINITY for a row with no visible key).
+ * r = 0 is plain attention; r >= 1 is the restricted window of
+ * sdpa_forward_restricted.  Otherwise as sdpa_forward (lse 4-byte aligned).
+ */
+sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                             const int32_t* kv_lengths, int r, float scale, void* stream);
+
+/*
+ * Gradients of scaled dot-product attention, for training the model by
+ * back-propagation ("Attention Is All You Need", section 5, through Eq. (1)).
+ * With S = scale Q K^T (masked entries -inf), P = softmax(S) row-wise,
+ * O = P V and the upstream gradient dO:
+ *   dV = P^T dO,   dP = dO V^T,   dS = P o (dP - rowsum(dO o O)),
+ *   dQ = scale dS K,   dK = scale dS^T Q.
+ *   q, k, v, out  the forward's bf16 BHSD inputs and output, device
+ *   dout [b, h, n_q, d_v] bf16, device: the gradient of the loss w.r.t. out
+ *   lse  [b, h, n_q] fp32, device: sdpa_forward_lse's output for this call
+ *   dq [b, h, n_q, d_k], dk [b, h, n_k, d_k], dv [b, h, n_k, d_v] bf16,
+ *        device, written (must not overlap the inputs or one another)
+ *   workspace: device buffer of ws_bytes >= sdpa_backward_workspace_size(b, h,
+ *        n_q, d_k), 16-byte aligned, caller-owned (fp32 dQ accumulator and
+ *        per-row vectors); reusable once the stream passes the call.
+ *   mask_kind, kv_lengths, r, scale: the values given to the forward.
+ * P is recomputed from lse, never stored; the products run on the tensor
+ * cores with bf16 operands (P and dS rounded to bf16) and fp32 accumulation;
+ * dQ is accumulated in fp32 across key tiles, then rounded.  Hidden keys get
+ * zero gradient.  Supported: d_k == d_v in {64, 128}.
+ */
+size_t sdpa_backward_workspace_size(int b, int h, int n_q, int d);
+
+sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const void* out,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          void* workspace, size_t ws_bytes, int b, int h, int n_q, int n_k,
+                          int d_k, int d_v, int mask_kind, const int32_t* kv_lengths, int r,
+                          float scale, void* stream);
+
+/*
  * The same operation in fp32 throughout (fp32 inputs, exact fp32 exponentials
  * and sums on the CUDA cores), for small fp32 problems and the worked
  * examples.  Layouts as sdpa_forward with float elements; any

@@ -1,0 +1,171 @@
+"""Gradients of attention (training by back-propagation through Eq. (1)) on
+the tensor cores against the oracle's fp64 gradients.
+
+The forward's per-row log-sum-exp is checked against the oracle's to 1e-3
+absolute (it is a log of a sum of fp32 exponentials of exact bf16 products).
+The gradients use the measure of the forward tests: max|gpu - ref| / max|ref|
+per tensor, bar 2e-2.  The arithmetic behind that bar:
+  - P and dS enter the tensor cores rounded to bf16 (relative 2^-9 each).
+  - O enters D_i = dO_i . O_i as the forward's bf16 output.
+  - The results are rounded to bf16 once.
+All accumulation is fp32.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+import transformer_scaled_dot_02_gb300 as sd
+from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+
+pytestmark = pytest.mark.gpu
+
+LSE_TOL = 1e-3
+
+
+def _rand(rng, shape, std=1.0):
+    return synthetic.round_to_bf16(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+def _inputs(seed, b, h, n_q, n_k, d, std=1.0):
+    rng = np.random.default_rng(seed)
+    return (_rand(rng, (b, h, n_q, d), std), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d)),
+            _rand(rng, (b, h, n_q, d)))
+
+
+def _gpu_forward_backward(q, k, v, do, mask, lens, r=0, scale=0.0):
+    lens_d = None if lens is None else dev_int(lens)
+    qd, kd, vd, dod = dev(q), dev(k), dev(v), dev(do)
+    out, lse = sd.attention_with_lse(qd, kd, vd, mask, lens_d, r, scale)
+    dq, dk, dv = sd.attention_backward(qd, kd, vd, out, lse, dod, mask, lens_d, r, scale)
+    sd.sdpa_device_check()
+    return host(out), lse.double().cpu().numpy(), host(dq), host(dk), host(dv)
+
+
+def _check(q, k, v, do, mask, lens, r=0, scale=0.0):
+    out, lse, dq, dk, dv = _gpu_forward_backward(q, k, v, do, mask, lens, r, scale)
+    window = r or None
+    ref_out = oracle.sdpa(q, k, v, mask, lens, scale=scale, window=window)
+    ref_lse = oracle.lse(q, k, mask, lens, scale=scale, window=window)
+    rq, rk, rv = oracle.backward(q, k, v, do, mask, lens, scale=scale, window=window)
+    assert rel_err(out, ref_out) <= TOL_BF16
+    hidden = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), hidden)
+    if (~hidden).any():
+        assert np.abs(lse[~hidden] - ref_lse[~hidden]).max() <= LSE_TOL
+    errs = {"dq": rel_err(dq, rq), "dk": rel_err(dk, rk), "dv": rel_err(dv, rv)}
+    assert max(errs.values()) <= TOL_BF16, errs
+    return errs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask", [0, 1, 2, 3])
+def test_backward_shapes(d, mask):
+    b, h, n = 2, 3, 300
+    n_k = n if mask & 1 else 650
+    q, k, v, do = _inputs(9000 + d + mask, b, h, n, n_k, d)
+    lens = np.array([n_k, 171], np.int32) if mask & 2 else None
+    _check(q, k, v, do, mask, lens)
+
+
+@pytest.mark.parametrize("n", [1, 17, 127, 128, 129, 256, 383])
+def test_backward_ragged_lengths(n):
+    q, k, v, do = _inputs(9100 + n, 1, 2, n, n, 128)
+    _check(q, k, v, do, 1, None)
+
+
+@pytest.mark.parametrize("r", [1, 2, 64, 127, 129, 300])
+@pytest.mark.parametrize("mask", [0, 1, 3])
+def test_backward_restricted(r, mask):
+    b, h, n = 2, 2, 520
+    q, k, v, do = _inputs(9200 + r + mask, b, h, n, n, 64)
+    lens = np.array([n, 290], np.int32) if mask & 2 else None
+    _check(q, k, v, do, mask, lens, r=r)
+
+
+def test_backward_unscaled_and_sharp():
+    """scale 1 (the unscaled dot-product attention of section 3.2.1) with
+    larger queries: peaked softmax rows."""
+    q, k, v, do = _inputs(9300, 1, 2, 256, 256, 64, std=0.25)
+    _check(q, k, v, do, 0, None, scale=1.0)
+    q, k, v, do = _inputs(9301, 1, 2, 256, 256, 128, std=3.0)
+    _check(q, k, v, do, 1, None)
+
+
+def test_backward_empty_rows_and_sequences():
+    """A batch whose every key is hidden gives zero gradients (and lse
+    -inf); n_q = 0 gives dK = dV = 0; n_k = 0 gives dQ = 0."""
+    q, k, v, do = _inputs(9400, 2, 2, 200, 200, 64)
+    lens = np.array([0, 77], np.int32)
+    out, lse, dq, dk, dv = _gpu_forward_backward(q, k, v, do, 2, lens)
+    assert np.all(np.isneginf(lse[0])) and not np.isneginf(lse[1]).any()
+    assert not dq[0].any() and not dk[0].any() and not dv[0].any()
+    assert not dk[1, :, 77:].any() and not dv[1, :, 77:].any()
+    _check(q, k, v, do, 2, lens)
+
+    # n_q = 0 and n_k = 0 with valid one-row buffers the sizes leave unread
+    t = __import__("torch")
+    d = 64
+    one = dev(np.ones((1, 2, 1, d), np.float32))
+    lse1 = t.zeros((1, 2, 1), dtype=t.float32, device="cuda")
+    kd = dev(_rand(np.random.default_rng(1), (1, 2, 50, d)))
+    vd = dev(_rand(np.random.default_rng(2), (1, 2, 50, d)))
+    dk = t.full((1, 2, 50, d), 5.0, dtype=t.bfloat16, device="cuda")
+    dv = t.full((1, 2, 50, d), 5.0, dtype=t.bfloat16, device="cuda")
+    ws = t.empty(max(16, sd.sdpa_backward_workspace_size(1, 2, 0, d)), dtype=t.uint8, device="cuda")
+    sd.sdpa_backward(one, kd, vd, one, one, lse1, one.clone(), dk, dv, ws, ws.numel(), 1, 2, 0, 50,
+                     d, d)
+    sd.sdpa_device_check()
+    assert not dk.any().item() and not dv.any().item()
+
+    qd = dev(_rand(np.random.default_rng(3), (1, 2, 40, d)))
+    dod = dev(_rand(np.random.default_rng(4), (1, 2, 40, d)))
+    out = t.full((1, 2, 40, d), 5.0, dtype=t.bfloat16, device="cuda")
+    lse = t.zeros((1, 2, 40), dtype=t.float32, device="cuda")
+    sd.sdpa_forward_lse(qd, one, one, out, lse, 1, 2, 40, 0, d, d)
+    dq = t.full((1, 2, 40, d), 5.0, dtype=t.bfloat16, device="cuda")
+    ws = t.empty(sd.sdpa_backward_workspace_size(1, 2, 40, d), dtype=t.uint8, device="cuda")
+    sd.sdpa_backward(qd, one, one, out, dod, lse, dq, one.clone(), one.clone(), ws, ws.numel(), 1,
+                     2, 40, 0, d, d)
+    sd.sdpa_device_check()
+    assert not out.any().item() and not dq.any().item()
+    assert bool(t.isneginf(lse).all().item())
+
+
+def test_backward_matches_across_calls_and_reuses_workspace():
+    """Two calls on one workspace give the same gradients (the fp32 dQ
+    accumulator is cleared by each call); the order of the floating-point
+    reductions may differ, so equality is to 1e-6 of the scale."""
+    q, k, v, do = _inputs(9500, 2, 4, 384, 384, 128)
+    t = __import__("torch")
+    qd, kd, vd, dod = dev(q), dev(k), dev(v), dev(do)
+    out, lse = sd.attention_with_lse(qd, kd, vd, 1)
+    ws = t.empty(sd.sdpa_backward_workspace_size(2, 4, 384, 128), dtype=t.uint8, device="cuda")
+    a = sd.attention_backward(qd, kd, vd, out, lse, dod, 1, workspace=ws)
+    b = sd.attention_backward(qd, kd, vd, out, lse, dod, 1, workspace=ws)
+    sd.sdpa_device_check()
+    for x, y in zip(a, b):
+        assert rel_err(host(x), host(y)) <= 1e-2 * TOL_BF16
+
+
+def test_backward_long_causal_sampled():
+    """Causal b1 h4 n4096 d128 (many key tiles per query tile): every
+    gradient checked against the oracle."""
+    q, k, v, do = _inputs(9600, 1, 4, 4096, 4096, 128)
+    errs = _check(q, k, v, do, 1, None)
+    assert max(errs.values()) <= TOL_BF16
+
+
+def test_backward_rejects_bad_arguments():
+    t = __import__("torch")
+    x = t.zeros((1, 1, 64, 64), dtype=t.bfloat16, device="cuda")
+    lse = t.zeros((1, 1, 64), dtype=t.float32, device="cuda")
+    ws = t.empty(sd.sdpa_backward_workspace_size(1, 1, 64, 64), dtype=t.uint8, device="cuda")
+    with pytest.raises(sd.SdpaError, match="WORKSPACE"):
+        sd.sdpa_backward(x, x, x, x, x, lse, x, x, x, ws, ws.numel() - 16, 1, 1, 64, 64, 64, 64)
+    x32 = t.zeros((1, 1, 64, 32), dtype=t.bfloat16, device="cuda")
+    with pytest.raises(sd.SdpaError, match="UNSUPPORTED"):
+        sd.sdpa_backward(x32, x32, x32, x32, x32, lse, x32, x32, x32, ws, ws.numel(), 1, 1, 64, 64,
+                         32, 32)
+    with pytest.raises(sd.SdpaError, match="INVALID_ARG"):
+        sd.sdpa_backward(x, x, x, x, None, lse, x, x, x, ws, ws.numel(), 1, 1, 64, 64, 64, 64)

@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
                 6: "SDPA_ERR_DEVICE_TIMEOUT"}
 
 # Every symbol include/sdpa.h declares.
-EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_f32",
+EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_lse",
+           "sdpa_backward_workspace_size", "sdpa_backward", "sdpa_forward_f32",
            "sdpa_decode_workspace_size", "sdpa_decode", "mha_workspace_size",
            "mha_forward",
            "mha_forward_noalloc", "linear_forward", "sdpa_device_check", "sdpa_status_string")
@@ -60,6 +61,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sdpa_forward.restype = I
     lib.sdpa_forward_restricted.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P, I, F, P]
     lib.sdpa_forward_restricted.restype = I
+    lib.sdpa_forward_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, I, F, P]
+    lib.sdpa_forward_lse.restype = I
+    lib.sdpa_backward_workspace_size.argtypes = [I, I, I, I]
+    lib.sdpa_backward_workspace_size.restype = SZ
+    lib.sdpa_backward.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, P, I, F,
+                                  P]
+    lib.sdpa_backward.restype = I
     lib.sdpa_forward_f32.argtypes = attn
     lib.sdpa_forward_f32.restype = I
     lib.sdpa_decode_workspace_size.argtypes = [I, I, I, I, I]
@@ -120,6 +128,31 @@ def sdpa_forward_restricted(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SD
                                                   n_q, n_k, d_k, d_v, mask_kind,
                                                   _addr(kv_lengths), int(r), float(scale),
                                                   _stream(stream)), "sdpa_forward_restricted")
+
+
+def sdpa_forward_lse(q, k, v, out, lse, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE,
+                     kv_lengths=None, r=0, scale=0.0, stream=None) -> None:
+    """sdpa_forward (r = 0) or the restricted form (r >= 1) that also writes
+    each row's natural log-sum-exp into lse [b, h, n_q] fp32."""
+    _check(load_library().sdpa_forward_lse(_addr(q), _addr(k), _addr(v), _addr(out), _addr(lse), b,
+                                           h, n_q, n_k, d_k, d_v, mask_kind, _addr(kv_lengths),
+                                           int(r), float(scale), _stream(stream)),
+           "sdpa_forward_lse")
+
+
+def sdpa_backward_workspace_size(b, h, n_q, d) -> int:
+    return int(load_library().sdpa_backward_workspace_size(b, h, n_q, d))
+
+
+def sdpa_backward(q, k, v, out, dout, lse, dq, dk, dv, workspace, ws_bytes, b, h, n_q, n_k, d_k,
+                  d_v, mask_kind=SDPA_MASK_NONE, kv_lengths=None, r=0, scale=0.0,
+                  stream=None) -> None:
+    """Gradients dq, dk, dv of attention given dout and the forward's lse."""
+    _check(load_library().sdpa_backward(_addr(q), _addr(k), _addr(v), _addr(out), _addr(dout),
+                                        _addr(lse), _addr(dq), _addr(dk), _addr(dv),
+                                        _addr(workspace), int(ws_bytes), b, h, n_q, n_k, d_k, d_v,
+                                        mask_kind, _addr(kv_lengths), int(r), float(scale),
+                                        _stream(stream)), "sdpa_backward")
 
 
 def sdpa_forward_f32(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE,
@@ -228,3 +261,36 @@ def multi_head_attention(xq, xkv, wq, wk, wv, wo, h, mask_kind=SDPA_MASK_NONE, k
     mha_forward(xq, xkv, wq, wk, wv, wo, y, workspace, workspace.numel() * workspace.element_size(),
                 b, n_q, n_k, d_model, h, d_k, d_v, mask_kind, kv_lengths, scale, stream)
     return y
+
+
+def attention_with_lse(q, k, v, mask_kind=SDPA_MASK_NONE, kv_lengths=None, r=0, scale=0.0,
+                       stream=None):
+    """Allocates out [b,h,n_q,d] and lse [b,h,n_q] with torch and calls
+    sdpa_forward_lse on bf16 BHSD tensors; returns (out, lse)."""
+    import torch
+    b, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    out = torch.empty((b, h, n_q, d), dtype=q.dtype, device=q.device)
+    lse = torch.empty((b, h, n_q), dtype=torch.float32, device=q.device)
+    sdpa_forward_lse(q, k, v, out, lse, b, h, n_q, n_k, d, d, mask_kind, kv_lengths, r, scale,
+                     stream)
+    return out, lse
+
+
+def attention_backward(q, k, v, out, lse, dout, mask_kind=SDPA_MASK_NONE, kv_lengths=None, r=0,
+                       scale=0.0, workspace=None, stream=None):
+    """Allocates dq, dk, dv (and, if not given, the workspace) with torch and
+    calls sdpa_backward; returns (dq, dk, dv)."""
+    import torch
+    b, h, n_q, d = q.shape
+    n_k = k.shape[2]
+    need = sdpa_backward_workspace_size(b, h, n_q, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    sdpa_backward(q, k, v, out, dout, lse, dq, dk, dv, workspace,
+                  workspace.numel() * workspace.element_size(), b, h, n_q, n_k, d, d, mask_kind,
+                  kv_lengths, r, scale, stream)
+    return dq, dk, dv

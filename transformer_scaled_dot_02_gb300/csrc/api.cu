@@ -153,7 +153,7 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
                                 long long o_sn, long long o_sh, long long o_sb, int mask_kind,
                                 const int32_t* kv_lengths, float scale, unsigned* status,
                                 cudaStream_t stream, int win_left = sdpa::kWindowUnbounded,
-                                int win_right = sdpa::kWindowUnbounded) {
+                                int win_right = sdpa::kWindowUnbounded, float* lse = nullptr) {
   SdpaTcParams p;
   if (!make_map_4d(&p.tm_q, q, d, n_q, h, b, q_sn, q_sh, q_sb) ||
       !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb) ||
@@ -171,6 +171,7 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.scale_log2 = effective_scale(scale, d) * 1.4426950408889634f;
   p.win_left = win_left;
   p.win_right = win_right;
+  p.lse = lse;
   return sdpa::launch_sdpa_tc(p, d, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -227,6 +228,104 @@ sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v,
                              1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
                              1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
                              static_cast<cudaStream_t>(stream), left, right);
+}
+
+sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                             const int32_t* kv_lengths, int r, float scale, void* stream) {
+  sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
+                                        kv_lengths, scale);
+  if (st != SDPA_OK) return st;
+  if (lse == nullptr || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || r < 0)
+    return SDPA_ERR_INVALID_ARG;
+  if (d_k != d_v || !tc_head_size(d_k)) return SDPA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0) return SDPA_OK;
+  const long long d = d_k;
+  const int left = r > 0 ? (r - 1) / 2 : sdpa::kWindowUnbounded;
+  const int right = r > 0 ? r / 2 : sdpa::kWindowUnbounded;
+  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d, 1ll * n_q * d,
+                             1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
+                             1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
+                             static_cast<cudaStream_t>(stream), left, right, lse);
+}
+
+size_t sdpa_backward_workspace_size(int b, int h, int n_q, int d) {
+  if (b < 1 || h < 1 || n_q < 0 || d < 1) return 0;
+  const size_t rows_pad = static_cast<size_t>(b) * h * ((n_q + 127) / 128 * 128);
+  return 2 * round256(rows_pad * 4) + round256(static_cast<size_t>(b) * h * n_q * d * 4);
+}
+
+sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const void* out,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          void* workspace, size_t ws_bytes, int b, int h, int n_q, int n_k,
+                          int d_k, int d_v, int mask_kind, const int32_t* kv_lengths, int r,
+                          float scale, void* stream) {
+  sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
+                                        kv_lengths, scale);
+  if (st != SDPA_OK) return st;
+  if (dout == nullptr || lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || r < 0)
+    return SDPA_ERR_INVALID_ARG;
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return SDPA_ERR_UNSUPPORTED;
+  const size_t need = sdpa_backward_workspace_size(b, h, n_q, d_k);
+  if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return SDPA_ERR_WORKSPACE;
+  unsigned* status = nullptr;
+  st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0 && n_k == 0) return SDPA_OK;
+  const int d = d_k;
+  const int n_q_pad = (n_q + 127) / 128 * 128;
+  const size_t rows_pad = static_cast<size_t>(b) * h * n_q_pad;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(ws);
+  float* dvec = reinterpret_cast<float*>(ws + round256(rows_pad * 4));
+  float* dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows_pad * 4));
+  sdpa::SdpaBwdParams bp;
+  const long long dd = d;
+  if (!make_map_4d(&bp.tm_q, q, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd) ||
+      !make_map_4d(&bp.tm_k, k, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
+      !make_map_4d(&bp.tm_v, v, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
+      !make_map_4d(&bp.tm_do, dout, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd))
+    return SDPA_ERR_CUDA;
+  bp.lse2 = lse2;
+  bp.dvec = dvec;
+  bp.dq_acc = dq_acc;
+  bp.dk = static_cast<uint16_t*>(dk);
+  bp.dv = static_cast<uint16_t*>(dv);
+  bp.kv_lengths = (mask_kind & SDPA_MASK_PADDING) ? kv_lengths : nullptr;
+  bp.status = status;
+  bp.b = b;
+  bp.h = h;
+  bp.n_q = n_q;
+  bp.n_k = n_k;
+  bp.n_q_pad = n_q_pad;
+  bp.mask_kind = mask_kind;
+  bp.num_kv_tiles = (n_k + 127) / 128;
+  const float sc = effective_scale(scale, d);
+  bp.scale_log2 = sc * 1.4426950408889634f;
+  bp.scale = sc;
+  bp.win_left = r > 0 ? (r - 1) / 2 : sdpa::kWindowUnbounded;
+  bp.win_right = r > 0 ? r / 2 : sdpa::kWindowUnbounded;
+  sdpa::SdpaBwdPrepParams pp;
+  pp.out = static_cast<const uint16_t*>(out);
+  pp.dout = static_cast<const uint16_t*>(dout);
+  pp.lse = lse;
+  pp.lse2 = lse2;
+  pp.dvec = dvec;
+  pp.dq_acc = dq_acc;
+  pp.dq = static_cast<uint16_t*>(dq);
+  pp.b = b;
+  pp.h = h;
+  pp.n_q = n_q;
+  pp.n_q_pad = n_q_pad;
+  pp.scale = sc;
+  return sdpa::launch_sdpa_bwd(bp, pp, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SDPA_OK
+             : SDPA_ERR_CUDA;
 }
 
 sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* out, int b, int h,

@@ -25,6 +25,7 @@ struct SdpaTcParams {
   // Restricted attention: query i sees keys [i - win_left, i + win_right]
   // (kWindowUnbounded for plain attention).
   int win_left, win_right;
+  float* lse;                 // optional [b, h, n_q] natural log-sum-exp per row
 };
 constexpr int kWindowUnbounded = 1 << 30;
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
@@ -46,6 +47,30 @@ constexpr int kDecodeMinKeysPerSplit = 256;
 constexpr int kDecodeMaxSplits = 256;
 int decode_splits(int b, int h, int n_k);
 cudaError_t launch_sdpa_decode(const DecodeParams& p, int head_dim, cudaStream_t stream);
+
+// Gradients of attention (bf16 BHSD tensors, fp32 accumulation).
+struct SdpaBwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 4-D (d, n, h, b) maps, 64 x 128 boxes
+  const float* lse2;          // [b*h][n_q_pad] log-sum-exp in log2 units (+inf past n_q)
+  const float* dvec;          // [b*h][n_q_pad] D_i = dO_i . O_i
+  float* dq_acc;              // [b*h][n_q][d] fp32 accumulator (zeroed by the prep kernel)
+  uint16_t *dk, *dv;          // [b*h][n_k][d] bf16 outputs
+  const int32_t* kv_lengths;
+  unsigned* status;
+  int b, h, n_q, n_k, n_q_pad, mask_kind, num_kv_tiles;
+  float scale_log2, scale;
+  int win_left, win_right;
+};
+struct SdpaBwdPrepParams {
+  const uint16_t *out, *dout;  // forward output and its gradient, [b*h][n_q][d]
+  const float* lse;            // [b*h][n_q] natural log-sum-exp
+  float *lse2, *dvec, *dq_acc;
+  uint16_t* dq;                // [b*h][n_q][d] bf16 output
+  int b, h, n_q, n_q_pad;
+  float scale;
+};
+cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
+                            cudaStream_t stream);
 
 // Exact fp32 attention on the CUDA cores, BHSD contiguous.
 struct SdpaF32Params {

@@ -1,0 +1,475 @@
+// Gradients of scaled dot-product attention for training ("Attention Is All
+// You Need", section 5, applied to Eq. (1) of section 3.2.1).  With
+// S = scale Q K^T, P = softmax(S) (masked entries 0), O = P V and upstream
+// dO:
+//   dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P o (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+// P is recomputed from the forward's per-row log-sum-exp, never stored.
+//
+//   sdpa_bwd_prep      D_i = dO_i . O_i and the log-sum-exp in log2 units for
+//                      every query row (padded to whole 128-row tiles with
+//                      D = 0 and +inf, so padded rows get P = 0); zeroes the
+//                      fp32 dQ accumulator.
+//   sdpa_bwd_tc<D>     one CTA per (128-key tile, batch, head), walking the
+//                      query tiles that can see its keys:
+//     warp 8     TMA producer: K_j, V_j once; Q_i, dO_i and the tile's
+//                log-sum-exp / D vectors per query tile.
+//     warp 9     MMA issuer: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (keys in
+//                tensor-memory lanes); then dV += P^T dO_i and
+//                dK += dS^T Q_i with the A operand read from tensor memory,
+//                and dQ_i = dS K_j with dS read from shared memory.
+//     warps 0-3  one thread per key row: P^T = exp2(S^T scale log2e - lse2),
+//                dS^T = P^T o (dP^T - D), both packed to bf16 into tensor
+//                memory (over the columns already read) and dS^T also into
+//                shared memory; at the end dK, dV to global memory.
+//     warps 4-7  one thread per query row: the dQ_i partial from tensor
+//                memory added into the fp32 accumulator with vector
+//                reductions.
+//   sdpa_bwd_dq_convert  dQ = scale * accumulator, rounded to bf16.
+//
+// Tensor memory (512 columns): S^T at 0 (P^T bf16 over its first 64 columns),
+// dP^T at 128 (dS^T bf16 over its first 64, then the dQ partial), dV at 256,
+// dK at 256 + D.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+namespace {
+
+constexpr int kBM = 128;               // keys per CTA (tensor-memory lanes)
+constexpr int kBN = 128;               // queries per step
+constexpr int kBoxBytes = 128 * 128;   // one 64-column box of 128 rows
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;           // 128 rows x D bf16
+  static constexpr int kStages = (D == 128) ? 1 : 2;       // Q/dO ring depth
+  static constexpr int kVecBytes = 2 * kBN * 4;            // lse2 + D for one query tile
+  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kDsOff = 2 * kTileBytes;            // dS^T: 128 keys x 128 queries bf16
+  static constexpr int kStageOff = kDsOff + 128 * 128 * 2;
+  static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kNumBars = 1 + 2 * kStages + 6;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+  // S^T, dP^T: M = keys, N = queries, both operands K-major (K = d)
+  static constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
+  // dV, dK: A from tensor memory (K = queries), B MN-major (N = d)
+  static constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);
+  // dQ: A = dS MN-major (M = queries contiguous), B = K_j MN-major (N = d)
+  static constexpr uint32_t kIdescQ = idesc_bf16(kBN, D, true, true);
+};
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// Query tiles [i_lo, i_hi) holding a query that can see a key of this tile.
+__device__ __forceinline__ int2 query_range(const SdpaBwdParams& p, int key0, int kv_len) {
+  const int key_hi = min(key0 + kBM, kv_len) - 1;   // last valid key of the tile
+  if (key_hi < key0) return make_int2(0, 0);
+  // query i sees key j iff j in [i - left, i + right] (and j <= i if causal)
+  long long q_lo = static_cast<long long>(key0) - p.win_right;
+  if (p.mask_kind & 1) q_lo = q_lo > key0 ? q_lo : key0;
+  if (q_lo < 0) q_lo = 0;
+  long long q_hi = static_cast<long long>(key_hi) + p.win_left + 1;
+  if (q_hi > p.n_q) q_hi = p.n_q;
+  if (q_hi <= q_lo) return make_int2(0, 0);
+  return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc(const __grid_constant__ SdpaBwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  const uint32_t smem_base = smem_u32(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* kv_full = bar;
+  uint64_t* q_full = bar + 1;
+  uint64_t* q_empty = q_full + C::kStages;
+  uint64_t* s_full = q_empty + C::kStages;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dq_full = p_full + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* acc_full = dq_empty + 1;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const AbortState ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh_count = p.b * p.h;
+  const int jt = static_cast<int>(blockIdx.x) / bh_count;   // key tile (ascending: causal-heavy first)
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int bi = bh / p.h;
+  const int hi = bh % p.h;
+  const bool causal = (p.mask_kind & 1) != 0;
+  int kv_len = p.n_k;
+  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
+    kv_len = p.kv_lengths[bi];
+    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
+  }
+  const int key0 = jt * kBM;
+  const int2 qr = query_range(p, key0, kv_len);
+  const int i_lo = qr.x, n_it = qr.y - qr.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(q_full + s, 1);
+      mbar_init(q_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kBM);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, kBN);
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+      for (int c = 0; c < C::kBoxes; ++c) {
+        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * kBoxBytes, c * 64, key0, hi, bi);
+        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * kBoxBytes, c * 64, key0, hi, bi);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t use = static_cast<uint32_t>(it / C::kStages);
+        if (it >= C::kStages && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
+        uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
+        const int q0 = (i_lo + it) * kBN;
+        mbar_arrive_expect_tx(q_full + s, 2 * C::kTileBytes + C::kVecBytes);
+        for (int c = 0; c < C::kBoxes; ++c) {
+          tma_load_4d(&p.tm_q, q_full + s, st + c * kBoxBytes, c * 64, q0, hi, bi);
+          tma_load_4d(&p.tm_do, q_full + s, st + C::kTileBytes + c * kBoxBytes, c * 64, q0, hi, bi);
+        }
+        const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
+        tma_load_1d(st + 2 * C::kTileBytes, p.lse2 + vrow, kBN * 4, q_full + s);
+        tma_load_1d(st + 2 * C::kTileBytes + kBN * 4, p.dvec + vrow, kBN * 4, q_full + s);
+        issued = it + 1;
+      }
+      mbar_wait_drain(kv_full, 0);
+      for (int it = max(0, issued - C::kStages); it < issued; ++it)
+        mbar_wait_drain(q_full + it % C::kStages, static_cast<uint32_t>(it / C::kStages) & 1u);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n_it > 0) {
+      const uint32_t k_smem = smem_base + C::kKOff;
+      const uint32_t v_smem = smem_base + C::kVOff;
+      const uint32_t ds_smem = smem_base + C::kDsOff;
+      bool ok = mbar_wait(kv_full, 0, ab);
+      tc_fence_after();
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t st = smem_base + C::kStageOff + s * C::kStageBytes;
+        ok = mbar_wait(q_full + s, static_cast<uint32_t>(it / C::kStages) & 1u, ab);
+        if (!ok) break;
+        // dP^T overwrites the previous dQ partial: its epilogue must have read it
+        if (it > 0) {
+          ok = mbar_wait(dq_empty, static_cast<uint32_t>(it - 1) & 1u, ab);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        // S^T = K_j Q_i^T (cols 0..127), dP^T = V_j dO_i^T (cols 128..255)
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = static_cast<uint32_t>((k >> 2) * kBoxBytes + (k & 3) * 32);
+          mma_bf16_ss(tmem, smem_desc_sw128(k_smem + off, 16, 1024),
+                      smem_desc_sw128(st + off, 16, 1024), C::kIdescS, k > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + 128, smem_desc_sw128(v_smem + off, 16, 1024),
+                      smem_desc_sw128(st + C::kTileBytes + off, 16, 1024), C::kIdescS,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        ok = mbar_wait(p_full, static_cast<uint32_t>(it) & 1u, ab);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO_i, dK += dS^T Q_i (K = queries, 16 per step = 8 packed columns)
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
+          mma_bf16_ts(tmem + 256, tmem + static_cast<uint32_t>(k * 8),
+                      smem_desc_sw128(st + C::kTileBytes + roff, kBoxBytes, 1024), C::kIdescKV,
+                      (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + 256 + D, tmem + 128 + static_cast<uint32_t>(k * 8),
+                      smem_desc_sw128(st + roff, kBoxBytes, 1024), C::kIdescKV,
+                      (it > 0 || k > 0) ? 1u : 0u);
+        }
+        // dQ_i = dS K_j (K = keys, 16 per step)
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k) {
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
+          mma_bf16_ss(tmem + 128, smem_desc_sw128(ds_smem + roff, kBoxBytes, 1024),
+                      smem_desc_sw128(k_smem + roff, kBoxBytes, 1024), C::kIdescQ,
+                      k > 0 ? 1u : 0u);
+        }
+        mma_commit(dq_full);
+        mma_commit(q_empty + s);
+      }
+      if (ok) mma_commit(acc_full);
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------- P^T, dS^T (key rows)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int key = key0 + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % C::kStages;
+      const uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
+      const float* lse2 = reinterpret_cast<const float*>(st + 2 * C::kTileBytes);
+      const float* dvec = lse2 + kBN;
+      const int q0 = (i_lo + it) * kBN;
+      // the stage's vectors arrive with its Q/dO tiles on q_full
+      ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / C::kStages) & 1u, ab) &&
+           mbar_wait_warp(s_full, static_cast<uint32_t>(it) & 1u, ab);
+      if (!ok) break;
+      tc_fence_after();
+      // every (query, key) pair of the tile visible: no per-element mask
+      const int key_last = key0 + kBM - 1;
+      const bool full = key_last < kv_len && (!causal || key_last <= q0) &&
+                        key0 >= q0 + kBN - 1 - p.win_left && key_last <= q0 + p.win_right;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(lane_base + c * 32, sv);
+        tmem_ld32(lane_base + 128 + c * 32, dp);
+        tmem_ld_wait();
+        reg_fence(sv);
+        reg_fence(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int qi = c * 32 + e + u;
+            const int query = q0 + qi;
+            const bool visible = full || (key < kv_len && (!causal || key <= query) &&
+                                          key >= query - p.win_left && key <= query + p.win_right);
+            const float pp = visible
+                ? ex2_approx(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lse2[qi]))
+                : 0.f;
+            pv[u] = pp;
+            dsv[u] = pp * (__uint_as_float(dp[e + u]) - dvec[qi]);
+          }
+          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+          dk[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // over columns already read: P^T at [16c, 16c+16), dS^T at [128+16c, ...)
+        tmem_st16(lane_base + c * 16, pk);
+        tmem_st16(lane_base + 128 + c * 16, dk);
+        // dS^T row r, queries [32c, 32c+32) into the 128-byte-swizzled smem tile
+        uint8_t* box = smem + C::kDsOff + (c >> 1) * kBoxBytes;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint4 v = make_uint4(dk[q4 * 4 + 0], dk[q4 * 4 + 1], dk[q4 * 4 + 2], dk[q4 * 4 + 3]);
+          const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
+          *reinterpret_cast<uint4*>(box + sw128_offset(static_cast<uint32_t>(r), chunk)) = v;
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    // ---- dK (scaled) and dV rows of this key tile to global memory (the
+    // tensor-memory loads are warp-collective: only the stores are per row)
+    if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+      bool have = ok && n_it > 0;
+      if (have) {
+        have = mbar_wait_warp(acc_full, 0, ab);
+        tc_fence_after();
+      }
+      if (have || n_it == 0) {
+        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D;
+        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32], g[32];
+          if (have) {
+            tmem_ld32(lane_base + 256 + c * 32, a);
+            tmem_ld32(lane_base + 256 + D + c * 32, g);
+            tmem_ld_wait();
+            reg_fence(a);
+            reg_fence(g);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v, w;
+            v.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]), __uint_as_float(a[q4 * 8 + 1]));
+            v.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]), __uint_as_float(a[q4 * 8 + 3]));
+            v.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]), __uint_as_float(a[q4 * 8 + 5]));
+            v.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]), __uint_as_float(a[q4 * 8 + 7]));
+            w.x = pack_bf16x2(__uint_as_float(g[q4 * 8 + 0]) * p.scale, __uint_as_float(g[q4 * 8 + 1]) * p.scale);
+            w.y = pack_bf16x2(__uint_as_float(g[q4 * 8 + 2]) * p.scale, __uint_as_float(g[q4 * 8 + 3]) * p.scale);
+            w.z = pack_bf16x2(__uint_as_float(g[q4 * 8 + 4]) * p.scale, __uint_as_float(g[q4 * 8 + 5]) * p.scale);
+            w.w = pack_bf16x2(__uint_as_float(g[q4 * 8 + 6]) * p.scale, __uint_as_float(g[q4 * 8 + 7]) * p.scale);
+            if (key < p.n_k) {
+              *reinterpret_cast<uint4*>(dv_row + c * 32 + q4 * 8) = v;
+              *reinterpret_cast<uint4*>(dk_row + c * 32 + q4 * 8) = w;
+            }
+          }
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------- dQ partials (query rows)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int it = 0; it < n_it; ++it) {
+      if (!mbar_wait_warp(dq_full, static_cast<uint32_t>(it) & 1u, ab)) break;
+      tc_fence_after();
+      uint32_t a[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t t32[32];
+        tmem_ld32(lane_base + 128 + c * 32, t32);
+        tmem_ld_wait();
+        reg_fence(t32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a[c * 32 + e] = t32[e];
+      }
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int query = (i_lo + it) * kBN + r;
+      if (query < p.n_q) {
+        float* row = p.dq_acc + (static_cast<long long>(bh) * p.n_q + query) * D;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 4; ++c4)
+          red_add_v4(row + c4 * 4, __uint_as_float(a[c4 * 4 + 0]), __uint_as_float(a[c4 * 4 + 1]),
+                     __uint_as_float(a[c4 * 4 + 2]), __uint_as_float(a[c4 * 4 + 3]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// D_i = dO_i . O_i, lse2_i = lse_i * log2(e) (padded rows: 0 and +inf), dQ accumulator = 0.
+template <int D>
+__global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // over b*h*n_q_pad
+  const long long rows = static_cast<long long>(p.b) * p.h * p.n_q_pad;
+  if (row >= rows) return;
+  const long long bh = row / p.n_q_pad;
+  const int i = static_cast<int>(row % p.n_q_pad);
+  if (i >= p.n_q) {
+    if (lane == 0) {
+      p.dvec[row] = 0.f;
+      p.lse2[row] = INFINITY;
+    }
+    return;
+  }
+  const long long src = (bh * p.n_q + i) * D;
+  float acc = 0.f;
+  for (int c = lane; c < D; c += 32) {
+    const float o = __uint_as_float(static_cast<uint32_t>(p.out[src + c]) << 16);
+    const float g = __uint_as_float(static_cast<uint32_t>(p.dout[src + c]) << 16);
+    acc = fmaf(o, g, acc);
+    p.dq_acc[src + c] = 0.f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    p.dvec[row] = acc;
+    p.lse2[row] = p.lse[bh * p.n_q + i] * 1.4426950408889634f;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const SdpaBwdPrepParams p) {
+  const long long idx = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  const long long n = static_cast<long long>(p.b) * p.h * p.n_q * D;
+  if (idx >= n) return;
+  p.dq[idx] = static_cast<uint16_t>(pack_bf16x2(p.dq_acc[idx] * p.scale, 0.f) & 0xffffu);
+}
+
+template <int D>
+cudaError_t launch_d(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
+  cudaError_t err = cudaSuccess;
+  if (rows > 0) {
+    sdpa_bwd_prep<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(pp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  const int smem = BwdCfg<D>::kSmemBytes;
+  err = cudaFuncSetAttribute(sdpa_bwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
+  if (blocks > 0) {
+    sdpa_bwd_tc<D><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(bp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * D;
+  if (n > 0) sdpa_bwd_dq_convert<D><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(pp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
+                            cudaStream_t stream) {
+  if (head_dim == 64) return launch_d<64>(bp, pp, stream);
+  if (head_dim == 128) return launch_d<128>(bp, pp, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sdpa

@@ -488,6 +488,11 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       }
       if (have_o || (ok && n_t == 0)) {
         const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
+        if (p.lse != nullptr && row < p.n_q) {
+          // natural log-sum-exp of the row's scaled scores (for the backward)
+          p.lse[static_cast<long long>(bh) * p.n_q + row] =
+              (have_o && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
 #pragma unroll
         for (int c = 0; c < D / C::kOChunk; ++c) {
           uint32_t o[C::kOChunk];
