@@ -83,7 +83,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
 // boxes of min(d, 64) x 128, swizzled at the row width, zero fill outside.
 bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
-                 long long stride_n, long long stride_h, long long stride_b) {
+                 long long stride_n, long long stride_h, long long stride_b, int box_rows = 128) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n > 0 ? n : 1),
@@ -92,7 +92,8 @@ bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
                                  static_cast<cuuint64_t>(stride_h) * 2,
                                  static_cast<cuuint64_t>(stride_b) * 2};
   // boxes of min(d, 64) columns: rows of 128, 64 or 32 bytes, swizzled at that width
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d < 64 ? d : 64), 128, 1, 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(d < 64 ? d : 64),
+                             static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle swz = d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                          : (d == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -286,10 +287,12 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   float* dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows_pad * 4));
   sdpa::SdpaBwdParams bp;
   const long long dd = d;
-  if (!make_map_4d(&bp.tm_q, q, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd) ||
+  // head size 128 steps through the queries 64 at a time
+  const int q_rows = d == 128 ? 64 : 128;
+  if (!make_map_4d(&bp.tm_q, q, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd, q_rows) ||
       !make_map_4d(&bp.tm_k, k, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
       !make_map_4d(&bp.tm_v, v, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
-      !make_map_4d(&bp.tm_do, dout, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd))
+      !make_map_4d(&bp.tm_do, dout, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd, q_rows))
     return SDPA_ERR_CUDA;
   bp.lse2 = lse2;
   bp.dvec = dvec;

@@ -400,6 +400,416 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc(const __grid_constant
   }
 }
 
+// ------------------------------------------------------------------------
+// Head size 128: 64-query steps with S^T / dP^T double-buffered in tensor
+// memory, so the tensor core computes the next step's products while the
+// compute warps turn the current ones into P^T and dS^T.
+//   warps 0-7  compute: warp w serves key lanes 32 (w % 4) .. +32 and query
+//              half w / 4 (32 queries) of each step; it also moves its share
+//              of the previous step's dQ^T into the shared staging tile.
+//   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i, lse2, D in 3 stages).
+//   warp 9     MMA issuer, in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T(i).
+// Tensor memory: buffer b = step & 1 holds S^T at 128 b (64 columns; P^T in
+// bf16 over columns 128 b + 32 h .. +16 of each half h) and dP^T at
+// 128 b + 64 (dS^T in bf16 the same way; then dQ^T = K^T dS^T, keyed by d),
+// dV at 256, dK at 384.  dQ^T leaves through a 32 KB fp32 staging tile and
+// one bulk reduce-add into the fp32 dQ accumulator per step.
+namespace n64 {
+
+constexpr int D = 128;
+constexpr int kBM = 128;                 // keys per CTA
+constexpr int kBN = 64;                  // queries per step
+constexpr int kStages = 3;
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;            // warps 0-7
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kKVBox = 128 * 128;        // 64 columns x 128 rows bf16
+constexpr int kQBox = 64 * 128;          // 64 columns x 64 rows bf16
+constexpr int kKVTile = 2 * kKVBox;
+constexpr int kQTile = 2 * kQBox;
+constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (128-byte rows)
+constexpr int kVecBytes = 2 * kBN * 4;   // lse2 and D of one step
+constexpr int kKOff = 0;
+constexpr int kVOff = kKVTile;
+constexpr int kStageOff = 2 * kKVTile;                    // Q, dO per stage
+constexpr int kDsOff = kStageOff + kStages * 2 * kQTile;  // two dS^T buffers
+constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // dQ rows: 64 x 128 fp32
+constexpr int kVecOff = kStagingOff + kBN * D * 4;
+constexpr int kBarOff = kVecOff + kStages * kVecBytes;
+// kv_full, q_full[3], q_empty[3], s_full[2], p_full[2], dq_full[2],
+// dq_empty[2], staging_full, staging_free, acc_full, drain
+constexpr int kNumBars = 1 + 2 * kStages + 8 + 4;
+constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
+
+constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
+constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);     // dV, dK (A in TMEM)
+constexpr uint32_t kIdescQ = idesc_bf16(D, kBN, true, true);       // dQ^T = K^T dS^T
+
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Query steps [i_lo, i_hi) of 64 holding a query that can see a key of this tile.
+__device__ __forceinline__ int2 query_steps(const SdpaBwdParams& p, int key0, int kv_len) {
+  const int key_hi = min(key0 + kBM, kv_len) - 1;
+  if (key_hi < key0) return make_int2(0, 0);
+  long long q_lo = static_cast<long long>(key0) - p.win_right;
+  if (p.mask_kind & 1) q_lo = q_lo > key0 ? q_lo : key0;
+  if (q_lo < 0) q_lo = 0;
+  long long q_hi = static_cast<long long>(key_hi) + p.win_left + 1;
+  if (q_hi > p.n_q) q_hi = p.n_q;
+  if (q_hi <= q_lo) return make_int2(0, 0);
+  return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_constant__ SdpaBwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  const uint32_t smem_base = smem_u32(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* kv_full = bar;
+  uint64_t* q_full = bar + 1;
+  uint64_t* q_empty = q_full + kStages;
+  uint64_t* s_full = q_empty + kStages;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* dq_full = p_full + 2;
+  uint64_t* dq_empty = dq_full + 2;
+  uint64_t* staging_full = dq_empty + 2;
+  uint64_t* staging_free = staging_full + 1;
+  uint64_t* acc_full = staging_free + 1;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const AbortState ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh_count = p.b * p.h;
+  const int jt = static_cast<int>(blockIdx.x) / bh_count;
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int bi = bh / p.h;
+  const int hi = bh % p.h;
+  const bool causal = (p.mask_kind & 1) != 0;
+  int kv_len = p.n_k;
+  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
+    kv_len = p.kv_lengths[bi];
+    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
+  }
+  const int key0 = jt * kBM;
+  const int2 qr = query_steps(p, key0, kv_len);
+  const int i_lo = qr.x, n_it = qr.y - qr.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(q_full + s, 1);
+      mbar_init(q_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, kCompute);
+      mbar_init(dq_full + b, 1);
+      mbar_init(dq_empty + b, kCompute);
+    }
+    mbar_init(staging_full, kCompute);
+    mbar_init(staging_free, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * kKVTile);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_4d(&p.tm_k, kv_full, smem + kKOff + c * kKVBox, c * 64, key0, hi, bi);
+        tma_load_4d(&p.tm_v, kv_full, smem + kVOff + c * kKVBox, c * 64, key0, hi, bi);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % kStages;
+        const uint32_t use = static_cast<uint32_t>(it / kStages);
+        if (it >= kStages && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
+        uint8_t* st = smem + kStageOff + s * 2 * kQTile;
+        const int q0 = (i_lo + it) * kBN;
+        mbar_arrive_expect_tx(q_full + s, 2 * kQTile + kVecBytes);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_4d(&p.tm_q, q_full + s, st + c * kQBox, c * 64, q0, hi, bi);
+          tma_load_4d(&p.tm_do, q_full + s, st + kQTile + c * kQBox, c * 64, q0, hi, bi);
+        }
+        const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
+        uint8_t* vec = smem + kVecOff + s * kVecBytes;
+        tma_load_1d(vec, p.lse2 + vrow, kBN * 4, q_full + s);
+        tma_load_1d(vec + kBN * 4, p.dvec + vrow, kBN * 4, q_full + s);
+        issued = it + 1;
+      }
+      mbar_wait_drain(kv_full, 0);
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        mbar_wait_drain(q_full + it % kStages, static_cast<uint32_t>(it / kStages) & 1u);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n_it > 0) {
+      const uint32_t k_smem = smem_base + kKOff;
+      const uint32_t v_smem = smem_base + kVOff;
+      // S^T(it) = K_j Q_i^T and dP^T(it) = V_j dO_i^T into buffer it & 1
+      auto issue_s = [&](int it, bool dp) {
+        const uint32_t st = smem_base + kStageOff + (it % kStages) * 2 * kQTile + (dp ? kQTile : 0);
+        const uint32_t a_base = dp ? v_smem : k_smem;
+        const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          mma_bf16_ss(d,
+                      smem_desc_sw128(a_base + (k >> 2) * kKVBox + (k & 3) * 32, 16, 1024),
+                      smem_desc_sw128(st + (k >> 2) * kQBox + (k & 3) * 32, 16, 1024), kIdescS,
+                      k > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, ab) && mbar_wait(q_full, 0, ab);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0, false);
+        issue_s(0, true);
+        mma_commit(s_full);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int b = it & 1;
+        if (it + 1 < n_it) {
+          const int nx = it + 1;
+          ok = mbar_wait(q_full + nx % kStages, static_cast<uint32_t>(nx / kStages) & 1u, ab);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(nx, false);
+          // dP^T(it+1) lands where dQ^T(it-1) was: its epilogue must have read it
+          if (it >= 1) {
+            ok = mbar_wait(dq_empty + (nx & 1), static_cast<uint32_t>((it - 1) >> 1) & 1u, ab);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          issue_s(nx, true);
+          mma_commit(s_full + (nx & 1));
+        }
+        ok = mbar_wait(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = smem_base + kStageOff + (it % kStages) * 2 * kQTile;
+        const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
+        // dV += P^T dO_i, dK += dS^T Q_i: 16 queries per step; queries
+        // [32h, 32h+32) sit in columns 32h .. 32h+16 of the S^T / dP^T halves
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {
+          const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
+          mma_bf16_ts(tmem + 256, buf + col, smem_desc_sw128(st + kQTile + roff, kQBox, 1024),
+                      kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + 384, buf + 64 + col, smem_desc_sw128(st + roff, kQBox, 1024),
+                      kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(q_empty + it % kStages);
+        // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
+        const uint32_t ds = smem_base + kDsOff + b * kDsTile;
+#pragma unroll
+        for (int k = 0; k < kBM / 16; ++k) {
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
+          mma_bf16_ss(buf + 64, smem_desc_sw128(k_smem + roff, kKVBox, 1024),
+                      smem_desc_sw128(ds + roff, kDsTile, 1024), kIdescQ, k > 0 ? 1u : 0u);
+        }
+        mma_commit(dq_full + b);
+      }
+      if (ok) mma_commit(acc_full);
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------- compute warps
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int r = quarter * 32 + lane;                // key lane, and d lane of dQ^T
+    const int key = key0 + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* staging = reinterpret_cast<float*>(smem + kStagingOff);
+    bool ok = true;
+
+    // dQ^T(j) columns of this warp -> staging rows 32 half .. +32, column r;
+    // then one thread adds the tile into the fp32 accumulator.
+    auto epilogue = [&](int j) -> bool {
+      const int b = j & 1;
+      if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) return false;
+      tc_fence_after();
+      uint32_t g[32];
+      tmem_ld32(lane_base + static_cast<uint32_t>(b * 128 + 64 + half * 32), g);
+      tmem_ld_wait();
+      reg_fence(g);
+      tc_fence_before();
+      mbar_arrive(dq_empty + b);
+      if (j >= 1) {
+        if (threadIdx.x == 0) {
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          mbar_arrive(staging_free);
+        }
+        if (!mbar_wait_warp(staging_free, static_cast<uint32_t>(j - 1) & 1u, ab)) return false;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) staging[(half * 32 + e) * D + r] = __uint_as_float(g[e]);
+      fence_proxy_async_smem();
+      mbar_arrive(staging_full);
+      bool good = true;
+      if (threadIdx.x == 0) {
+        good = mbar_wait(staging_full, static_cast<uint32_t>(j) & 1u, ab);
+        const int q0 = (i_lo + j) * kBN;
+        const int rows = min(kBN, p.n_q - q0);
+        if (good && rows > 0)
+          bulk_reduce_add_f32(p.dq_acc + (static_cast<long long>(bh) * p.n_q + q0) * D, staging,
+                              static_cast<uint32_t>(rows) * D * 4);
+        tma_store_commit();
+      }
+      // lane 0 of warp 0 decided alone: make the answer warp-uniform there
+      if (warp == 0) good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      return good;
+    };
+
+    for (int it = 0; it < n_it; ++it) {
+      const int b = it & 1;
+      const int s = it % kStages;
+      ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / kStages) & 1u, ab) &&
+           mbar_wait_warp(s_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
+      if (!ok) break;
+      tc_fence_after();
+      const int qh0 = (i_lo + it) * kBN + half * 32;
+      const float* lse2 = reinterpret_cast<const float*>(smem + kVecOff + s * kVecBytes) + half * 32;
+      const float* dvec = lse2 + kBN;
+      // this key sees every query of its half: no per-element mask
+      const bool full = key < kv_len && (!causal || key <= qh0) && key >= qh0 + 31 - p.win_left &&
+                        key <= qh0 + p.win_right;
+      const uint32_t s_col = static_cast<uint32_t>(b * 128 + half * 32);
+      uint32_t sv[32], dp[32];
+      tmem_ld32(lane_base + s_col, sv);
+      tmem_ld32(lane_base + s_col + 64, dp);
+      tmem_ld_wait();
+      reg_fence(sv);
+      reg_fence(dp);
+      uint32_t pk[16], dk[16];
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + e4 * 4);
+        const float4 d4 = *reinterpret_cast<const float4*>(dvec + e4 * 4);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e4 * 4 + u;
+          const int query = qh0 + e;
+          const bool visible = full || (key < kv_len && (!causal || key <= query) &&
+                                        key >= query - p.win_left && key <= query + p.win_right);
+          const float pp =
+              visible ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -lv[u])) : 0.f;
+          pv[u] = pp;
+          dsv[u] = pp * (__uint_as_float(dp[e]) - dv4[u]);
+        }
+        pk[e4 * 2] = pack_bf16x2(pv[0], pv[1]);
+        pk[e4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+        dk[e4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
+        dk[e4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+      }
+      tmem_st16(lane_base + s_col, pk);
+      tmem_st16(lane_base + s_col + 64, dk);
+      // dS^T row r, queries [32 half, +32): 16-byte chunks 4 half .. +4 of the 128-byte row
+      uint8_t* dsb = smem + kDsOff + b * kDsTile;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = make_uint4(dk[c * 4 + 0], dk[c * 4 + 1], dk[c * 4 + 2], dk[c * 4 + 3]);
+        *reinterpret_cast<uint4*>(dsb + sw128_offset(static_cast<uint32_t>(r),
+                                                     static_cast<uint32_t>(half * 4 + c))) = v;
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full + b);
+      if (it >= 1 && !epilogue(it - 1)) {
+        ok = false;
+        break;
+      }
+    }
+    if (ok && n_it > 0) ok = epilogue(n_it - 1);
+    // ---- dK (scaled) and dV rows: warp half h takes columns [64h, 64h+64)
+    if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+      bool have = ok && n_it > 0;
+      if (have) {
+        have = mbar_wait_warp(acc_full, 0, ab);
+        tc_fence_after();
+      }
+      if (have || n_it == 0) {
+        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D + half * 64;
+        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D + half * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t a[32], g[32];
+          if (have) {
+            tmem_ld32(lane_base + 256 + half * 64 + c * 32, a);
+            tmem_ld32(lane_base + 384 + half * 64 + c * 32, g);
+            tmem_ld_wait();
+            reg_fence(a);
+            reg_fence(g);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v, w;
+            v.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]), __uint_as_float(a[q4 * 8 + 1]));
+            v.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]), __uint_as_float(a[q4 * 8 + 3]));
+            v.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]), __uint_as_float(a[q4 * 8 + 5]));
+            v.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]), __uint_as_float(a[q4 * 8 + 7]));
+            w.x = pack_bf16x2(__uint_as_float(g[q4 * 8 + 0]) * p.scale,
+                              __uint_as_float(g[q4 * 8 + 1]) * p.scale);
+            w.y = pack_bf16x2(__uint_as_float(g[q4 * 8 + 2]) * p.scale,
+                              __uint_as_float(g[q4 * 8 + 3]) * p.scale);
+            w.z = pack_bf16x2(__uint_as_float(g[q4 * 8 + 4]) * p.scale,
+                              __uint_as_float(g[q4 * 8 + 5]) * p.scale);
+            w.w = pack_bf16x2(__uint_as_float(g[q4 * 8 + 6]) * p.scale,
+                              __uint_as_float(g[q4 * 8 + 7]) * p.scale);
+            if (key < p.n_k) {
+              *reinterpret_cast<uint4*>(dv_row + c * 32 + q4 * 8) = v;
+              *reinterpret_cast<uint4*>(dk_row + c * 32 + q4 * 8) = w;
+            }
+          }
+        }
+      }
+    }
+    if (threadIdx.x == 0) bulk_wait_all();   // the last reduce has finished
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace n64
+
 // D_i = dO_i . O_i, lse2_i = lse_i * log2(e) (padded rows: 0 and +inf), dQ accumulator = 0.
 template <int D>
 __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
@@ -463,12 +873,36 @@ cudaError_t launch_d(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaS
   return cudaGetLastError();
 }
 
+cudaError_t launch_d128(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp,
+                        cudaStream_t stream) {
+  const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
+  cudaError_t err = cudaSuccess;
+  if (rows > 0) {
+    sdpa_bwd_prep<128><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(pp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             n64::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
+  if (blocks > 0) {
+    n64::sdpa_bwd_tc_n64<<<static_cast<unsigned>(blocks), n64::kThreads, n64::kSmemBytes, stream>>>(
+        bp);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * 128;
+  if (n > 0) sdpa_bwd_dq_convert<128><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(pp);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
                             cudaStream_t stream) {
   if (head_dim == 64) return launch_d<64>(bp, pp, stream);
-  if (head_dim == 128) return launch_d<128>(bp, pp, stream);
+  if (head_dim == 128) return launch_d128(bp, pp, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -5,9 +5,12 @@ C ABI, for profiling a single kernel launch under a profiler.
     python -m transformer_scaled_dot_02_gb300.profile --mha --b 32 --n 128 --d-model 512 --h 8
     python -m transformer_scaled_dot_02_gb300.profile --decode --b 32 --h 16 --n 1 --nk 8192 --d 128
     python -m transformer_scaled_dot_02_gb300.profile --restricted 1024 --b 4 --h 16 --n 8192 --mask 1
+    python -m transformer_scaled_dot_02_gb300.profile --backward --b 4 --h 16 --n 8192 --mask 1
 
 Inputs are seeded N(0,1) bf16 values made on the device; nothing is checked.
-Prints the mean launch time measured with CUDA events.
+Prints the mean call time measured with CUDA events; for plain attention
+and the backward also TFLOP/s counting 4 (forward) or 10 (backward: five
+products) b h n_q n_k d FLOP per call, halved when causal.
 """
 from __future__ import annotations
 
@@ -30,6 +33,7 @@ def main():
     ap.add_argument("--mha", action="store_true", help="multi-head attention with projections")
     ap.add_argument("--decode", action="store_true", help="one decoding step: --n new queries, --nk cache")
     ap.add_argument("--restricted", type=int, default=0, help="neighbourhood size r (restricted)")
+    ap.add_argument("--backward", action="store_true", help="the gradients (after one forward)")
     ap.add_argument("--d-model", type=int, default=512)
     ap.add_argument("--iters", type=int, default=3)
     a = ap.parse_args()
@@ -64,6 +68,17 @@ def main():
 
         def run():
             sd.multi_head_attention(xq, xkv, *ws, a.h, a.mask, lens, workspace=work)
+    elif a.backward:
+        q, k, v, dout = (torch.randn(a.b, a.h, n, a.d, device=dev).to(torch.bfloat16)
+                         for n in (n_q, n_k, n_k, n_q))
+        out, lse = sd.attention_with_lse(q, k, v, a.mask, lens, a.restricted)
+        grads = [torch.empty_like(x) for x in (q, k, v)]
+        work = torch.empty(sd.sdpa_backward_workspace_size(a.b, a.h, n_q, a.d), dtype=torch.uint8,
+                           device=dev)
+
+        def run():
+            sd.sdpa_backward(q, k, v, out, dout, lse, *grads, work, work.numel(), a.b, a.h, n_q,
+                             n_k, a.d, a.d, a.mask, lens, a.restricted)
     else:
         q = torch.randn(a.b, a.h, n_q, a.d, device=dev).to(torch.bfloat16)
         k = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
@@ -85,7 +100,12 @@ def main():
     e.record()
     torch.cuda.synchronize()
     sd.sdpa_device_check()
-    print("mean %.4f ms per call over %d calls" % (s.elapsed_time(e) / a.iters, a.iters))
+    ms = s.elapsed_time(e) / a.iters
+    line = "mean %.4f ms per call over %d calls" % (ms, a.iters)
+    if not (a.mha or a.decode or a.restricted):
+        flops = (10 if a.backward else 4) * a.b * a.h * n_q * n_k * a.d * (0.5 if a.mask & 1 else 1)
+        line += ", %.1f TFLOP/s" % (flops / (ms * 1e-3) / 1e12)
+    print(line)
 
 
 if __name__ == "__main__":
