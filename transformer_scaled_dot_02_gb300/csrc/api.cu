@@ -287,8 +287,8 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   float* dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows_pad * 4));
   sdpa::SdpaBwdParams bp;
   const long long dd = d;
-  // head size 128 steps through the queries 64 at a time
-  const int q_rows = d == 128 ? 64 : 128;
+  // the backward steps through the queries 64 at a time
+  const int q_rows = 64;
   if (!make_map_4d(&bp.tm_q, q, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd, q_rows) ||
       !make_map_4d(&bp.tm_k, k, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
       !make_map_4d(&bp.tm_v, v, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||

@@ -6,30 +6,19 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 // P is recomputed from the forward's per-row log-sum-exp, never stored.
 //
-//   sdpa_bwd_prep      D_i = dO_i . O_i and the log-sum-exp in log2 units for
-//                      every query row (padded to whole 128-row tiles with
-//                      D = 0 and +inf, so padded rows get P = 0); zeroes the
-//                      fp32 dQ accumulator.
-//   sdpa_bwd_tc<D>     one CTA per (128-key tile, batch, head), walking the
-//                      query tiles that can see its keys:
-//     warp 8     TMA producer: K_j, V_j once; Q_i, dO_i and the tile's
-//                log-sum-exp / D vectors per query tile.
-//     warp 9     MMA issuer: S^T = K_j Q_i^T and dP^T = V_j dO_i^T (keys in
-//                tensor-memory lanes); then dV += P^T dO_i and
-//                dK += dS^T Q_i with the A operand read from tensor memory,
-//                and dQ_i = dS K_j with dS read from shared memory.
-//     warps 0-3  one thread per key row: P^T = exp2(S^T scale log2e - lse2),
-//                dS^T = P^T o (dP^T - D), both packed to bf16 into tensor
-//                memory (over the columns already read) and dS^T also into
-//                shared memory; at the end dK, dV to global memory.
-//     warps 4-7  one thread per query row: the dQ_i partial from tensor
-//                memory added into the fp32 accumulator with vector
-//                reductions.
+//   sdpa_bwd_prep        D_i = dO_i . O_i and the log-sum-exp in log2 units
+//                        for every query row (padded to whole 128-row tiles
+//                        with D = 0 and +inf, so padded rows get P = 0);
+//                        zeroes the fp32 dQ accumulator.
+//   sdpa_bwd_tc_n64<D>   one CTA per (128-key tile, batch, head), walking in
+//                        steps of 64 the queries that can see its keys; dK
+//                        and dV accumulate in tensor memory, dQ leaves each
+//                        step as a bulk reduce-add into the accumulator.
 //   sdpa_bwd_dq_convert  dQ = scale * accumulator, rounded to bf16.
 //
-// Tensor memory (512 columns): S^T at 0 (P^T bf16 over its first 64 columns),
-// dP^T at 128 (dS^T bf16 over its first 64, then the dQ partial), dV at 256,
-// dK at 256 + D.
+// Everything runs in the transposed frame, with the keys of the CTA in
+// tensor-memory lanes.  The five products per step are
+// S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q and dQ^T = K^T dS^T.
 #include <cmath>
 
 #include "kernels.h"
@@ -37,36 +26,6 @@
 
 namespace sdpa {
 namespace {
-
-constexpr int kBM = 128;               // keys per CTA (tensor-memory lanes)
-constexpr int kBN = 128;               // queries per step
-constexpr int kBoxBytes = 128 * 128;   // one 64-column box of 128 rows
-constexpr int kThreads = 384;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
-
-template <int D>
-struct BwdCfg {
-  static constexpr int kBoxes = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;           // 128 rows x D bf16
-  static constexpr int kStages = (D == 128) ? 1 : 2;       // Q/dO ring depth
-  static constexpr int kVecBytes = 2 * kBN * 4;            // lse2 + D for one query tile
-  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kTileBytes;
-  static constexpr int kDsOff = 2 * kTileBytes;            // dS^T: 128 keys x 128 queries bf16
-  static constexpr int kStageOff = kDsOff + 128 * 128 * 2;
-  static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kNumBars = 1 + 2 * kStages + 6;
-  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-  // S^T, dP^T: M = keys, N = queries, both operands K-major (K = d)
-  static constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);
-  // dV, dK: A from tensor memory (K = queries), B MN-major (N = d)
-  static constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);
-  // dQ: A = dS MN-major (M = queries contiguous), B = K_j MN-major (N = d)
-  static constexpr uint32_t kIdescQ = idesc_bf16(kBN, D, true, true);
-};
 
 template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
@@ -83,327 +42,10 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
-// Query tiles [i_lo, i_hi) holding a query that can see a key of this tile.
-__device__ __forceinline__ int2 query_range(const SdpaBwdParams& p, int key0, int kv_len) {
-  const int key_hi = min(key0 + kBM, kv_len) - 1;   // last valid key of the tile
-  if (key_hi < key0) return make_int2(0, 0);
-  // query i sees key j iff j in [i - left, i + right] (and j <= i if causal)
-  long long q_lo = static_cast<long long>(key0) - p.win_right;
-  if (p.mask_kind & 1) q_lo = q_lo > key0 ? q_lo : key0;
-  if (q_lo < 0) q_lo = 0;
-  long long q_hi = static_cast<long long>(key_hi) + p.win_left + 1;
-  if (q_hi > p.n_q) q_hi = p.n_q;
-  if (q_hi <= q_lo) return make_int2(0, 0);
-  return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
-}
-
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc(const __grid_constant__ SdpaBwdParams p) {
-  using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_u32 = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
-  const uint32_t smem_base = smem_u32(smem);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* kv_full = bar;
-  uint64_t* q_full = bar + 1;
-  uint64_t* q_empty = q_full + C::kStages;
-  uint64_t* s_full = q_empty + C::kStages;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* dq_full = p_full + 1;
-  uint64_t* dq_empty = dq_full + 1;
-  uint64_t* acc_full = dq_empty + 1;
-  uint64_t* drain = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const AbortState ab{abort_flag, p.status};
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int bh_count = p.b * p.h;
-  const int jt = static_cast<int>(blockIdx.x) / bh_count;   // key tile (ascending: causal-heavy first)
-  const int bh = static_cast<int>(blockIdx.x) % bh_count;
-  const int bi = bh / p.h;
-  const int hi = bh % p.h;
-  const bool causal = (p.mask_kind & 1) != 0;
-  int kv_len = p.n_k;
-  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
-    kv_len = p.kv_lengths[bi];
-    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
-  }
-  const int key0 = jt * kBM;
-  const int2 qr = query_range(p, key0, kv_len);
-  const int i_lo = qr.x, n_it = qr.y - qr.x;
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(q_full + s, 1);
-      mbar_init(q_empty + s, 1);
-    }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, kBM);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, kBN);
-    mbar_init(acc_full, 1);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == kProducerWarp) {
-    if (lane == 0 && n_it > 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
-      for (int c = 0; c < C::kBoxes; ++c) {
-        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * kBoxBytes, c * 64, key0, hi, bi);
-        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * kBoxBytes, c * 64, key0, hi, bi);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t use = static_cast<uint32_t>(it / C::kStages);
-        if (it >= C::kStages && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
-        uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
-        const int q0 = (i_lo + it) * kBN;
-        mbar_arrive_expect_tx(q_full + s, 2 * C::kTileBytes + C::kVecBytes);
-        for (int c = 0; c < C::kBoxes; ++c) {
-          tma_load_4d(&p.tm_q, q_full + s, st + c * kBoxBytes, c * 64, q0, hi, bi);
-          tma_load_4d(&p.tm_do, q_full + s, st + C::kTileBytes + c * kBoxBytes, c * 64, q0, hi, bi);
-        }
-        const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
-        tma_load_1d(st + 2 * C::kTileBytes, p.lse2 + vrow, kBN * 4, q_full + s);
-        tma_load_1d(st + 2 * C::kTileBytes + kBN * 4, p.dvec + vrow, kBN * 4, q_full + s);
-        issued = it + 1;
-      }
-      mbar_wait_drain(kv_full, 0);
-      for (int it = max(0, issued - C::kStages); it < issued; ++it)
-        mbar_wait_drain(q_full + it % C::kStages, static_cast<uint32_t>(it / C::kStages) & 1u);
-    }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0 && n_it > 0) {
-      const uint32_t k_smem = smem_base + C::kKOff;
-      const uint32_t v_smem = smem_base + C::kVOff;
-      const uint32_t ds_smem = smem_base + C::kDsOff;
-      bool ok = mbar_wait(kv_full, 0, ab);
-      tc_fence_after();
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t st = smem_base + C::kStageOff + s * C::kStageBytes;
-        ok = mbar_wait(q_full + s, static_cast<uint32_t>(it / C::kStages) & 1u, ab);
-        if (!ok) break;
-        // dP^T overwrites the previous dQ partial: its epilogue must have read it
-        if (it > 0) {
-          ok = mbar_wait(dq_empty, static_cast<uint32_t>(it - 1) & 1u, ab);
-          if (!ok) break;
-        }
-        tc_fence_after();
-        // S^T = K_j Q_i^T (cols 0..127), dP^T = V_j dO_i^T (cols 128..255)
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = static_cast<uint32_t>((k >> 2) * kBoxBytes + (k & 3) * 32);
-          mma_bf16_ss(tmem, smem_desc_sw128(k_smem + off, 16, 1024),
-                      smem_desc_sw128(st + off, 16, 1024), C::kIdescS, k > 0 ? 1u : 0u);
-          mma_bf16_ss(tmem + 128, smem_desc_sw128(v_smem + off, 16, 1024),
-                      smem_desc_sw128(st + C::kTileBytes + off, 16, 1024), C::kIdescS,
-                      k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full);
-        ok = mbar_wait(p_full, static_cast<uint32_t>(it) & 1u, ab);
-        if (!ok) break;
-        tc_fence_after();
-        // dV += P^T dO_i, dK += dS^T Q_i (K = queries, 16 per step = 8 packed columns)
-#pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
-          mma_bf16_ts(tmem + 256, tmem + static_cast<uint32_t>(k * 8),
-                      smem_desc_sw128(st + C::kTileBytes + roff, kBoxBytes, 1024), C::kIdescKV,
-                      (it > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + 256 + D, tmem + 128 + static_cast<uint32_t>(k * 8),
-                      smem_desc_sw128(st + roff, kBoxBytes, 1024), C::kIdescKV,
-                      (it > 0 || k > 0) ? 1u : 0u);
-        }
-        // dQ_i = dS K_j (K = keys, 16 per step)
-#pragma unroll
-        for (int k = 0; k < kBM / 16; ++k) {
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
-          mma_bf16_ss(tmem + 128, smem_desc_sw128(ds_smem + roff, kBoxBytes, 1024),
-                      smem_desc_sw128(k_smem + roff, kBoxBytes, 1024), C::kIdescQ,
-                      k > 0 ? 1u : 0u);
-        }
-        mma_commit(dq_full);
-        mma_commit(q_empty + s);
-      }
-      if (ok) mma_commit(acc_full);
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0);
-    }
-  } else if (warp < 4) {
-    // ------------------------------------------------- P^T, dS^T (key rows)
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const int key = key0 + r;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % C::kStages;
-      const uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
-      const float* lse2 = reinterpret_cast<const float*>(st + 2 * C::kTileBytes);
-      const float* dvec = lse2 + kBN;
-      const int q0 = (i_lo + it) * kBN;
-      // the stage's vectors arrive with its Q/dO tiles on q_full
-      ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / C::kStages) & 1u, ab) &&
-           mbar_wait_warp(s_full, static_cast<uint32_t>(it) & 1u, ab);
-      if (!ok) break;
-      tc_fence_after();
-      // every (query, key) pair of the tile visible: no per-element mask
-      const int key_last = key0 + kBM - 1;
-      const bool full = key_last < kv_len && (!causal || key_last <= q0) &&
-                        key0 >= q0 + kBN - 1 - p.win_left && key_last <= q0 + p.win_right;
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(lane_base + c * 32, sv);
-        tmem_ld32(lane_base + 128 + c * 32, dp);
-        tmem_ld_wait();
-        reg_fence(sv);
-        reg_fence(dp);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qi = c * 32 + e + u;
-            const int query = q0 + qi;
-            const bool visible = full || (key < kv_len && (!causal || key <= query) &&
-                                          key >= query - p.win_left && key <= query + p.win_right);
-            const float pp = visible
-                ? ex2_approx(fmaf(__uint_as_float(sv[e + u]), p.scale_log2, -lse2[qi]))
-                : 0.f;
-            pv[u] = pp;
-            dsv[u] = pp * (__uint_as_float(dp[e + u]) - dvec[qi]);
-          }
-          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          dk[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-        }
-        // over columns already read: P^T at [16c, 16c+16), dS^T at [128+16c, ...)
-        tmem_st16(lane_base + c * 16, pk);
-        tmem_st16(lane_base + 128 + c * 16, dk);
-        // dS^T row r, queries [32c, 32c+32) into the 128-byte-swizzled smem tile
-        uint8_t* box = smem + C::kDsOff + (c >> 1) * kBoxBytes;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint4 v = make_uint4(dk[q4 * 4 + 0], dk[q4 * 4 + 1], dk[q4 * 4 + 2], dk[q4 * 4 + 3]);
-          const uint32_t chunk = static_cast<uint32_t>((c & 1) * 4 + q4);
-          *reinterpret_cast<uint4*>(box + sw128_offset(static_cast<uint32_t>(r), chunk)) = v;
-        }
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // ---- dK (scaled) and dV rows of this key tile to global memory (the
-    // tensor-memory loads are warp-collective: only the stores are per row)
-    if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
-      bool have = ok && n_it > 0;
-      if (have) {
-        have = mbar_wait_warp(acc_full, 0, ab);
-        tc_fence_after();
-      }
-      if (have || n_it == 0) {
-        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D;
-        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t a[32], g[32];
-          if (have) {
-            tmem_ld32(lane_base + 256 + c * 32, a);
-            tmem_ld32(lane_base + 256 + D + c * 32, g);
-            tmem_ld_wait();
-            reg_fence(a);
-            reg_fence(g);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
-          }
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v, w;
-            v.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]), __uint_as_float(a[q4 * 8 + 1]));
-            v.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]), __uint_as_float(a[q4 * 8 + 3]));
-            v.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]), __uint_as_float(a[q4 * 8 + 5]));
-            v.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]), __uint_as_float(a[q4 * 8 + 7]));
-            w.x = pack_bf16x2(__uint_as_float(g[q4 * 8 + 0]) * p.scale, __uint_as_float(g[q4 * 8 + 1]) * p.scale);
-            w.y = pack_bf16x2(__uint_as_float(g[q4 * 8 + 2]) * p.scale, __uint_as_float(g[q4 * 8 + 3]) * p.scale);
-            w.z = pack_bf16x2(__uint_as_float(g[q4 * 8 + 4]) * p.scale, __uint_as_float(g[q4 * 8 + 5]) * p.scale);
-            w.w = pack_bf16x2(__uint_as_float(g[q4 * 8 + 6]) * p.scale, __uint_as_float(g[q4 * 8 + 7]) * p.scale);
-            if (key < p.n_k) {
-              *reinterpret_cast<uint4*>(dv_row + c * 32 + q4 * 8) = v;
-              *reinterpret_cast<uint4*>(dk_row + c * 32 + q4 * 8) = w;
-            }
-          }
-        }
-      }
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------- dQ partials (query rows)
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    for (int it = 0; it < n_it; ++it) {
-      if (!mbar_wait_warp(dq_full, static_cast<uint32_t>(it) & 1u, ab)) break;
-      tc_fence_after();
-      uint32_t a[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t t32[32];
-        tmem_ld32(lane_base + 128 + c * 32, t32);
-        tmem_ld_wait();
-        reg_fence(t32);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) a[c * 32 + e] = t32[e];
-      }
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      const int query = (i_lo + it) * kBN + r;
-      if (query < p.n_q) {
-        float* row = p.dq_acc + (static_cast<long long>(bh) * p.n_q + query) * D;
-#pragma unroll
-        for (int c4 = 0; c4 < D / 4; ++c4)
-          red_add_v4(row + c4 * 4, __uint_as_float(a[c4 * 4 + 0]), __uint_as_float(a[c4 * 4 + 1]),
-                     __uint_as_float(a[c4 * 4 + 2]), __uint_as_float(a[c4 * 4 + 3]));
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
 // ------------------------------------------------------------------------
-// Head size 128: 64-query steps with S^T / dP^T double-buffered in tensor
-// memory, so the tensor core computes the next step's products while the
-// compute warps turn the current ones into P^T and dS^T.
+// 64-query steps with S^T / dP^T double-buffered in tensor memory, so the
+// tensor core computes the next step's products while the compute warps turn
+// the current ones into P^T and dS^T.
 //   warps 0-7  compute: warp w serves key lanes 32 (w % 4) .. +32 and query
 //              half w / 4 (32 queries) of each step; it also moves its share
 //              of the previous step's dQ^T into the shared staging tile.
@@ -412,11 +54,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc(const __grid_constant
 // Tensor memory: buffer b = step & 1 holds S^T at 128 b (64 columns; P^T in
 // bf16 over columns 128 b + 32 h .. +16 of each half h) and dP^T at
 // 128 b + 64 (dS^T in bf16 the same way; then dQ^T = K^T dS^T, keyed by d),
-// dV at 256, dK at 384.  dQ^T leaves through a 32 KB fp32 staging tile and
-// one bulk reduce-add into the fp32 dQ accumulator per step.
+// dV at 256, dK at 256 + D.  dQ^T leaves through a 64 x D fp32 staging tile
+// and one bulk reduce-add into the fp32 dQ accumulator per step.
 namespace n64 {
 
-constexpr int D = 128;
 constexpr int kBM = 128;                 // keys per CTA
 constexpr int kBN = 64;                  // queries per step
 constexpr int kStages = 3;
@@ -426,27 +67,33 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kKVBox = 128 * 128;        // 64 columns x 128 rows bf16
 constexpr int kQBox = 64 * 128;          // 64 columns x 64 rows bf16
-constexpr int kKVTile = 2 * kKVBox;
-constexpr int kQTile = 2 * kQBox;
 constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (128-byte rows)
 constexpr int kVecBytes = 2 * kBN * 4;   // lse2 and D of one step
-constexpr int kKOff = 0;
-constexpr int kVOff = kKVTile;
-constexpr int kStageOff = 2 * kKVTile;                    // Q, dO per stage
-constexpr int kDsOff = kStageOff + kStages * 2 * kQTile;  // two dS^T buffers
-constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // dQ rows: 64 x 128 fp32
-constexpr int kVecOff = kStagingOff + kBN * D * 4;
-constexpr int kBarOff = kVecOff + kStages * kVecBytes;
 // kv_full, q_full[3], q_empty[3], s_full[2], p_full[2], dq_full[2],
 // dq_empty[2], staging_full, staging_free, acc_full, drain
 constexpr int kNumBars = 1 + 2 * kStages + 8 + 4;
-constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory");
-static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
-
 constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
-constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);     // dV, dK (A in TMEM)
-constexpr uint32_t kIdescQ = idesc_bf16(D, kBN, true, true);       // dQ^T = K^T dS^T
+// dQ^T = K^T dS^T always with M = 128 lanes of d: for D = 64 the upper 64
+// lanes read the V tile that follows K in shared memory and are discarded.
+constexpr uint32_t kIdescQ = idesc_bf16(128, kBN, true, true);
+
+template <int D>
+struct Cfg {
+  static constexpr int kKVTile = (D / 64) * kKVBox;
+  static constexpr int kQTile = (D / 64) * kQBox;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKVTile;
+  static constexpr int kStageOff = 2 * kKVTile;                    // Q, dO per stage
+  static constexpr int kDsOff = kStageOff + kStages * 2 * kQTile;  // two dS^T buffers
+  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // dQ rows: 64 x D fp32
+  static constexpr int kVecOff = kStagingOff + kBN * D * 4;
+  static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);   // dV, dK (A in TMEM)
+  static constexpr uint32_t kDkCol = 256 + D;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
+};
 
 __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
@@ -471,12 +118,14 @@ __device__ __forceinline__ int2 query_steps(const SdpaBwdParams& p, int key0, in
   return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_constant__ SdpaBwdParams p) {
+  using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   const uint32_t smem_base = smem_u32(smem);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* kv_full = bar;
   uint64_t* q_full = bar + 1;
   uint64_t* q_empty = q_full + kStages;
@@ -540,25 +189,25 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * kKVTile);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_4d(&p.tm_k, kv_full, smem + kKOff + c * kKVBox, c * 64, key0, hi, bi);
-        tma_load_4d(&p.tm_v, kv_full, smem + kVOff + c * kKVBox, c * 64, key0, hi, bi);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kKVTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * kKVBox, c * 64, key0, hi, bi);
+        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * kKVBox, c * 64, key0, hi, bi);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t use = static_cast<uint32_t>(it / kStages);
         if (it >= kStages && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
-        uint8_t* st = smem + kStageOff + s * 2 * kQTile;
+        uint8_t* st = smem + C::kStageOff + s * 2 * C::kQTile;
         const int q0 = (i_lo + it) * kBN;
-        mbar_arrive_expect_tx(q_full + s, 2 * kQTile + kVecBytes);
-        for (int c = 0; c < 2; ++c) {
+        mbar_arrive_expect_tx(q_full + s, 2 * C::kQTile + kVecBytes);
+        for (int c = 0; c < D / 64; ++c) {
           tma_load_4d(&p.tm_q, q_full + s, st + c * kQBox, c * 64, q0, hi, bi);
-          tma_load_4d(&p.tm_do, q_full + s, st + kQTile + c * kQBox, c * 64, q0, hi, bi);
+          tma_load_4d(&p.tm_do, q_full + s, st + C::kQTile + c * kQBox, c * 64, q0, hi, bi);
         }
         const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
-        uint8_t* vec = smem + kVecOff + s * kVecBytes;
+        uint8_t* vec = smem + C::kVecOff + s * kVecBytes;
         tma_load_1d(vec, p.lse2 + vrow, kBN * 4, q_full + s);
         tma_load_1d(vec + kBN * 4, p.dvec + vrow, kBN * 4, q_full + s);
         issued = it + 1;
@@ -569,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && n_it > 0) {
-      const uint32_t k_smem = smem_base + kKOff;
-      const uint32_t v_smem = smem_base + kVOff;
+      const uint32_t k_smem = smem_base + C::kKOff;
+      const uint32_t v_smem = smem_base + C::kVOff;
       // S^T(it) = K_j Q_i^T and dP^T(it) = V_j dO_i^T into buffer it & 1
       auto issue_s = [&](int it, bool dp) {
-        const uint32_t st = smem_base + kStageOff + (it % kStages) * 2 * kQTile + (dp ? kQTile : 0);
+        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * 2 * C::kQTile + (dp ? C::kQTile : 0);
         const uint32_t a_base = dp ? v_smem : k_smem;
         const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
 #pragma unroll
@@ -611,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         ok = mbar_wait(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t st = smem_base + kStageOff + (it % kStages) * 2 * kQTile;
+        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * 2 * C::kQTile;
         const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
         // dV += P^T dO_i, dK += dS^T Q_i: 16 queries per step; queries
         // [32h, 32h+32) sit in columns 32h .. 32h+16 of the S^T / dP^T halves
@@ -619,14 +268,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         for (int k = 0; k < kBN / 16; ++k) {
           const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
           const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
-          mma_bf16_ts(tmem + 256, buf + col, smem_desc_sw128(st + kQTile + roff, kQBox, 1024),
-                      kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + 384, buf + 64 + col, smem_desc_sw128(st + roff, kQBox, 1024),
-                      kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + 256, buf + col, smem_desc_sw128(st + C::kQTile + roff, kQBox, 1024),
+                      C::kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kDkCol, buf + 64 + col, smem_desc_sw128(st + roff, kQBox, 1024),
+                      C::kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(q_empty + it % kStages);
         // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
-        const uint32_t ds = smem_base + kDsOff + b * kDsTile;
+        const uint32_t ds = smem_base + C::kDsOff + b * kDsTile;
 #pragma unroll
         for (int k = 0; k < kBM / 16; ++k) {
           const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
@@ -646,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     const int r = quarter * 32 + lane;                // key lane, and d lane of dQ^T
     const int key = key0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* staging = reinterpret_cast<float*>(smem + kStagingOff);
+    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff);
     bool ok = true;
 
     // dQ^T(j) columns of this warp -> staging rows 32 half .. +32, column r;
@@ -668,8 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         }
         if (!mbar_wait_warp(staging_free, static_cast<uint32_t>(j - 1) & 1u, ab)) return false;
       }
+      if (D == 128 || r < D) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) staging[(half * 32 + e) * D + r] = __uint_as_float(g[e]);
+        for (int e = 0; e < 32; ++e) staging[(half * 32 + e) * D + r] = __uint_as_float(g[e]);
+      }
       fence_proxy_async_smem();
       mbar_arrive(staging_full);
       bool good = true;
@@ -695,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       const int qh0 = (i_lo + it) * kBN + half * 32;
-      const float* lse2 = reinterpret_cast<const float*>(smem + kVecOff + s * kVecBytes) + half * 32;
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::kVecOff + s * kVecBytes) + half * 32;
       const float* dvec = lse2 + kBN;
       // this key sees every query of its half: no per-element mask
       const bool full = key < kv_len && (!causal || key <= qh0) && key >= qh0 + 31 - p.win_left &&
@@ -734,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       tmem_st16(lane_base + s_col, pk);
       tmem_st16(lane_base + s_col + 64, dk);
       // dS^T row r, queries [32 half, +32): 16-byte chunks 4 half .. +4 of the 128-byte row
-      uint8_t* dsb = smem + kDsOff + b * kDsTile;
+      uint8_t* dsb = smem + C::kDsOff + b * kDsTile;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint4 v = make_uint4(dk[c * 4 + 0], dk[c * 4 + 1], dk[c * 4 + 2], dk[c * 4 + 3]);
@@ -751,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       }
     }
     if (ok && n_it > 0) ok = epilogue(n_it - 1);
-    // ---- dK (scaled) and dV rows: warp half h takes columns [64h, 64h+64)
+    // ---- dK (scaled) and dV rows: warp half h takes columns [h D/2, (h+1) D/2)
     if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
       bool have = ok && n_it > 0;
       if (have) {
@@ -759,14 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tc_fence_after();
       }
       if (have || n_it == 0) {
-        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D + half * 64;
-        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D + half * 64;
+        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D + half * (D / 2);
+        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D + half * (D / 2);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t a[32], g[32];
           if (have) {
-            tmem_ld32(lane_base + 256 + half * 64 + c * 32, a);
-            tmem_ld32(lane_base + 384 + half * 64 + c * 32, g);
+            tmem_ld32(lane_base + 256 + half * (D / 2) + c * 32, a);
+            tmem_ld32(lane_base + C::kDkCol + half * (D / 2) + c * 32, g);
             tmem_ld_wait();
             reg_fence(a);
             reg_fence(g);
@@ -851,7 +502,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const SdpaBwdPrepPara
 }
 
 template <int D>
-cudaError_t launch_d(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
+cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
   const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
   cudaError_t err = cudaSuccess;
   if (rows > 0) {
@@ -859,12 +510,13 @@ cudaError_t launch_d(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaS
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  const int smem = BwdCfg<D>::kSmemBytes;
-  err = cudaFuncSetAttribute(sdpa_bwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = n64::Cfg<D>::kSmemBytes;
+  err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
   if (blocks > 0) {
-    sdpa_bwd_tc<D><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(bp);
+    n64::sdpa_bwd_tc_n64<D><<<static_cast<unsigned>(blocks), n64::kThreads, smem, stream>>>(bp);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -873,36 +525,12 @@ cudaError_t launch_d(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaS
   return cudaGetLastError();
 }
 
-cudaError_t launch_d128(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp,
-                        cudaStream_t stream) {
-  const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
-  cudaError_t err = cudaSuccess;
-  if (rows > 0) {
-    sdpa_bwd_prep<128><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(pp);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-  }
-  err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             n64::kSmemBytes);
-  if (err != cudaSuccess) return err;
-  const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
-  if (blocks > 0) {
-    n64::sdpa_bwd_tc_n64<<<static_cast<unsigned>(blocks), n64::kThreads, n64::kSmemBytes, stream>>>(
-        bp);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-  }
-  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * 128;
-  if (n > 0) sdpa_bwd_dq_convert<128><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(pp);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
                             cudaStream_t stream) {
-  if (head_dim == 64) return launch_d<64>(bp, pp, stream);
-  if (head_dim == 128) return launch_d128(bp, pp, stream);
+  if (head_dim == 64) return launch_n64<64>(bp, pp, stream);
+  if (head_dim == 128) return launch_n64<128>(bp, pp, stream);
   return cudaErrorInvalidValue;
 }
 
