@@ -46,11 +46,12 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 // 64-query steps with S^T / dP^T double-buffered in tensor memory, so the
 // tensor core computes the next step's products while the compute warps turn
 // the current ones into P^T and dS^T.
-//   warps 0-7  compute: warp w serves key lanes 32 (w % 4) .. +32 and query
-//              half w / 4 (32 queries) of each step; it also moves its share
-//              of the previous step's dQ^T into the shared staging tile.
-//   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i, lse2, D in 3 stages).
-//   warp 9     MMA issuer, in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T(i).
+//   warps 0-7    compute: warp w serves key lanes 32 (w % 4) .. +32 and
+//                query half w / 4 (32 queries) of each step; at the end they
+//                write dK and dV.
+//   warp 8       TMA producer (K_j, V_j once; Q_i, dO_i, lse2, D in 3 stages).
+//   warp 9       MMA issuer, in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T(i).
+//   warps 10-13  dQ^T of each step out of tensor memory into the staging tile.
 // Tensor memory: buffer b = step & 1 holds S^T at 128 b (64 columns; P^T in
 // bf16 over columns 128 b + 32 h .. +16 of each half h) and dP^T at
 // 128 b + 64 (dS^T in bf16 the same way; then dQ^T = K^T dS^T, keyed by d),
@@ -61,10 +62,13 @@ namespace n64 {
 constexpr int kBM = 128;                 // keys per CTA
 constexpr int kBN = 64;                  // queries per step
 constexpr int kStages = 3;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kCompute = 256;            // warps 0-7
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kEpilogueWarp0 = 10;       // warps 10-13: dQ^T out of tensor memory
+constexpr int kEpilogue = 128;
+constexpr int kHeadGroup = 4;            // heads whose key tiles run together
 constexpr int kKVBox = 128 * 128;        // 64 columns x 128 rows bf16
 constexpr int kQBox = 64 * 128;          // 64 columns x 64 rows bf16
 constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (128-byte rows)
@@ -144,8 +148,21 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh_count = p.b * p.h;
-  const int jt = static_cast<int>(blockIdx.x) / bh_count;
-  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  // Heads in groups of kHeadGroup, each group's key tiles in ascending order
+  // (the longest causal walks first): the dQ accumulator and the Q / dO rows
+  // of the heads in flight stay in L2.
+  const int group_ctas = kHeadGroup * p.num_kv_tiles;
+  const int full_groups = bh_count / kHeadGroup;
+  int g = static_cast<int>(blockIdx.x) / group_ctas;
+  int rr = static_cast<int>(blockIdx.x) % group_ctas;
+  int heads_in_group = kHeadGroup;
+  if (g >= full_groups) {
+    g = full_groups;
+    rr = static_cast<int>(blockIdx.x) - full_groups * group_ctas;
+    heads_in_group = bh_count - full_groups * kHeadGroup;
+  }
+  const int jt = rr / heads_in_group;
+  const int bh = g * kHeadGroup + rr % heads_in_group;
   const int bi = bh / p.h;
   const int hi = bh % p.h;
   const bool causal = (p.mask_kind & 1) != 0;
@@ -168,9 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, kCompute);
       mbar_init(dq_full + b, 1);
-      mbar_init(dq_empty + b, kCompute);
+      mbar_init(dq_empty + b, kEpilogue);
     }
-    mbar_init(staging_full, kCompute);
+    mbar_init(staging_full, kEpilogue);
     mbar_init(staging_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
@@ -288,43 +305,46 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
-  } else {
-    // ------------------------------------------------------- compute warps
+  } else if (warp >= kEpilogueWarp0) {
+    // ------------------------------------------ dQ^T out of tensor memory
+    // warp 10 + k serves d lanes 32 (warp % 4) .. +32 of every step: the 64
+    // query columns go to staging rows 0..63, column d; then one thread adds
+    // the tile into the fp32 accumulator with a bulk reduce.
     const int quarter = warp & 3;
-    const int half = warp >> 2;
-    const int r = quarter * 32 + lane;                // key lane, and d lane of dQ^T
-    const int key = key0 + r;
+    const int d = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* staging = reinterpret_cast<float*>(smem + C::kStagingOff);
-    bool ok = true;
-
-    // dQ^T(j) columns of this warp -> staging rows 32 half .. +32, column r;
-    // then one thread adds the tile into the fp32 accumulator.
-    auto epilogue = [&](int j) -> bool {
+    const bool leader = threadIdx.x == kEpilogueWarp0 * 32;
+    for (int j = 0; j < n_it; ++j) {
       const int b = j & 1;
-      if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) return false;
+      if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
       tc_fence_after();
-      uint32_t g[32];
-      tmem_ld32(lane_base + static_cast<uint32_t>(b * 128 + 64 + half * 32), g);
+      uint32_t g0[32], g1[32];
+      tmem_ld32(lane_base + static_cast<uint32_t>(b * 128 + 64), g0);
+      tmem_ld32(lane_base + static_cast<uint32_t>(b * 128 + 96), g1);
       tmem_ld_wait();
-      reg_fence(g);
+      reg_fence(g0);
+      reg_fence(g1);
       tc_fence_before();
       mbar_arrive(dq_empty + b);
       if (j >= 1) {
-        if (threadIdx.x == 0) {
+        if (leader) {
           asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
           mbar_arrive(staging_free);
         }
-        if (!mbar_wait_warp(staging_free, static_cast<uint32_t>(j - 1) & 1u, ab)) return false;
+        if (!mbar_wait_warp(staging_free, static_cast<uint32_t>(j - 1) & 1u, ab)) break;
       }
-      if (D == 128 || r < D) {
+      if (D == 128 || d < D) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) staging[(half * 32 + e) * D + r] = __uint_as_float(g[e]);
+        for (int e = 0; e < 32; ++e) {
+          staging[e * D + d] = __uint_as_float(g0[e]);
+          staging[(32 + e) * D + d] = __uint_as_float(g1[e]);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(staging_full);
       bool good = true;
-      if (threadIdx.x == 0) {
+      if (leader) {
         good = mbar_wait(staging_full, static_cast<uint32_t>(j) & 1u, ab);
         const int q0 = (i_lo + j) * kBN;
         const int rows = min(kBN, p.n_q - q0);
@@ -333,10 +353,19 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
                               static_cast<uint32_t>(rows) * D * 4);
         tma_store_commit();
       }
-      // lane 0 of warp 0 decided alone: make the answer warp-uniform there
-      if (warp == 0) good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
-      return good;
-    };
+      // the leader decided alone: make the answer uniform across its warp
+      if (warp == kEpilogueWarp0) good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      if (!good) break;
+    }
+    if (leader) bulk_wait_all();   // the last reduce has finished
+  } else {
+    // ------------------------------------------------------- compute warps
+    const int quarter = warp & 3;
+    const int half = warp >> 2;
+    const int r = quarter * 32 + lane;                // key lane
+    const int key = key0 + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    bool ok = true;
 
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1;
@@ -396,12 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(p_full + b);
-      if (it >= 1 && !epilogue(it - 1)) {
-        ok = false;
-        break;
-      }
     }
-    if (ok && n_it > 0) ok = epilogue(n_it - 1);
     // ---- dK (scaled) and dV rows: warp half h takes columns [h D/2, (h+1) D/2)
     if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
       bool have = ok && n_it > 0;
@@ -448,7 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         }
       }
     }
-    if (threadIdx.x == 0) bulk_wait_all();   // the last reduce has finished
   }
 
   tc_fence_before();
