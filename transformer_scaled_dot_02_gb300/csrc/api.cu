@@ -103,6 +103,23 @@ bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 map over the backward's dQ accumulator [bh][n_q][d]: boxes of 32
+// columns x 64 rows, unswizzled (one 128-byte row per query), for the
+// kernel's tensor reduce-adds; rows past n_q are clipped by the copy engine.
+bool make_map_dq(CUtensorMap* map, const float* base, int d, int n_q, int bh) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_q > 0 ? n_q : 1),
+                              static_cast<cuuint64_t>(bh)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(n_q > 0 ? n_q : 1) * d * 4};
+  const cuuint32_t box[3] = {32, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D bf16 map over a row-major [rows, cols] matrix: box (64 cols, box_rows).
 bool make_map_2d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
   auto enc = encode_fn();
@@ -282,8 +299,8 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   const int n_q_pad = (n_q + 127) / 128 * 128;
   const size_t rows_pad = static_cast<size_t>(b) * h * n_q_pad;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* lse2 = reinterpret_cast<float*>(ws);
-  float* dvec = reinterpret_cast<float*>(ws + round256(rows_pad * 4));
+  float* neg_lse2 = reinterpret_cast<float*>(ws);
+  float* neg_dvec = reinterpret_cast<float*>(ws + round256(rows_pad * 4));
   float* dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows_pad * 4));
   sdpa::SdpaBwdParams bp;
   const long long dd = d;
@@ -294,8 +311,9 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
       !make_map_4d(&bp.tm_v, v, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
       !make_map_4d(&bp.tm_do, dout, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd, q_rows))
     return SDPA_ERR_CUDA;
-  bp.lse2 = lse2;
-  bp.dvec = dvec;
+  if (!make_map_dq(&bp.tm_dq, dq_acc, d, n_q, b * h)) return SDPA_ERR_CUDA;
+  bp.neg_lse2 = neg_lse2;
+  bp.neg_dvec = neg_dvec;
   bp.dq_acc = dq_acc;
   bp.dk = static_cast<uint16_t*>(dk);
   bp.dv = static_cast<uint16_t*>(dv);
@@ -317,8 +335,8 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   pp.out = static_cast<const uint16_t*>(out);
   pp.dout = static_cast<const uint16_t*>(dout);
   pp.lse = lse;
-  pp.lse2 = lse2;
-  pp.dvec = dvec;
+  pp.neg_lse2 = neg_lse2;
+  pp.neg_dvec = neg_dvec;
   pp.dq_acc = dq_acc;
   pp.dq = static_cast<uint16_t*>(dq);
   pp.b = b;

@@ -50,9 +50,10 @@ cudaError_t launch_sdpa_decode(const DecodeParams& p, int head_dim, cudaStream_t
 
 // Gradients of attention (bf16 BHSD tensors, fp32 accumulation).
 struct SdpaBwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 4-D (d, n, h, b) maps, 64 x 128 boxes
-  const float* lse2;          // [b*h][n_q_pad] log-sum-exp in log2 units (+inf past n_q)
-  const float* dvec;          // [b*h][n_q_pad] D_i = dO_i . O_i
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 4-D (d, n, h, b) bf16 maps
+  CUtensorMap tm_dq;          // 3-D (d, n_q, b*h) fp32 map of dq_acc, 32 x 64 boxes
+  const float* neg_lse2;      // [b*h][n_q_pad] -lse_i log2(e) (-inf past n_q)
+  const float* neg_dvec;      // [b*h][n_q_pad] -D_i = -dO_i . O_i
   float* dq_acc;              // [b*h][n_q][d] fp32 accumulator (zeroed by the prep kernel)
   uint16_t *dk, *dv;          // [b*h][n_k][d] bf16 outputs
   const int32_t* kv_lengths;
@@ -64,7 +65,7 @@ struct SdpaBwdParams {
 struct SdpaBwdPrepParams {
   const uint16_t *out, *dout;  // forward output and its gradient, [b*h][n_q][d]
   const float* lse;            // [b*h][n_q] natural log-sum-exp
-  float *lse2, *dvec, *dq_acc;
+  float *neg_lse2, *neg_dvec, *dq_acc;
   uint16_t* dq;                // [b*h][n_q][d] bf16 output
   int b, h, n_q, n_q_pad;
   float scale;

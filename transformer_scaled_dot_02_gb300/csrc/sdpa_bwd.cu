@@ -6,10 +6,10 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 // P is recomputed from the forward's per-row log-sum-exp, never stored.
 //
-//   sdpa_bwd_prep        D_i = dO_i . O_i and the log-sum-exp in log2 units
-//                        for every query row (padded to whole 128-row tiles
-//                        with D = 0 and +inf, so padded rows get P = 0);
-//                        zeroes the fp32 dQ accumulator.
+//   sdpa_bwd_prep        -D_i = -dO_i . O_i and the negated log-sum-exp in
+//                        log2 units for every query row (padded to whole
+//                        128-row tiles with 0 and -inf, so padded rows get
+//                        P = 0); zeroes the fp32 dQ accumulator.
 //   sdpa_bwd_tc_n64<D>   one CTA per (128-key tile, batch, head), walking in
 //                        steps of 64 the queries that can see its keys; dK
 //                        and dV accumulate in tensor memory, dQ leaves each
@@ -20,6 +20,7 @@
 // tensor-memory lanes.  The five products per step are
 // S^T = K Q^T, dP^T = V dO^T, dV += P^T dO, dK += dS^T Q and dQ^T = K^T dS^T.
 #include <cmath>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -72,10 +73,10 @@ constexpr int kHeadGroup = 4;            // heads whose key tiles run together
 constexpr int kKVBox = 128 * 128;        // 64 columns x 128 rows bf16
 constexpr int kQBox = 64 * 128;          // 64 columns x 64 rows bf16
 constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (128-byte rows)
-constexpr int kVecBytes = 2 * kBN * 4;   // lse2 and D of one step
+constexpr int kVecBytes = 2 * kBN * 4;   // -lse2 and -D of one step
 // kv_full, q_full[3], q_empty[3], s_full[2], p_full[2], dq_full[2],
-// dq_empty[2], staging_full, staging_free, acc_full, drain
-constexpr int kNumBars = 1 + 2 * kStages + 8 + 4;
+// dq_empty[2], acc_full, drain
+constexpr int kNumBars = 1 + 2 * kStages + 8 + 2;
 constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
 // dQ^T = K^T dS^T always with M = 128 lanes of d: for D = 64 the upper 64
 // lanes read the V tile that follows K in shared memory and are discarded.
@@ -89,8 +90,8 @@ struct Cfg {
   static constexpr int kVOff = kKVTile;
   static constexpr int kStageOff = 2 * kKVTile;                    // Q, dO per stage
   static constexpr int kDsOff = kStageOff + kStages * 2 * kQTile;  // two dS^T buffers
-  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // dQ rows: 64 x D fp32
-  static constexpr int kVecOff = kStagingOff + kBN * D * 4;
+  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // 4 warps x [64][32] fp32
+  static constexpr int kVecOff = kStagingOff + 4 * kBN * 32 * 4;
   static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);   // dV, dK (A in TMEM)
@@ -99,11 +100,21 @@ struct Cfg {
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
 };
 
-__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   dst),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
+// Adds a [64][32] fp32 box from shared memory into the tensor at (x, y, z).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
+                                                  int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          map),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
 }
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -137,9 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   uint64_t* p_full = s_full + 2;
   uint64_t* dq_full = p_full + 2;
   uint64_t* dq_empty = dq_full + 2;
-  uint64_t* staging_full = dq_empty + 2;
-  uint64_t* staging_free = staging_full + 1;
-  uint64_t* acc_full = staging_free + 1;
+  uint64_t* acc_full = dq_empty + 2;
   uint64_t* drain = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -187,8 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       mbar_init(dq_full + b, 1);
       mbar_init(dq_empty + b, kEpilogue);
     }
-    mbar_init(staging_full, kEpilogue);
-    mbar_init(staging_free, 1);
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -225,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         }
         const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
         uint8_t* vec = smem + C::kVecOff + s * kVecBytes;
-        tma_load_1d(vec, p.lse2 + vrow, kBN * 4, q_full + s);
-        tma_load_1d(vec + kBN * 4, p.dvec + vrow, kBN * 4, q_full + s);
+        tma_load_1d(vec, p.neg_lse2 + vrow, kBN * 4, q_full + s);
+        tma_load_1d(vec + kBN * 4, p.neg_dvec + vrow, kBN * 4, q_full + s);
         issued = it + 1;
       }
       mbar_wait_drain(kv_full, 0);
@@ -237,17 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     if (lane == 0 && n_it > 0) {
       const uint32_t k_smem = smem_base + C::kKOff;
       const uint32_t v_smem = smem_base + C::kVOff;
+      // Shared-memory descriptors as 32-bit halves: every operand here is
+      // 128-byte swizzled with 8-row groups 1024 bytes apart, so the high
+      // half is one constant and a k step only adds to the start address.
+      constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       // S^T(it) = K_j Q_i^T and dP^T(it) = V_j dO_i^T into buffer it & 1
       auto issue_s = [&](int it, bool dp) {
         const uint32_t st = smem_base + C::kStageOff + (it % kStages) * 2 * C::kQTile + (dp ? C::kQTile : 0);
-        const uint32_t a_base = dp ? v_smem : k_smem;
+        const uint32_t a0 = lo(dp ? v_smem : k_smem, 16);
+        const uint32_t b0 = lo(st, 16);
         const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          mma_bf16_ss(d,
-                      smem_desc_sw128(a_base + (k >> 2) * kKVBox + (k & 3) * 32, 16, 1024),
-                      smem_desc_sw128(st + (k >> 2) * kQBox + (k & 3) * 32, 16, 1024), kIdescS,
-                      k > 0 ? 1u : 0u);
+          mma_bf16_ss_lohi(d, a0 + static_cast<uint32_t>(((k >> 2) * kKVBox + (k & 3) * 32) >> 4),
+                           kDescHi,
+                           b0 + static_cast<uint32_t>(((k >> 2) * kQBox + (k & 3) * 32) >> 4),
+                           kDescHi, kIdescS, k > 0 ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(kv_full, 0, ab) && mbar_wait(q_full, 0, ab);
@@ -281,23 +294,24 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
         // dV += P^T dO_i, dK += dS^T Q_i: 16 queries per step; queries
         // [32h, 32h+32) sit in columns 32h .. 32h+16 of the S^T / dP^T halves
+        const uint32_t bdo = lo(st + C::kQTile, kQBox), bq = lo(st, kQBox);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
-          mma_bf16_ts(tmem + 256, buf + col, smem_desc_sw128(st + C::kQTile + roff, kQBox, 1024),
-                      C::kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ts(tmem + C::kDkCol, buf + 64 + col, smem_desc_sw128(st + roff, kQBox, 1024),
-                      C::kIdescKV, (it > 0 || k > 0) ? 1u : 0u);
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128) >> 4;
+          mma_bf16_ts_lohi(tmem + 256, buf + col, bdo + roff, kDescHi, C::kIdescKV,
+                           (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts_lohi(tmem + C::kDkCol, buf + 64 + col, bq + roff, kDescHi, C::kIdescKV,
+                           (it > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(q_empty + it % kStages);
         // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
-        const uint32_t ds = smem_base + C::kDsOff + b * kDsTile;
+        const uint32_t ak = lo(k_smem, kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
 #pragma unroll
         for (int k = 0; k < kBM / 16; ++k) {
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128);
-          mma_bf16_ss(buf + 64, smem_desc_sw128(k_smem + roff, kKVBox, 1024),
-                      smem_desc_sw128(ds + roff, kDsTile, 1024), kIdescQ, k > 0 ? 1u : 0u);
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128) >> 4;
+          mma_bf16_ss_lohi(buf + 64, ak + roff, kDescHi, bds + roff, kDescHi, kIdescQ,
+                           k > 0 ? 1u : 0u);
         }
         mma_commit(dq_full + b);
       }
@@ -307,14 +321,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     }
   } else if (warp >= kEpilogueWarp0) {
     // ------------------------------------------ dQ^T out of tensor memory
-    // warp 10 + k serves d lanes 32 (warp % 4) .. +32 of every step: the 64
-    // query columns go to staging rows 0..63, column d; then one thread adds
-    // the tile into the fp32 accumulator with a bulk reduce.
+    // Warp 10 + k serves the d lanes 32 q .. +32 (q = warp % 4) of every
+    // step.  It writes its [64 queries][32 d] block into its own staging
+    // tile and adds that block into the fp32 accumulator with one tensor
+    // reduce; rows past n_q are clipped by the copy engine.
     const int quarter = warp & 3;
-    const int d = quarter * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff);
-    const bool leader = threadIdx.x == kEpilogueWarp0 * 32;
+    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff) + quarter * (kBN * 32);
+    const bool active = D == 128 || quarter * 32 < D;   // d = 64: lanes 64..127 are not d
     for (int j = 0; j < n_it; ++j) {
       const int b = j & 1;
       if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
@@ -327,37 +341,23 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       reg_fence(g1);
       tc_fence_before();
       mbar_arrive(dq_empty + b);
-      if (j >= 1) {
-        if (leader) {
-          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          mbar_arrive(staging_free);
-        }
-        if (!mbar_wait_warp(staging_free, static_cast<uint32_t>(j - 1) & 1u, ab)) break;
-      }
-      if (D == 128 || d < D) {
+      if (!active) continue;
+      // this warp's previous reduce has finished reading the staging tile
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          staging[e * D + d] = __uint_as_float(g0[e]);
-          staging[(32 + e) * D + d] = __uint_as_float(g1[e]);
-        }
+      for (int e = 0; e < 32; ++e) {
+        staging[e * 32 + lane] = __uint_as_float(g0[e]);
+        staging[(32 + e) * 32 + lane] = __uint_as_float(g1[e]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(staging_full);
-      bool good = true;
-      if (leader) {
-        good = mbar_wait(staging_full, static_cast<uint32_t>(j) & 1u, ab);
-        const int q0 = (i_lo + j) * kBN;
-        const int rows = min(kBN, p.n_q - q0);
-        if (good && rows > 0)
-          bulk_reduce_add_f32(p.dq_acc + (static_cast<long long>(bh) * p.n_q + q0) * D, staging,
-                              static_cast<uint32_t>(rows) * D * 4);
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(&p.tm_dq, staging, quarter * 32, (i_lo + j) * kBN, bh);
         tma_store_commit();
       }
-      // the leader decided alone: make the answer uniform across its warp
-      if (warp == kEpilogueWarp0) good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
-      if (!good) break;
     }
-    if (leader) bulk_wait_all();   // the last reduce has finished
+    if (lane == 0) bulk_wait_all();   // this warp's last reduce has finished
   } else {
     // ------------------------------------------------------- compute warps
     const int quarter = warp & 3;
@@ -375,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       if (!ok) break;
       tc_fence_after();
       const int qh0 = (i_lo + it) * kBN + half * 32;
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::kVecOff + s * kVecBytes) + half * 32;
-      const float* dvec = lse2 + kBN;
+      // -lse2 and -D of this half's 32 queries (broadcast shared loads)
+      const uint32_t vec = smem_base + C::kVecOff + s * kVecBytes + half * 32 * 4;
       // this key sees every query of its half: no per-element mask
       const bool full = key < kv_len && (!causal || key <= qh0) && key >= qh0 + 31 - p.win_left &&
                         key <= qh0 + p.win_right;
@@ -388,29 +388,42 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       reg_fence(sv);
       reg_fence(dp);
       uint32_t pk[16], dk[16];
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      // P^T = exp2(S^T scale log2e - lse2), dS^T = P^T (dP^T - D), two at a time
+      auto rows = [&](auto masked) {
 #pragma unroll
-      for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(lse2 + e4 * 4);
-        const float4 d4 = *reinterpret_cast<const float4*>(dvec + e4 * 4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pv[4], dsv[4];
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 nl = lds_f4(vec + e4 * 16);
+          const float4 nd = lds_f4(vec + kBN * 4 + e4 * 16);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = e4 * 4 + u;
-          const int query = qh0 + e;
-          const bool visible = full || (key < kv_len && (!causal || key <= query) &&
-                                        key >= query - p.win_left && key <= query + p.win_right);
-          const float pp =
-              visible ? ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -lv[u])) : 0.f;
-          pv[u] = pp;
-          dsv[u] = pp * (__uint_as_float(dp[e]) - dv4[u]);
+          for (int u = 0; u < 2; ++u) {
+            const int e = e4 * 4 + u * 2;
+            const float2 nl2 = u ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y);
+            const float2 nd2 = u ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y);
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
+                                        sc2, nl2);
+            float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            if (decltype(masked)::value) {
+              const int q = qh0 + e;
+              if (!(key < kv_len && (!causal || key <= q) && key >= q - p.win_left &&
+                    key <= q + p.win_right))
+                p0 = 0.f;
+              if (!(key < kv_len && (!causal || key <= q + 1) && key >= q + 1 - p.win_left &&
+                    key <= q + 1 + p.win_right))
+                p1 = 0.f;
+            }
+            const float2 t = __fadd2_rn(
+                make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2);
+            const float2 ds = __fmul2_rn(make_float2(p0, p1), t);
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+            dk[e >> 1] = pack_bf16x2(ds.x, ds.y);
+          }
         }
-        pk[e4 * 2] = pack_bf16x2(pv[0], pv[1]);
-        pk[e4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-        dk[e4 * 2] = pack_bf16x2(dsv[0], dsv[1]);
-        dk[e4 * 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-      }
+      };
+      if (__all_sync(0xffffffffu, full))
+        rows(std::false_type{});
+      else
+        rows(std::true_type{});
       tmem_st16(lane_base + s_col, pk);
       tmem_st16(lane_base + s_col + 64, dk);
       // dS^T row r, queries [32 half, +32): 16-byte chunks 4 half .. +4 of the 128-byte row
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 
 }  // namespace n64
 
-// D_i = dO_i . O_i, lse2_i = lse_i * log2(e) (padded rows: 0 and +inf), dQ accumulator = 0.
+// -D_i = -dO_i . O_i and -lse_i log2(e) (padded rows: 0 and -inf), dQ accumulator = 0.
 template <int D>
 __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -495,8 +508,8 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
   const int i = static_cast<int>(row % p.n_q_pad);
   if (i >= p.n_q) {
     if (lane == 0) {
-      p.dvec[row] = 0.f;
-      p.lse2[row] = INFINITY;
+      p.neg_dvec[row] = 0.f;
+      p.neg_lse2[row] = -INFINITY;
     }
     return;
   }
@@ -511,8 +524,8 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) {
-    p.dvec[row] = acc;
-    p.lse2[row] = p.lse[bh * p.n_q + i] * 1.4426950408889634f;
+    p.neg_dvec[row] = -acc;
+    p.neg_lse2[row] = -p.lse[bh * p.n_q + i] * 1.4426950408889634f;
   }
 }
 
