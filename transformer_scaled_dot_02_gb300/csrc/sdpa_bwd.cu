@@ -498,43 +498,60 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 }  // namespace n64
 
 // -D_i = -dO_i . O_i and -lse_i log2(e) (padded rows: 0 and -inf), dQ accumulator = 0.
+// D / 8 lanes per row, 16 bytes of O and dO per lane.
 template <int D>
 __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + warp;   // over b*h*n_q_pad
+  constexpr int kLanes = D / 8;
+  constexpr int kRowsPerBlock = 256 / kLanes;
+  const int sub = threadIdx.x % kLanes;
+  const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanes;
   const long long rows = static_cast<long long>(p.b) * p.h * p.n_q_pad;
-  if (row >= rows) return;
+  if (row >= rows) return;   // whole groups of kLanes lanes leave together
   const long long bh = row / p.n_q_pad;
   const int i = static_cast<int>(row % p.n_q_pad);
+  const unsigned group = ((1u << kLanes) - 1u) << (threadIdx.x & 31 & ~(kLanes - 1));
   if (i >= p.n_q) {
-    if (lane == 0) {
+    if (sub == 0) {
       p.neg_dvec[row] = 0.f;
       p.neg_lse2[row] = -INFINITY;
     }
     return;
   }
-  const long long src = (bh * p.n_q + i) * D;
+  const long long src = (bh * p.n_q + i) * D + sub * 8;
+  const uint4 o = *reinterpret_cast<const uint4*>(p.out + src);
+  const uint4 g = *reinterpret_cast<const uint4*>(p.dout + src);
+  const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
   float acc = 0.f;
-  for (int c = lane; c < D; c += 32) {
-    const float o = __uint_as_float(static_cast<uint32_t>(p.out[src + c]) << 16);
-    const float g = __uint_as_float(static_cast<uint32_t>(p.dout[src + c]) << 16);
-    acc = fmaf(o, g, acc);
-    p.dq_acc[src + c] = 0.f;
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
+  for (int w = 0; w < 4; ++w) {
+    acc = fmaf(__uint_as_float(ow[w] << 16), __uint_as_float(gw[w] << 16), acc);
+    acc = fmaf(__uint_as_float(ow[w] & 0xffff0000u), __uint_as_float(gw[w] & 0xffff0000u), acc);
+  }
+  float4* z = reinterpret_cast<float4*>(p.dq_acc + src);
+  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(group, acc, off);
+  if (sub == 0) {
     p.neg_dvec[row] = -acc;
     p.neg_lse2[row] = -p.lse[bh * p.n_q + i] * 1.4426950408889634f;
   }
 }
 
+// dQ = scale * accumulator in bf16, 8 elements per thread.
 template <int D>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const SdpaBwdPrepParams p) {
-  const long long idx = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  const long long idx = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) * 8;
   const long long n = static_cast<long long>(p.b) * p.h * p.n_q * D;
   if (idx >= n) return;
-  p.dq[idx] = static_cast<uint16_t>(pack_bf16x2(p.dq_acc[idx] * p.scale, 0.f) & 0xffffu);
+  const float4 a = *reinterpret_cast<const float4*>(p.dq_acc + idx);
+  const float4 c = *reinterpret_cast<const float4*>(p.dq_acc + idx + 4);
+  uint4 r;
+  r.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
+  r.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
+  r.z = pack_bf16x2(c.x * p.scale, c.y * p.scale);
+  r.w = pack_bf16x2(c.z * p.scale, c.w * p.scale);
+  *reinterpret_cast<uint4*>(p.dq + idx) = r;
 }
 
 template <int D>
@@ -542,7 +559,9 @@ cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cud
   const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
   cudaError_t err = cudaSuccess;
   if (rows > 0) {
-    sdpa_bwd_prep<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(pp);
+    constexpr long long kRowsPerBlock = 256 / (D / 8);
+    sdpa_bwd_prep<D><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0,
+                       stream>>>(pp);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
@@ -557,7 +576,8 @@ cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cud
     if (err != cudaSuccess) return err;
   }
   const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * D;
-  if (n > 0) sdpa_bwd_dq_convert<D><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(pp);
+  if (n > 0)
+    sdpa_bwd_dq_convert<D><<<static_cast<unsigned>((n / 8 + 255) / 256), 256, 0, stream>>>(pp);
   return cudaGetLastError();
 }
 
