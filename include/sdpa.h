@@ -58,9 +58,11 @@ enum { SDPA_MASK_NONE = 0, SDPA_MASK_CAUSAL = 1, SDPA_MASK_PADDING = 2 };
  *   out [b, h, n_q, d_v]  bf16, device, written (must not overlap the inputs)
  * Scores, softmax statistics and the P.V accumulation are fp32; the
  * softmax weights enter P.V rounded to bf16.  Supported: d_k == d_v in
- * {16, 32, 64, 128} (the head sizes of the paper's Table 3 that fit one
- * 128-byte tile row; else SDPA_ERR_UNSUPPORTED).  b, h >= 1; n_q, n_k >= 0 (zero-sized
- * work returns SDPA_OK with nothing enqueued; n_k == 0 writes zeros).
+ * {16, 32, 64, 128, 256, 512}, the head sizes of the paper's Table 3 (else
+ * SDPA_ERR_UNSUPPORTED).  256 and 512 run on a kernel of their own with one
+ * query tile per CTA; for 512 two CTAs split d_v and both compute the scores.
+ * b, h >= 1; n_q, n_k >= 0 (zero-sized work returns SDPA_OK with nothing
+ * enqueued; n_k == 0 writes zeros).
  */
 sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
                          int b, int h, int n_q, int n_k, int d_k, int d_v,
@@ -179,7 +181,7 @@ size_t mha_workspace_size(int b, int n_q, int n_k, int h, int d_k, int d_v);
  *   aligned, owned by the caller and reusable once the stream passes the call.
  * Projections run on the tensor cores with fp32 accumulation and bf16
  * outputs; the heads are written straight into the Concat layout.
- * Supported: d_k == d_v in {16, 32, 64, 128}; d_model a multiple of 8.
+ * Supported: d_k == d_v in {16, 32, 64, 128, 256, 512}; d_model a multiple of 8.
  */
 sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const void* wk,
                         const void* wv, const void* wo, void* y, void* workspace,

@@ -138,7 +138,9 @@ def test_unsupported_shapes(lib):
     assert _attn(lib, "sdpa_forward", d_k=48, d_v=48) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=8, d_v=8) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=64, d_v=128) == UNSUPPORTED
-    assert _attn(lib, "sdpa_forward", d_k=256, d_v=256) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=384, d_v=384) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=1024, d_v=1024) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=256, d_v=512) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward_f32", d_k=129, d_v=64) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward_f32", b=70000, h=1) == UNSUPPORTED
 

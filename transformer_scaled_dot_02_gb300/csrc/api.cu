@@ -157,7 +157,9 @@ sdpa_status check_attention_args(const void* q, const void* k, const void* v, co
 }
 
 // head sizes the tensor-core attention kernel is built for
-bool tc_head_size(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool tc_head_size(int d) {
+  return d == 16 || d == 32 || d == 64 || d == 128 || d == 256 || d == 512;
+}
 
 float effective_scale(float scale, int d_k) {
   return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
@@ -173,9 +175,12 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
                                 cudaStream_t stream, int win_left = sdpa::kWindowUnbounded,
                                 int win_right = sdpa::kWindowUnbounded, float* lse = nullptr) {
   SdpaTcParams p;
+  // wide heads walk the keys in tiles of 64 (d = 256) or 32 (d = 512)
+  const bool wide = d > 128;
+  const int kv_rows = wide ? sdpa::wide_key_tile(d) : 128;
   if (!make_map_4d(&p.tm_q, q, d, n_q, h, b, q_sn, q_sh, q_sb) ||
-      !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb) ||
-      !make_map_4d(&p.tm_v, v, d, n_k, h, b, kv_sn, kv_sh, kv_sb) ||
+      !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb, kv_rows) ||
+      !make_map_4d(&p.tm_v, v, d, n_k, h, b, kv_sn, kv_sh, kv_sb, kv_rows) ||
       !make_map_4d(&p.tm_o, out, d, n_q, h, b, o_sn, o_sh, o_sb))
     return SDPA_ERR_CUDA;
   p.kv_lengths = (mask_kind & SDPA_MASK_PADDING) ? kv_lengths : nullptr;
@@ -185,12 +190,13 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.n_q = n_q;
   p.n_k = n_k;
   p.mask_kind = mask_kind;
-  p.num_q_blocks = (n_q + 255) / 256;
+  p.num_q_blocks = wide ? (n_q + 127) / 128 : (n_q + 255) / 256;
   p.scale_log2 = effective_scale(scale, d) * 1.4426950408889634f;
   p.win_left = win_left;
   p.win_right = win_right;
   p.lse = lse;
-  return sdpa::launch_sdpa_tc(p, d, stream) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  const cudaError_t err = wide ? sdpa::launch_sdpa_wide(p, d, stream) : sdpa::launch_sdpa_tc(p, d, stream);
+  return err == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 bool fill_gemm_problem(GemmProblem* pr, const void* x, const void* w, void* y, int m, int n,

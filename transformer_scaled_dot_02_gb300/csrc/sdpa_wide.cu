@@ -1,0 +1,427 @@
+// Scaled dot-product attention for wide heads, d_k = d_v in {256, 512}
+// ("Attention Is All You Need", Table 3, rows (A): fewer heads of larger
+// size at a fixed model width), bf16 in/out, fp32 accumulation, on the
+// tensor cores.  Same operation and masks as the 64/128 kernel (Eq. (1) of
+// section 3.2.1, the -infinity mask of section 3.2.3, key padding and the
+// restricted window of section 4).
+//
+// Wide heads do not fit that kernel's plan of two query tiles with a 128 x d
+// fp32 O accumulator each in the 512 tensor-memory columns, so here one CTA
+// owns ONE 128-row query tile and a 256-column slice of O:
+//   d = 256: key tiles of 64; one CTA per query tile.
+//   d = 512: key tiles of 32; two CTAs per query tile, one per half of d_v,
+//            each recomputing the scores (Q, 128 KB, stays in shared memory).
+//   warp 4      TMA producer: Q once, K_j and V_j (this CTA's d_v slice) in
+//               two stages each.
+//   warp 5      MMA issuer: S(j+1) = Q K_{j+1}^T into the free score buffer,
+//               then O += P(j) V_j with P(j) read from tensor memory.
+//   warps 0-3   softmax, one thread per query row (tensor-memory lane): the
+//               running max / sum, P in bf16 over the scores it replaces, the
+//               O rescale when the max moves, and the epilogue.
+// Tensor memory: score buffers S_0 at 0 and S_1 at BN (fp32, BN keys each),
+// O at 2 BN (256 fp32 columns).
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kDvc = 256;                  // O columns per CTA
+constexpr int kHeadGroup = 8;              // (head, d_v slice) units sharing L2
+constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the 64/128 kernel
+
+template <int DK>
+struct WCfg {
+  static constexpr int BN = DK == 256 ? 64 : 32;            // keys per tile
+  static constexpr int kChunks = DK / kDvc;                 // CTAs per query tile
+  static constexpr int kQBox = 128 * 128;                   // 64 columns x 128 rows
+  static constexpr int kKVBox = BN * 128;                   // 64 columns x BN rows
+  static constexpr int kQBytes = (DK / 64) * kQBox;
+  static constexpr int kKBytes = (DK / 64) * kKVBox;
+  static constexpr int kVBytes = (kDvc / 64) * kKVBox;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + 2 * kKBytes;
+  static constexpr int kBarOff = kVOff + 2 * kVBytes;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full, drain
+  static constexpr int kNumBars = 1 + 8 + 4 + 2;
+  static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+  static constexpr uint32_t kOCol = 2 * BN;
+  static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, kDvc, false, true);
+  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kKVBox % 1024 == 0, "alignment");
+  static_assert(kOCol + kDvc <= 512, "tensor memory");
+};
+
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_constant__ SdpaTcParams p) {
+  using C = WCfg<DK>;
+  constexpr int BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  const uint32_t smem_base = smem_u32(smem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* q_full = bar;
+  uint64_t* k_full = bar + 1;
+  uint64_t* k_empty = k_full + 2;
+  uint64_t* v_full = k_empty + 2;
+  uint64_t* v_empty = v_full + 2;
+  uint64_t* s_full = v_empty + 2;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* drain = o_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const AbortState ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work: units = (batch*head, d_v slice) in groups of kHeadGroup; inside
+  // a group the longest query tiles (causal) go first.
+  const int units = p.b * p.h * C::kChunks;
+  const int nqb = p.num_q_blocks;
+  const int group_ctas = kHeadGroup * nqb;
+  const int full_groups = units / kHeadGroup;
+  const int idx = static_cast<int>(blockIdx.x);
+  int g = idx / group_ctas, r = idx % group_ctas, in_group = kHeadGroup;
+  if (g >= full_groups) {
+    g = full_groups;
+    r = idx - full_groups * group_ctas;
+    in_group = units - full_groups * kHeadGroup;
+  }
+  const int qb = nqb - 1 - r / in_group;
+  const int unit = g * kHeadGroup + r % in_group;
+  const int chunk = unit % C::kChunks;
+  const int bh = unit / C::kChunks;
+  const int bi = bh / p.h;
+  const int hi = bh % p.h;
+  const bool causal = (p.mask_kind & 1) != 0;
+  int kv_len = p.n_k;
+  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
+    kv_len = p.kv_lengths[bi];
+    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
+  }
+  // key tiles [j_lo, j_hi) hold a key some row of the tile can see
+  const int qs = qb * kBlockM;
+  int j_lo = 0, j_hi = 0;
+  {
+    const int row_hi = min(qs + kBlockM, p.n_q) - 1;
+    const int key_lo = max(0, qs - p.win_left);
+    int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
+    if (causal) key_hi = min(key_hi, row_hi + 1);
+    if (key_hi > key_lo) {
+      j_lo = key_lo / BN;
+      j_hi = (key_hi + BN - 1) / BN;
+    }
+  }
+  const int n_kv = j_hi - j_lo;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+      mbar_init(s_full + s, 1);
+      mbar_init(p_full + s, kBlockM);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_o);
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
+      for (int c = 0; c < DK / 64; ++c)
+        tma_load_4d(&p.tm_q, q_full, smem + C::kQOff + c * C::kQBox, c * 64, qs, hi, bi);
+      int k_issued = 0, v_issued = 0;
+      for (int u = 0; u < n_kv; ++u) {
+        const int j = j_lo + u;
+        const int s = u & 1;
+        const uint32_t use = static_cast<uint32_t>(u >> 1);
+        if (u >= 2 && !mbar_wait(k_empty + s, (use - 1) & 1u, ab)) break;
+        mbar_arrive_expect_tx(k_full + s, C::kKBytes);
+        for (int c = 0; c < DK / 64; ++c)
+          tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox, c * 64,
+                      j * BN, hi, bi);
+        k_issued = u + 1;
+        if (u >= 2 && !mbar_wait(v_empty + s, (use - 1) & 1u, ab)) break;
+        mbar_arrive_expect_tx(v_full + s, C::kVBytes);
+        for (int c = 0; c < kDvc / 64; ++c)
+          tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
+                      chunk * kDvc + c * 64, j * BN, hi, bi);
+        v_issued = u + 1;
+      }
+      mbar_wait_drain(q_full, 0);
+      for (int u = max(0, k_issued - 2); u < k_issued; ++u)
+        mbar_wait_drain(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
+      for (int u = max(0, v_issued - 2); u < v_issued; ++u)
+        mbar_wait_drain(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
+      const uint32_t q_lo = lo(smem_base + C::kQOff, 16);
+      auto issue_s = [&](int u) {
+        const uint32_t d = tmem + static_cast<uint32_t>((u & 1) * BN);
+        const uint32_t b0 = lo(smem_base + C::kKOff + (u & 1) * C::kKBytes, 16);
+#pragma unroll
+        for (int k = 0; k < DK / 16; ++k) {
+          mma_bf16_ss_lohi(d, q_lo + static_cast<uint32_t>(((k >> 2) * C::kQBox + (k & 3) * 32) >> 4),
+                           kDescHi,
+                           b0 + static_cast<uint32_t>(((k >> 2) * C::kKVBox + (k & 3) * 32) >> 4),
+                           kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int u) {
+        const uint32_t pa = tmem + static_cast<uint32_t>((u & 1) * BN);
+        const uint32_t b0 = lo(smem_base + C::kVOff + (u & 1) * C::kVBytes, C::kKVBox);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {
+          mma_bf16_ts_lohi(tmem + C::kOCol, pa + static_cast<uint32_t>(k * 8),
+                           b0 + static_cast<uint32_t>((k * 16 * 128) >> 4), kDescHi, C::kIdescPV,
+                           (u > 0 || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, ab) && mbar_wait(k_full, 0, ab);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0);
+        mma_commit(s_full);
+        mma_commit(k_empty);
+      }
+      for (int u = 0; ok && u < n_kv; ++u) {
+        if (u + 1 < n_kv) {
+          // S(u+1) into the buffer of P(u-1): PV(u-1) was issued before it
+          const int nx = u + 1;
+          ok = mbar_wait(k_full + (nx & 1), static_cast<uint32_t>(nx >> 1) & 1u, ab);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(nx);
+          mma_commit(s_full + (nx & 1));
+          mma_commit(k_empty + (nx & 1));
+        }
+        ok = mbar_wait(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
+             mbar_wait(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(u);
+        mma_commit(o_full);
+        mma_commit(v_empty + (u & 1));
+      }
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    const int row = qs + row_in_tile;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float scale_log2 = p.scale_log2;
+    const int lo_lim = row - p.win_left;
+    const int hi_lim = min(kv_len - 1, causal ? row : row + min(p.win_right, p.n_k));
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int u = 0; u < n_kv; ++u) {
+      const uint32_t s_col = static_cast<uint32_t>((u & 1) * BN);
+      ok = mbar_wait_warp(s_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
+      if (!ok) break;
+      tc_fence_after();
+      float s[BN];
+      {
+        uint32_t sr[32];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_ld32(lane_base + s_col + c * 32, sr);
+          tmem_ld_wait();
+          reg_fence(sr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[e]);
+        }
+      }
+      const int key0 = (j_lo + u) * BN;
+      const bool tile_masked = (key0 + BN > kv_len) || (causal && key0 + BN - 1 > qs) ||
+                               (key0 + BN - 1 > qs + p.win_right) ||
+                               (key0 < qs + kBlockM - 1 - p.win_left);
+      if (tile_masked) {
+        const int lo_c = lo_lim - key0, hi_c = hi_lim - key0;   // visible columns [lo_c, hi_c]
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c < lo_c || c > hi_c) s[c] = -INFINITY;
+      }
+      float mx4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx4[i] = s[i];
+#pragma unroll
+      for (int c = 4; c < BN; c += 8)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx4[i] = fmax3(mx4[i], s[c + i], c + 4 + i < BN ? s[c + 4 + i] : s[c + i]);
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      const float m_new = fmaxf(m_used, mx * scale_log2);
+      float alpha = 1.f;
+      bool rescale_warp = false;
+      if (u == 0) {
+        m_used = m_new;
+      } else {
+        const bool need = m_new > m_used + kRescaleThreshold;
+        rescale_warp = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2_approx(m_used - m_new);
+          m_used = m_new;
+          l *= alpha;
+        }
+        // O holds P(u-1) V(u-1) once its commit lands (also orders the
+        // rescale below after that product)
+        ok = mbar_wait_warp(o_full, static_cast<uint32_t>(u - 1) & 1u, ab);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 neg2 = make_float2(-m_sub, -m_sub);
+      float2 acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int e = 0; e < BN / 2; ++e) {
+        const float2 x = __ffma2_rn(make_float2(s[2 * e], s[2 * e + 1]), sc2, neg2);
+        const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        acc[e & 3] = __fadd2_rn(acc[e & 3], pe);
+        pk[e] = pack_bf16x2(pe.x, pe.y);
+      }
+      if constexpr (BN == 64) {
+        tmem_st32(lane_base + s_col, pk);
+      } else {
+        tmem_st16(lane_base + s_col, pk);
+      }
+      const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+      if (rescale_warp) {
+#pragma unroll
+        for (int c = 0; c < kDvc / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + C::kOCol + c * 32, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(lane_base + C::kOCol + c * 32, o);
+        }
+      }
+      l += a.x + a.y;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full + (u & 1));
+    }
+
+    // ---- epilogue: O / l -> bf16 -> swizzled staging over Q -> TMA store.
+    // Uniform over the warpgroup, so all 128 threads reach the named barrier.
+    if (qs < p.n_q) {
+      uint8_t* stage = smem + C::kQOff;   // Q is dead once the last product finished
+      bool have_o = ok && n_kv > 0;
+      if (have_o) {
+        have_o = mbar_wait_warp(o_full, static_cast<uint32_t>(n_kv - 1) & 1u, ab);
+        tc_fence_after();
+      }
+      if (have_o || (ok && n_kv == 0)) {
+        const float inv_l = (have_o && l > 0.f) ? 1.f / l : 0.f;
+        if (p.lse != nullptr && chunk == 0 && row < p.n_q)
+          p.lse[static_cast<long long>(bh) * p.n_q + row] =
+              (have_o && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kDvc / 32; ++c) {
+          uint32_t o[32];
+          if (have_o) {
+            tmem_ld32(lane_base + C::kOCol + c * 32, o);
+            tmem_ld_wait();
+            reg_fence(o);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          uint8_t* box = stage + (c >> 1) * C::kQBox;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+            const uint32_t ch = static_cast<uint32_t>((c & 1) * 4 + q4);
+            *reinterpret_cast<uint4*>(box + sw128_offset(static_cast<uint32_t>(row_in_tile), ch)) = v;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1, kBlockM);
+      if (quarter == 0 && lane == 0 && !*abort_flag) {
+        for (int c = 0; c < kDvc / 64; ++c)
+          tma_store_4d(&p.tm_o, stage + c * C::kQBox, chunk * kDvc + c * 64, qs, hi, bi);
+        tma_store_commit();
+        tma_store_wait_read();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DK>
+cudaError_t launch_wide_impl(const SdpaTcParams& p, cudaStream_t stream) {
+  const int smem = WCfg<DK>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_wide<DK>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h * WCfg<DK>::kChunks;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+  sdpa_fwd_wide<DK><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int wide_key_tile(int head_dim) { return head_dim == 256 ? WCfg<256>::BN : WCfg<512>::BN; }
+
+cudaError_t launch_sdpa_wide(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
+  if (head_dim == 256) return launch_wide_impl<256>(p, stream);
+  if (head_dim == 512) return launch_wide_impl<512>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sdpa
