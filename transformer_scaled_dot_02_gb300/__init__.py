@@ -294,3 +294,51 @@ def attention_backward(q, k, v, out, lse, dout, mask_kind=SDPA_MASK_NONE, kv_len
                   workspace.numel() * workspace.element_size(), b, h, n_q, n_k, d, d, mask_kind,
                   kv_lengths, r, scale, stream)
     return dq, dk, dv
+
+
+_copy_streams = {}
+
+
+def attention_from_host(qh, kh, vh, oh, qd, kd, vd, od, mask_kind=SDPA_MASK_NONE, kv_lengths=None,
+                        scale=0.0, heads_per_chunk=None, stream=None):
+    """Attention over pinned HOST tensors: qh/kh/vh [b,h,n,d] bf16 -> oh.
+
+    qd/kd/vd/od are caller-owned device buffers of the same shapes.  The work
+    is cut into (batch, head-range) chunks of `heads_per_chunk` heads; each
+    chunk's host->device copy, sdpa_forward call and device->host copy go on
+    three streams, so copies of one chunk overlap the attention of another.
+    Ordered after prior work on `stream` (default: the current stream), which
+    waits for the last copy back.  kv_lengths: device int32 [b] or None."""
+    import torch
+    main = stream or torch.cuda.current_stream()
+    dev = qd.device
+    if dev not in _copy_streams:
+        _copy_streams[dev] = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
+    s_in, s_cmp, s_out = _copy_streams[dev]
+    b, h, n_q, d = qh.shape
+    n_k = kh.shape[2]
+    hc = heads_per_chunk or h
+    start = torch.cuda.Event()
+    start.record(main)
+    for s in (s_in, s_cmp, s_out):
+        s.wait_event(start)
+    for bi in range(b):
+        for h0 in range(0, h, hc):
+            h1 = min(h, h0 + hc)
+            with torch.cuda.stream(s_in):
+                for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
+                    dst[bi, h0:h1].copy_(src[bi, h0:h1], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_in)
+            s_cmp.wait_event(ev)
+            lens = None if kv_lengths is None else kv_lengths[bi:bi + 1]
+            sdpa_forward(qd[bi, h0:h1], kd[bi, h0:h1], vd[bi, h0:h1], od[bi, h0:h1], 1, h1 - h0, n_q,
+                         n_k, d, d, mask_kind, lens, scale, s_cmp)
+            ev = torch.cuda.Event()
+            ev.record(s_cmp)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                oh[bi, h0:h1].copy_(od[bi, h0:h1], non_blocking=True)
+    end = torch.cuda.Event()
+    end.record(s_out)
+    main.wait_event(end)
