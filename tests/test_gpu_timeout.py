@@ -29,20 +29,26 @@ pytestmark = pytest.mark.gpu
 def faulty_lib():
     sd_build.build()
     d = tempfile.mkdtemp(prefix="sdpa_timeout_")
-    obj = os.path.join(d, "sdpa_tc_withhold.o")
     nvcc = sd_build._nvcc()
-    subprocess.check_call([nvcc] + sd_build._flags() + ["-DSDPA_TEST_WITHHOLD_FIRST_S_COMMIT", "-c",
-                          os.path.join(sd_build.CSRC, "sdpa_tc.cu"), "-o", obj])
+    hooked = ["sdpa_tc.cu", "sdpa_one_tile.cu"]   # both attention kernels carry the hook
+    objs = []
+    for src in hooked:
+        obj = os.path.join(d, src.replace(".cu", "_withhold.o"))
+        subprocess.check_call([nvcc] + sd_build._flags() + ["-DSDPA_TEST_WITHHOLD_FIRST_S_COMMIT",
+                              "-c", os.path.join(sd_build.CSRC, src), "-o", obj])
+        objs.append(obj)
     others = [os.path.join(sd_build.BUILD_DIR, s.replace(".cu", ".o"))
-              for s in sd_build.SOURCES if s != "sdpa_tc.cu"]
+              for s in sd_build.SOURCES if s not in hooked]
     lib_path = os.path.join(d, "libsdpa_withhold.so")
-    subprocess.check_call([nvcc] + sd_build.ARCH + ["-shared", "-cudart", "static", "-o", lib_path,
-                                                   obj] + others)
+    subprocess.check_call([nvcc] + sd_build.ARCH + ["-shared", "-cudart", "static", "-o", lib_path]
+                          + objs + others)
     return sd.load_library(lib_path)
 
 
-def test_bounded_wait_times_out_and_reports(faulty_lib):
+@pytest.mark.parametrize("kernel", ["two_tile", "one_tile"])
+def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, monkeypatch):
     import torch
+    monkeypatch.setenv("LIBSDPA_ATTENTION_KERNEL", kernel)
     rng = np.random.default_rng(1)
     b, h, n, d = 1, 1, 128, 64   # one CTA, one query tile
     q = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))

@@ -2,7 +2,10 @@
 // maps for the TMA, and the launches of the attention and projection kernels.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <cstdint>
 #include <mutex>
 
@@ -79,6 +82,9 @@ sdpa_status current_device(unsigned** status) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Key spans up to this length use the one-tile kernel at d = 128.
+constexpr long long kOneTileMaxKeys = 2048;
 
 // 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
 // boxes of min(d, 64) x 128, swizzled at the row width, zero fill outside.
@@ -165,6 +171,23 @@ float effective_scale(float scale, int d_k) {
   return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
 }
 
+// Kernel choice for tensor-core attention.  LIBSDPA_ATTENTION_KERNEL =
+// "one_tile" / "two_tile" pins it (tests use this to cover both kernels on
+// the same shapes); anything else, or unset, picks by shape.
+// Measured on GB300: the one-tile kernel is as fast or faster at d = 64 for
+// every shape tried, and at d = 128 while a query tile sees at most 2048 keys;
+// beyond that the two-tile kernel keeps the lead (n = 8192 causal).
+bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
+  if (d > 128) return true;
+  if (d < 64) return false;
+  const char* e = std::getenv("LIBSDPA_ATTENTION_KERNEL");
+  if (e != nullptr && std::strcmp(e, "one_tile") == 0) return true;
+  if (e != nullptr && std::strcmp(e, "two_tile") == 0) return false;
+  if (d == 64) return true;
+  const long long span = std::min<long long>(n_k, 1ll * win_left + win_right + 128);
+  return span <= kOneTileMaxKeys;
+}
+
 // Launches the tensor-core attention over tensors with arbitrary (n, h, b)
 // element strides (BHSD for sdpa_forward, BSHD inside mha_forward).
 sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, void* out, int b,
@@ -175,9 +198,11 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
                                 cudaStream_t stream, int win_left = sdpa::kWindowUnbounded,
                                 int win_right = sdpa::kWindowUnbounded, float* lse = nullptr) {
   SdpaTcParams p;
-  // wide heads walk the keys in tiles of 64 (d = 256) or 32 (d = 512)
-  const bool wide = d > 128;
-  const int kv_rows = wide ? sdpa::wide_key_tile(d) : 128;
+  // The one-tile kernel (one 128-row query tile per CTA, 64-key tiles; two
+  // CTAs per SM at d <= 128) takes wide heads, and the short key walks where
+  // the two-tile kernel's longer per-CTA chain would leave SMs idle.
+  const bool one_tile = use_one_tile_kernel(d, n_k, win_left, win_right);
+  const int kv_rows = one_tile ? sdpa::one_tile_key_tile(d) : 128;
   if (!make_map_4d(&p.tm_q, q, d, n_q, h, b, q_sn, q_sh, q_sb) ||
       !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb, kv_rows) ||
       !make_map_4d(&p.tm_v, v, d, n_k, h, b, kv_sn, kv_sh, kv_sb, kv_rows) ||
@@ -190,12 +215,13 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.n_q = n_q;
   p.n_k = n_k;
   p.mask_kind = mask_kind;
-  p.num_q_blocks = wide ? (n_q + 127) / 128 : (n_q + 255) / 256;
+  p.num_q_blocks = one_tile ? (n_q + 127) / 128 : (n_q + 255) / 256;
   p.scale_log2 = effective_scale(scale, d) * 1.4426950408889634f;
   p.win_left = win_left;
   p.win_right = win_right;
   p.lse = lse;
-  const cudaError_t err = wide ? sdpa::launch_sdpa_wide(p, d, stream) : sdpa::launch_sdpa_tc(p, d, stream);
+  const cudaError_t err =
+      one_tile ? sdpa::launch_sdpa_one_tile(p, d, stream) : sdpa::launch_sdpa_tc(p, d, stream);
   return err == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 

@@ -29,10 +29,10 @@ struct SdpaTcParams {
 };
 constexpr int kWindowUnbounded = 1 << 30;
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
-// Wide heads (d = 256, 512): one 128-row query tile per CTA; K/V boxes of
-// wide_key_tile(d) rows; num_q_blocks = ceil(n_q / 128).
-int wide_key_tile(int head_dim);
-cudaError_t launch_sdpa_wide(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
+// One 128-row query tile per CTA (d = 64, 128, 256, 512); K/V boxes of
+// one_tile_key_tile(d) rows; num_q_blocks = ceil(n_q / 128).
+int one_tile_key_tile(int head_dim);
+cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
 
 // One decoding step over a K/V cache on the CUDA cores, split across CTAs.
 struct DecodeParams {

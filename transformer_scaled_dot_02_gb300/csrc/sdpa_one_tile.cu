@@ -1,16 +1,18 @@
-// Scaled dot-product attention for wide heads, d_k = d_v in {256, 512}
-// ("Attention Is All You Need", Table 3, rows (A): fewer heads of larger
-// size at a fixed model width), bf16 in/out, fp32 accumulation, on the
-// tensor cores.  Same operation and masks as the 64/128 kernel (Eq. (1) of
-// section 3.2.1, the -infinity mask of section 3.2.3, key padding and the
-// restricted window of section 4).
-//
-// Wide heads do not fit that kernel's plan of two query tiles with a 128 x d
-// fp32 O accumulator each in the 512 tensor-memory columns, so here one CTA
-// owns ONE 128-row query tile and a 256-column slice of O:
-//   d = 256: key tiles of 64; one CTA per query tile.
-//   d = 512: key tiles of 32; two CTAs per query tile, one per half of d_v,
-//            each recomputing the scores (Q, 128 KB, stays in shared memory).
+// Scaled dot-product attention with ONE 128-row query tile per CTA, bf16
+// in/out, fp32 accumulation, on the tensor cores.  Same operation and masks
+// as the two-tile kernel of sdpa_tc.cu (Eq. (1) of "Attention Is All You
+// Need", section 3.2.1, the -infinity mask of section 3.2.3, key padding and
+// the restricted window of section 4).  It serves two cases:
+//   - wide heads, d_k = d_v in {256, 512} (Table 3, rows (A)), whose 128 x d
+//     fp32 O does not fit the two-tile plan in 512 tensor-memory columns:
+//       d = 256: key tiles of 64; one CTA per query tile.
+//       d = 512: key tiles of 32; two CTAs per query tile, one per half of
+//                d_v, each recomputing the scores (Q, 128 KB, stays in
+//                shared memory).
+//   - d = 64 and 128 where the key walk is short: key tiles of 64, 256
+//     tensor-memory columns, two CTAs per SM, so short sequences get twice
+//     the CTAs in flight and half the serial chain per CTA.
+// Roles:
 //   warp 4      TMA producer: Q once, K_j and V_j (this CTA's d_v slice) in
 //               two stages each.
 //   warp 5      MMA issuer: S(j+1) = Q K_{j+1}^T into the free score buffer,
@@ -19,7 +21,7 @@
 //               running max / sum, P in bf16 over the scores it replaces, the
 //               O rescale when the max moves, and the epilogue.
 // Tensor memory: score buffers S_0 at 0 and S_1 at BN (fp32, BN keys each),
-// O at 2 BN (256 fp32 columns).
+// O at 2 BN (min(d, 256) fp32 columns).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -30,13 +32,13 @@ constexpr int kBlockM = 128;
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDvc = 256;                  // O columns per CTA
 constexpr int kHeadGroup = 8;              // (head, d_v slice) units sharing L2
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the 64/128 kernel
 
 template <int DK>
-struct WCfg {
-  static constexpr int BN = DK == 256 ? 64 : 32;            // keys per tile
+struct OCfg {
+  static constexpr int BN = DK == 512 ? 32 : 64;            // keys per tile
+  static constexpr int kDvc = DK < 256 ? DK : 256;          // O columns per CTA
   static constexpr int kChunks = DK / kDvc;                 // CTAs per query tile
   static constexpr int kQBox = 128 * 128;                   // 64 columns x 128 rows
   static constexpr int kKVBox = BN * 128;                   // 64 columns x BN rows
@@ -55,7 +57,11 @@ struct WCfg {
   static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, kDvc, false, true);
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kKVBox % 1024 == 0, "alignment");
-  static_assert(kOCol + kDvc <= 512, "tensor memory");
+  // d <= 128 fits 256 columns, so two CTAs share an SM
+  static constexpr uint32_t kTmemCols = kOCol + kDvc <= 256 ? 256u : 512u;
+  static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
+  static_assert(kOCol + kDvc <= kTmemCols, "tensor memory");
+  static_assert(kTmemCols == 512 || kSmemBytes <= 232448 / 2 - 1024, "two CTAs per SM");
 };
 
 template <int N>
@@ -65,8 +71,9 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 }
 
 template <int DK>
-__global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_constant__ SdpaTcParams p) {
-  using C = WCfg<DK>;
+__global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
+    sdpa_fwd_one_tile(const __grid_constant__ SdpaTcParams p) {
+  using C = OCfg<DK>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, 512);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -173,9 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
         k_issued = u + 1;
         if (u >= 2 && !mbar_wait(v_empty + s, (use - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(v_full + s, C::kVBytes);
-        for (int c = 0; c < kDvc / 64; ++c)
+        for (int c = 0; c < C::kDvc / 64; ++c)
           tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
-                      chunk * kDvc + c * 64, j * BN, hi, bi);
+                      chunk * C::kDvc + c * 64, j * BN, hi, bi);
         v_issued = u + 1;
       }
       mbar_wait_drain(q_full, 0);
@@ -215,7 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
       tc_fence_after();
       if (ok) {
         issue_s(0);
+#ifndef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
         mma_commit(s_full);
+#endif
+        // (test builds only, never in libsdpa.so: the first score tile is
+        // never signalled, so the softmax warps' bounded wait runs out)
         mma_commit(k_empty);
       }
       for (int u = 0; ok && u < n_kv; ++u) {
@@ -328,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
       const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
       if (rescale_warp) {
 #pragma unroll
-        for (int c = 0; c < kDvc / 32; ++c) {
+        for (int c = 0; c < C::kDvc / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(lane_base + C::kOCol + c * 32, o);
           tmem_ld_wait();
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
           p.lse[static_cast<long long>(bh) * p.n_q + row] =
               (have_o && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kDvc / 32; ++c) {
+        for (int c = 0; c < C::kDvc / 32; ++c) {
           uint32_t o[32];
           if (have_o) {
             tmem_ld32(lane_base + C::kOCol + c * 32, o);
@@ -385,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
       }
       named_bar_sync(1, kBlockM);
       if (quarter == 0 && lane == 0 && !*abort_flag) {
-        for (int c = 0; c < kDvc / 64; ++c)
-          tma_store_4d(&p.tm_o, stage + c * C::kQBox, chunk * kDvc + c * 64, qs, hi, bi);
+        for (int c = 0; c < C::kDvc / 64; ++c)
+          tma_store_4d(&p.tm_o, stage + c * C::kQBox, chunk * C::kDvc + c * 64, qs, hi, bi);
         tma_store_commit();
         tma_store_wait_read();
       }
@@ -397,30 +408,32 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_fwd_wide(const __grid_consta
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
 template <int DK>
-cudaError_t launch_wide_impl(const SdpaTcParams& p, cudaStream_t stream) {
-  const int smem = WCfg<DK>::kSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_wide<DK>,
+cudaError_t launch_one_tile_impl(const SdpaTcParams& p, cudaStream_t stream) {
+  const int smem = OCfg<DK>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_one_tile<DK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h * WCfg<DK>::kChunks;
+  const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h * OCfg<DK>::kChunks;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  sdpa_fwd_wide<DK><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+  sdpa_fwd_one_tile<DK><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int wide_key_tile(int head_dim) { return head_dim == 256 ? WCfg<256>::BN : WCfg<512>::BN; }
+int one_tile_key_tile(int head_dim) { return head_dim == 512 ? OCfg<512>::BN : OCfg<256>::BN; }
 
-cudaError_t launch_sdpa_wide(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
-  if (head_dim == 256) return launch_wide_impl<256>(p, stream);
-  if (head_dim == 512) return launch_wide_impl<512>(p, stream);
+cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
+  if (head_dim == 64) return launch_one_tile_impl<64>(p, stream);
+  if (head_dim == 128) return launch_one_tile_impl<128>(p, stream);
+  if (head_dim == 256) return launch_one_tile_impl<256>(p, stream);
+  if (head_dim == 512) return launch_one_tile_impl<512>(p, stream);
   return cudaErrorInvalidValue;
 }
 
