@@ -49,8 +49,9 @@ struct OCfg {
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + 2 * kKBytes;
   static constexpr int kBarOff = kVOff + 2 * kVBytes;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full, drain
-  static constexpr int kNumBars = 1 + 8 + 4 + 2;
+  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full,
+  // o_last, drain
+  static constexpr int kNumBars = 1 + 8 + 4 + 3;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
@@ -87,8 +88,9 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   uint64_t* v_empty = v_full + 2;
   uint64_t* s_full = v_empty + 2;
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;
-  uint64_t* drain = o_full + 1;
+  uint64_t* o_full = p_full + 2;   // one phase per O += P V
+  uint64_t* o_last = o_full + 1;   // once, after the last O += P V
+  uint64_t* drain = o_last + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const AbortState ab{abort_flag, p.status};
@@ -147,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
       mbar_init(p_full + s, kBlockM);
     }
     mbar_init(o_full, 1);
+    mbar_init(o_last, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
         tc_fence_after();
         issue_pv(u);
         mma_commit(o_full);
+        if (u + 1 == n_kv) mma_commit(o_last);
         mma_commit(v_empty + (u & 1));
       }
       mma_commit(drain);
@@ -311,11 +315,15 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
           m_used = m_new;
           l *= alpha;
         }
-        // O holds P(u-1) V(u-1) once its commit lands (also orders the
-        // rescale below after that product)
-        ok = mbar_wait_warp(o_full, static_cast<uint32_t>(u - 1) & 1u, ab);
-        if (!ok) break;
-        tc_fence_after();
+        // Only a rescale touches O, and it must follow O += P(u-1) V(u-1).
+        // Holding S(u) means O += P(u-2) V(u-2) has landed (S(u) was issued
+        // after it), so o_full is in phase u-1 or u and its parity wait for
+        // phase u-1 is exact even though earlier phases were not waited on.
+        if (rescale_warp) {
+          ok = mbar_wait_warp(o_full, static_cast<uint32_t>(u - 1) & 1u, ab);
+          if (!ok) break;
+          tc_fence_after();
+        }
       }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
       const float2 sc2 = make_float2(scale_log2, scale_log2);
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
       uint8_t* stage = smem + C::kQOff;   // Q is dead once the last product finished
       bool have_o = ok && n_kv > 0;
       if (have_o) {
-        have_o = mbar_wait_warp(o_full, static_cast<uint32_t>(n_kv - 1) & 1u, ab);
+        have_o = mbar_wait_warp(o_last, 0, ab);
         tc_fence_after();
       }
       if (have_o || (ok && n_kv == 0)) {
