@@ -57,10 +57,12 @@ enum { SDPA_MASK_NONE = 0, SDPA_MASK_CAUSAL = 1, SDPA_MASK_PADDING = 2 };
  *   v   [b, h, n_k, d_v]  bf16, device
  *   out [b, h, n_q, d_v]  bf16, device, written (must not overlap the inputs)
  * Scores, softmax statistics and the P.V accumulation are fp32; the
- * softmax weights enter P.V rounded to bf16.  Supported: d_k == d_v in
- * {16, 32, 64, 128, 256, 512}, the head sizes of the paper's Table 3 (else
- * SDPA_ERR_UNSUPPORTED).  256 and 512 run on a kernel of their own with one
- * query tile per CTA; for 512 two CTAs split d_v and both compute the scores.
+ * softmax weights enter P.V rounded to bf16.  Supported (else
+ * SDPA_ERR_UNSUPPORTED), the head shapes of the paper's Table 3:
+ *   d_k == d_v in {16, 32, 64, 128, 256, 512} (rows (A), (C));
+ *   d_k in {16, 32} with d_v == 64 (rows (B): smaller keys than values).
+ * 256 and 512 run on a kernel with one query tile per CTA; for 512 two CTAs
+ * split d_v and both compute the scores.
  * b, h >= 1; n_q, n_k >= 0 (zero-sized work returns SDPA_OK with nothing
  * enqueued; n_k == 0 writes zeros).
  */
@@ -181,7 +183,7 @@ size_t mha_workspace_size(int b, int n_q, int n_k, int h, int d_k, int d_v);
  *   aligned, owned by the caller and reusable once the stream passes the call.
  * Projections run on the tensor cores with fp32 accumulation and bf16
  * outputs; the heads are written straight into the Concat layout.
- * Supported: d_k == d_v in {16, 32, 64, 128, 256, 512}; d_model a multiple of 8.
+ * Supported: the (d_k, d_v) pairs of sdpa_forward; d_model a multiple of 8.
  */
 sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const void* wk,
                         const void* wv, const void* wo, void* y, void* workspace,

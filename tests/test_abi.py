@@ -141,6 +141,8 @@ def test_unsupported_shapes(lib):
     assert _attn(lib, "sdpa_forward", d_k=384, d_v=384) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=1024, d_v=1024) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward", d_k=256, d_v=512) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=64, d_v=16) == UNSUPPORTED
+    assert _attn(lib, "sdpa_forward", d_k=32, d_v=128) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward_f32", d_k=129, d_v=64) == UNSUPPORTED
     assert _attn(lib, "sdpa_forward_f32", b=70000, h=1) == UNSUPPORTED
 
@@ -181,6 +183,8 @@ def test_linear_argument_checks(lib):
 @pytest.mark.skipif(_gpu_visible(), reason="valid placeholder arguments would reach a real GPU")
 def test_valid_arguments_without_gpu_report_no_device(lib):
     assert _attn(lib, "sdpa_forward") == NODEV
+    assert _attn(lib, "sdpa_forward", d_k=16, d_v=64) == NODEV    # Table 3, row (B)
+    assert _attn(lib, "sdpa_forward", d_k=512, d_v=512) == NODEV
     assert _attn(lib, "sdpa_forward_f32", d_k=1, d_v=1) == NODEV
     assert lib.sdpa_forward_restricted(A, A, A, A, 1, 1, 16, 16, 64, 64, 0, None, 3,
                                        ctypes.c_float(0.0), None) == NODEV

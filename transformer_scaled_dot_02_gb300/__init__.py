@@ -265,14 +265,14 @@ def multi_head_attention(xq, xkv, wq, wk, wv, wo, h, mask_kind=SDPA_MASK_NONE, k
 
 def attention_with_lse(q, k, v, mask_kind=SDPA_MASK_NONE, kv_lengths=None, r=0, scale=0.0,
                        stream=None):
-    """Allocates out [b,h,n_q,d] and lse [b,h,n_q] with torch and calls
+    """Allocates out [b,h,n_q,d_v] and lse [b,h,n_q] with torch and calls
     sdpa_forward_lse on bf16 BHSD tensors; returns (out, lse)."""
     import torch
-    b, h, n_q, d = q.shape
-    n_k = k.shape[2]
-    out = torch.empty((b, h, n_q, d), dtype=q.dtype, device=q.device)
+    b, h, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    out = torch.empty((b, h, n_q, d_v), dtype=q.dtype, device=q.device)
     lse = torch.empty((b, h, n_q), dtype=torch.float32, device=q.device)
-    sdpa_forward_lse(q, k, v, out, lse, b, h, n_q, n_k, d, d, mask_kind, kv_lengths, r, scale,
+    sdpa_forward_lse(q, k, v, out, lse, b, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths, r, scale,
                      stream)
     return out, lse
 

@@ -167,6 +167,13 @@ bool tc_head_size(int d) {
   return d == 16 || d == 32 || d == 64 || d == 128 || d == 256 || d == 512;
 }
 
+// (d_k, d_v) pairs the tensor-core attention is built for: equal sizes, or
+// the smaller keys of Table 3's rows (B) against 64-wide values.
+bool tc_head_sizes(int d_k, int d_v) {
+  if (d_k == d_v) return tc_head_size(d_k);
+  return d_v == 64 && (d_k == 16 || d_k == 32);
+}
+
 float effective_scale(float scale, int d_k) {
   return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
 }
@@ -188,25 +195,31 @@ bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
   return span <= kOneTileMaxKeys;
 }
 
+// Element strides of a 4-D (d, n, h, b) tensor along n, h and b.
+struct Strides {
+  long long n, h, b;
+};
+Strides bhsd(int h, int n, int d) { return {d, 1ll * n * d, 1ll * h * n * d}; }
+Strides bshd(int h, int n, int d) { return {1ll * h * d, d, 1ll * n * h * d}; }
+
 // Launches the tensor-core attention over tensors with arbitrary (n, h, b)
 // element strides (BHSD for sdpa_forward, BSHD inside mha_forward).
 sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, void* out, int b,
-                                int h, int n_q, int n_k, int d, long long q_sn, long long q_sh,
-                                long long q_sb, long long kv_sn, long long kv_sh, long long kv_sb,
-                                long long o_sn, long long o_sh, long long o_sb, int mask_kind,
-                                const int32_t* kv_lengths, float scale, unsigned* status,
-                                cudaStream_t stream, int win_left = sdpa::kWindowUnbounded,
+                                int h, int n_q, int n_k, int d_k, int d_v, Strides sq, Strides sk,
+                                Strides sv, Strides so, int mask_kind, const int32_t* kv_lengths,
+                                float scale, unsigned* status, cudaStream_t stream,
+                                int win_left = sdpa::kWindowUnbounded,
                                 int win_right = sdpa::kWindowUnbounded, float* lse = nullptr) {
   SdpaTcParams p;
   // The one-tile kernel (one 128-row query tile per CTA, 64-key tiles; two
   // CTAs per SM at d <= 128) takes wide heads, and the short key walks where
   // the two-tile kernel's longer per-CTA chain would leave SMs idle.
-  const bool one_tile = use_one_tile_kernel(d, n_k, win_left, win_right);
-  const int kv_rows = one_tile ? sdpa::one_tile_key_tile(d) : 128;
-  if (!make_map_4d(&p.tm_q, q, d, n_q, h, b, q_sn, q_sh, q_sb) ||
-      !make_map_4d(&p.tm_k, k, d, n_k, h, b, kv_sn, kv_sh, kv_sb, kv_rows) ||
-      !make_map_4d(&p.tm_v, v, d, n_k, h, b, kv_sn, kv_sh, kv_sb, kv_rows) ||
-      !make_map_4d(&p.tm_o, out, d, n_q, h, b, o_sn, o_sh, o_sb))
+  const bool one_tile = d_k == d_v && use_one_tile_kernel(d_k, n_k, win_left, win_right);
+  const int kv_rows = one_tile ? sdpa::one_tile_key_tile(d_k) : 128;
+  if (!make_map_4d(&p.tm_q, q, d_k, n_q, h, b, sq.n, sq.h, sq.b) ||
+      !make_map_4d(&p.tm_k, k, d_k, n_k, h, b, sk.n, sk.h, sk.b, kv_rows) ||
+      !make_map_4d(&p.tm_v, v, d_v, n_k, h, b, sv.n, sv.h, sv.b, kv_rows) ||
+      !make_map_4d(&p.tm_o, out, d_v, n_q, h, b, so.n, so.h, so.b))
     return SDPA_ERR_CUDA;
   p.kv_lengths = (mask_kind & SDPA_MASK_PADDING) ? kv_lengths : nullptr;
   p.status = status;
@@ -216,12 +229,12 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.n_k = n_k;
   p.mask_kind = mask_kind;
   p.num_q_blocks = one_tile ? (n_q + 127) / 128 : (n_q + 255) / 256;
-  p.scale_log2 = effective_scale(scale, d) * 1.4426950408889634f;
+  p.scale_log2 = effective_scale(scale, d_k) * 1.4426950408889634f;
   p.win_left = win_left;
   p.win_right = win_right;
   p.lse = lse;
-  const cudaError_t err =
-      one_tile ? sdpa::launch_sdpa_one_tile(p, d, stream) : sdpa::launch_sdpa_tc(p, d, stream);
+  const cudaError_t err = one_tile ? sdpa::launch_sdpa_one_tile(p, d_k, stream)
+                                   : sdpa::launch_sdpa_tc(p, d_k, d_v, stream);
   return err == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -246,16 +259,14 @@ sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out,
   sdpa_status st = check_attention_args(q, k, v, out, b, h, n_q, n_k, d_k, d_v, mask_kind,
                                         kv_lengths, scale);
   if (st != SDPA_OK) return st;
-  if (d_k != d_v || !tc_head_size(d_k)) return SDPA_ERR_UNSUPPORTED;
+  if (!tc_head_sizes(d_k, d_v)) return SDPA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = current_device(&status);
   if (st != SDPA_OK) return st;
   if (n_q == 0) return SDPA_OK;
-  const long long d = d_k;
-  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d, 1ll * n_q * d,
-                             1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
-                             1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
-                             static_cast<cudaStream_t>(stream));
+  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d_v, bhsd(h, n_q, d_k),
+                             bhsd(h, n_k, d_k), bhsd(h, n_k, d_v), bhsd(h, n_q, d_v), mask_kind,
+                             kv_lengths, scale, status, static_cast<cudaStream_t>(stream));
 }
 
 sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v, void* out,
@@ -266,18 +277,17 @@ sdpa_status sdpa_forward_restricted(const void* q, const void* k, const void* v,
                                         kv_lengths, scale);
   if (st != SDPA_OK) return st;
   if (r < 1) return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || !tc_head_size(d_k)) return SDPA_ERR_UNSUPPORTED;
+  if (!tc_head_sizes(d_k, d_v)) return SDPA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = current_device(&status);
   if (st != SDPA_OK) return st;
   if (n_q == 0) return SDPA_OK;
-  const long long d = d_k;
   // a neighbourhood of r positions: floor((r-1)/2) before i, floor(r/2) after
   const int left = (r - 1) / 2, right = r / 2;
-  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d, 1ll * n_q * d,
-                             1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
-                             1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
-                             static_cast<cudaStream_t>(stream), left, right);
+  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d_v, bhsd(h, n_q, d_k),
+                             bhsd(h, n_k, d_k), bhsd(h, n_k, d_v), bhsd(h, n_q, d_v), mask_kind,
+                             kv_lengths, scale, status, static_cast<cudaStream_t>(stream), left,
+                             right);
 }
 
 sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -288,18 +298,17 @@ sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* 
   if (st != SDPA_OK) return st;
   if (lse == nullptr || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || r < 0)
     return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || !tc_head_size(d_k)) return SDPA_ERR_UNSUPPORTED;
+  if (!tc_head_sizes(d_k, d_v)) return SDPA_ERR_UNSUPPORTED;
   unsigned* status = nullptr;
   st = current_device(&status);
   if (st != SDPA_OK) return st;
   if (n_q == 0) return SDPA_OK;
-  const long long d = d_k;
   const int left = r > 0 ? (r - 1) / 2 : sdpa::kWindowUnbounded;
   const int right = r > 0 ? r / 2 : sdpa::kWindowUnbounded;
-  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d, 1ll * n_q * d,
-                             1ll * h * n_q * d, d, 1ll * n_k * d, 1ll * h * n_k * d, d,
-                             1ll * n_q * d, 1ll * h * n_q * d, mask_kind, kv_lengths, scale, status,
-                             static_cast<cudaStream_t>(stream), left, right, lse);
+  return launch_attention_tc(q, k, v, out, b, h, n_q, n_k, d_k, d_v, bhsd(h, n_q, d_k),
+                             bhsd(h, n_k, d_k), bhsd(h, n_k, d_v), bhsd(h, n_q, d_v), mask_kind,
+                             kv_lengths, scale, status, static_cast<cudaStream_t>(stream), left,
+                             right, lse);
 }
 
 size_t sdpa_backward_workspace_size(int b, int h, int n_q, int d) {
@@ -490,8 +499,8 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
       (kv_lengths == nullptr || (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0))
     return SDPA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || !tc_head_size(d_k) || d_model % 8 != 0) return SDPA_ERR_UNSUPPORTED;
-  if (1ll * b * (n_q > n_k ? n_q : n_k) > (1ll << 30) || 1ll * h * d_k > 65536)
+  if (!tc_head_sizes(d_k, d_v) || d_model % 8 != 0) return SDPA_ERR_UNSUPPORTED;
+  if (1ll * b * (n_q > n_k ? n_q : n_k) > (1ll << 30) || 1ll * h * (d_k > d_v ? d_k : d_v) > 65536)
     return SDPA_ERR_UNSUPPORTED;
   const size_t need = mha_workspace_size(b, n_q, n_k, h, d_k, d_v);
   if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return SDPA_ERR_WORKSPACE;
@@ -508,7 +517,7 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
   void* op = static_cast<uint8_t*>(vp) + round256(bk * h * d_v * 2);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int m_q = static_cast<int>(bq), m_k = static_cast<int>(bk);
-  const int hd = h * d_k;
+  const int hd = h * d_k, hv = h * d_v;
 
   // Q = X_q W^Q, K = X_kv W^K, V = X_kv W^V in one launch; outputs [b*n, h*d]
   // row-major, which is the per-head layout [b, n, h, d] the attention reads.
@@ -519,16 +528,16 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
     return SDPA_ERR_CUDA;
   if (m_k > 0) {
     if (!fill_gemm_problem(&gp.prob[gp.num_problems++], xkv, wk, kp, m_k, hd, d_model) ||
-        !fill_gemm_problem(&gp.prob[gp.num_problems++], xkv, wv, vp, m_k, hd, d_model))
+        !fill_gemm_problem(&gp.prob[gp.num_problems++], xkv, wv, vp, m_k, hv, d_model))
       return SDPA_ERR_CUDA;
   }
-  if (sdpa::launch_gemm_tc(gp, m_q > m_k ? m_q : m_k, hd, s) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (sdpa::launch_gemm_tc(gp, m_q > m_k ? m_q : m_k, hd > hv ? hd : hv, s) != cudaSuccess)
+    return SDPA_ERR_CUDA;
 
   // Heads: strides of [b, n, h, d]; the output lands in Concat order.
-  const long long d = d_k;
-  st = launch_attention_tc(qp, kp, vp, op, b, h, n_q, n_k, d_k, 1ll * h * d, d, 1ll * n_q * h * d,
-                           1ll * h * d, d, 1ll * n_k * h * d, 1ll * h * d, d, 1ll * n_q * h * d,
-                           mask_kind, kv_lengths, scale, status, s);
+  st = launch_attention_tc(qp, kp, vp, op, b, h, n_q, n_k, d_k, d_v, bshd(h, n_q, d_k),
+                           bshd(h, n_k, d_k), bshd(h, n_k, d_v), bshd(h, n_q, d_v), mask_kind,
+                           kv_lengths, scale, status, s);
   if (st != SDPA_OK) return st;
 
   // Y = Concat(heads) W^O

@@ -28,7 +28,8 @@ struct SdpaTcParams {
   float* lse;                 // optional [b, h, n_q] natural log-sum-exp per row
 };
 constexpr int kWindowUnbounded = 1 << 30;
-cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
+// Two query tiles per CTA; (d_k, d_v) in {(16,16), (32,32), (64,64), (128,128), (16,64), (32,64)}.
+cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int d_k, int d_v, cudaStream_t stream);
 // One 128-row query tile per CTA (d = 64, 128, 256, 512); K/V boxes of
 // one_tile_key_tile(d) rows; num_q_blocks = ceil(n_q / 128).
 int one_tile_key_tile(int head_dim);

@@ -50,6 +50,8 @@ constexpr int kHeadGroup = 8;    // heads whose K/V share L2 at a time
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: a factor of 256
 
+// Layout of one operand whose rows hold D bf16 values (Q and K at d_k; V
+// and O at d_v).
 template <int D>
 struct Cfg {
   // Tiles move as boxes of kBoxCols columns x 128 rows, rows of kRowBytes
@@ -63,18 +65,31 @@ struct Cfg {
   static constexpr int kStepsPerRow = kRowBytes / 32;      // K=16 steps per swizzled row
   static constexpr int kOChunk = D < 32 ? D : 32;          // O columns per TMEM load
   static constexpr int kTileBytes = kBlockM * D * 2;
-  // K/V ring depths: Q (2 tiles) + K + V stages fill the 227 KB of shared memory.
-  static constexpr int kKStages = (D == 128) ? 2 : 4;
-  static constexpr int kVStages = (D == 128) ? 2 : 4;
   static_assert(D == 16 || D == 32 || D == 64 || D == 128, "head size");
+};
+
+// Shared memory of one CTA for key size DK and value size DV: two Q tiles,
+// rings of K and V tiles, and the two O tiles' staging for the TMA store
+// (over the Q tiles when those are at least as large).
+template <int DK, int DV>
+struct Plan {
+  using CK = Cfg<DK>;
+  using CV = Cfg<DV>;
+  // K/V ring depths: Q (2 tiles) + K + V stages fill the 227 KB of shared memory.
+  static constexpr int kKStages = (DK == 128 || DV == 128) ? 2 : 4;
+  static constexpr int kVStages = kKStages;
+  static constexpr bool kStageOverQ = CK::kTileBytes >= CV::kTileBytes;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kKOff = kQOff + 2 * CK::kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * CK::kTileBytes;
+  static constexpr int kVEnd = kVOff + kVStages * CV::kTileBytes;
+  static constexpr int kStageOff = kStageOverQ ? kQOff : kVEnd;
+  static constexpr int kBarOff = kStageOverQ ? kVEnd : kVEnd + 2 * CV::kTileBytes;
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6 + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false, false);
-  static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, D, false, true);
+  static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, DV, false, true);
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct Bars {
@@ -101,10 +116,12 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-template <int D>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
-  using C = Cfg<D>;
+  using C = Plan<DK, DV>;
+  using CK = Cfg<DK>;
+  using CV = Cfg<DV>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms.
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -213,15 +230,15 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_o);
       uint32_t q_bytes = 0;
-      q_bytes += has0 ? C::kTileBytes : 0;
-      q_bytes += has1 ? C::kTileBytes : 0;
+      q_bytes += has0 ? CK::kTileBytes : 0;
+      q_bytes += has1 ? CK::kTileBytes : 0;
       if (q_bytes > 0) {
         mbar_arrive_expect_tx(bars.q_full, q_bytes);
         for (int t = 0; t < 2; ++t) {
           if (hi_of(t) <= lo_of(t)) continue;
-          for (int c = 0; c < C::kBoxes; ++c)
-            tma_load_4d(&p.tm_q, bars.q_full, smem + C::kQOff + t * C::kTileBytes + c * C::kBoxBytes,
-                        c * C::kBoxCols, q0 + t * kBlockM, hi, bi);
+          for (int c = 0; c < CK::kBoxes; ++c)
+            tma_load_4d(&p.tm_q, bars.q_full, smem + C::kQOff + t * CK::kTileBytes + c * CK::kBoxBytes,
+                        c * CK::kBoxCols, q0 + t * kBlockM, hi, bi);
         }
       }
       int k_issued = 0, v_issued = 0;  // tiles whose K (V) copy was started
@@ -230,19 +247,19 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         const int sk = u % C::kKStages;
         const uint32_t uk = static_cast<uint32_t>(u / C::kKStages);
         if (u >= C::kKStages && !mbar_wait(bars.k_empty + sk, (uk - 1) & 1u, ab)) break;
-        mbar_arrive_expect_tx(bars.k_full + sk, C::kTileBytes);
-        for (int c = 0; c < C::kBoxes; ++c)
+        mbar_arrive_expect_tx(bars.k_full + sk, CK::kTileBytes);
+        for (int c = 0; c < CK::kBoxes; ++c)
           tma_load_4d(&p.tm_k, bars.k_full + sk,
-                      smem + C::kKOff + sk * C::kTileBytes + c * C::kBoxBytes, c * C::kBoxCols,
+                      smem + C::kKOff + sk * CK::kTileBytes + c * CK::kBoxBytes, c * CK::kBoxCols,
                       j * kBlockN, hi, bi);
         k_issued = u + 1;
         const int sv = u % C::kVStages;
         const uint32_t uv = static_cast<uint32_t>(u / C::kVStages);
         if (u >= C::kVStages && !mbar_wait(bars.v_empty + sv, (uv - 1) & 1u, ab)) break;
-        mbar_arrive_expect_tx(bars.v_full + sv, C::kTileBytes);
-        for (int c = 0; c < C::kBoxes; ++c)
+        mbar_arrive_expect_tx(bars.v_full + sv, CV::kTileBytes);
+        for (int c = 0; c < CV::kBoxes; ++c)
           tma_load_4d(&p.tm_v, bars.v_full + sv,
-                      smem + C::kVOff + sv * C::kTileBytes + c * C::kBoxBytes, c * C::kBoxCols,
+                      smem + C::kVOff + sv * CV::kTileBytes + c * CV::kBoxBytes, c * CV::kBoxCols,
                       j * kBlockN, hi, bi);
         v_issued = u + 1;
       }
@@ -262,31 +279,31 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       // Descriptors split in halves: the high word is fixed by the layout, the
       // low word holds (address >> 4) and the leading offset; a K step adds
       // its byte offset >> 4 to the low word (no carry: smem < 256 KB).
-      const uint64_t kq = smem_desc(q_smem, 16, C::kSBO, C::kLayout);
-      const uint64_t kk = smem_desc(k_smem, 16, C::kSBO, C::kLayout);
-      const uint64_t kv = smem_desc(v_smem, C::kBoxBytes, C::kSBO, C::kLayout);
+      const uint64_t kq = smem_desc(q_smem, 16, CK::kSBO, CK::kLayout);
+      const uint64_t kk = smem_desc(k_smem, 16, CK::kSBO, CK::kLayout);
+      const uint64_t kv = smem_desc(v_smem, CV::kBoxBytes, CV::kSBO, CV::kLayout);
       const uint32_t q_lo = static_cast<uint32_t>(kq), qk_hi = static_cast<uint32_t>(kq >> 32);
       const uint32_t k_lo = static_cast<uint32_t>(kk);
       const uint32_t v_lo = static_cast<uint32_t>(kv), v_hi = static_cast<uint32_t>(kv >> 32);
       auto issue_s = [&](int t, int stage) {
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
-        const uint32_t a0 = q_lo + static_cast<uint32_t>((t * C::kTileBytes) >> 4);
-        const uint32_t b0 = k_lo + static_cast<uint32_t>((stage * C::kTileBytes) >> 4);
+        const uint32_t a0 = q_lo + static_cast<uint32_t>((t * CK::kTileBytes) >> 4);
+        const uint32_t b0 = k_lo + static_cast<uint32_t>((stage * CK::kTileBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < DK / 16; ++k) {
           const uint32_t off = static_cast<uint32_t>(
-              ((k / C::kStepsPerRow) * C::kBoxBytes + (k % C::kStepsPerRow) * 32) >> 4);
+              ((k / CK::kStepsPerRow) * CK::kBoxBytes + (k % CK::kStepsPerRow) * 32) >> 4);
           mma_bf16_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int stage, bool accumulate) {
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(256 + t * D);
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(256 + t * DV);
         const uint32_t p_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
-        const uint32_t b0 = v_lo + static_cast<uint32_t>((stage * C::kTileBytes) >> 4);
+        const uint32_t b0 = v_lo + static_cast<uint32_t>((stage * CV::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k) {
           mma_bf16_ts_lohi(d_tmem, p_tmem + static_cast<uint32_t>(k * 8),
-                           b0 + static_cast<uint32_t>((k * 16 * C::kRowBytes) >> 4), v_hi, C::kIdescPV,
+                           b0 + static_cast<uint32_t>((k * 16 * CV::kRowBytes) >> 4), v_hi, C::kIdescPV,
                            (accumulate || k > 0) ? 1u : 0u);
         }
       };
@@ -366,7 +383,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
     const int row = q_start_t + row_in_tile;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t s_col = static_cast<uint32_t>(t * kBlockN);
-    const uint32_t o_col = static_cast<uint32_t>(256 + t * D);
+    const uint32_t o_col = static_cast<uint32_t>(256 + t * DV);
     const float scale_log2 = p.scale_log2;
     const int t_lo = lo_of(t), t_hi = hi_of(t);
     const int n_t = t_hi - t_lo;
@@ -460,14 +477,14 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       // covers every MMA issued before it, PV_t(j-1) included.
       if (rescale_warp) {
 #pragma unroll
-        for (int c = 0; c < D / C::kOChunk; ++c) {
-          uint32_t o[C::kOChunk];
-          tmem_ld_chunk(lane_base + o_col + c * C::kOChunk, o);
+        for (int c = 0; c < DV / CV::kOChunk; ++c) {
+          uint32_t o[CV::kOChunk];
+          tmem_ld_chunk(lane_base + o_col + c * CV::kOChunk, o);
           tmem_ld_wait();
           reg_fence(o);
 #pragma unroll
-          for (int e = 0; e < C::kOChunk; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_chunk(lane_base + o_col + c * C::kOChunk, o);
+          for (int e = 0; e < CV::kOChunk; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_chunk(lane_base + o_col + c * CV::kOChunk, o);
         }
       }
       l += rowsum;
@@ -476,11 +493,12 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
       mbar_arrive(bars.p_full + t);
     }
 
-    // ---- epilogue: O / l -> bf16 -> swizzled staging (Q_t's smem) -> TMA store.
+    // ---- epilogue: O / l -> bf16 -> swizzled staging (over Q_t when it is at
+    // least as large, else a region of its own) -> TMA store.
     // The branch is uniform over the warpgroup, so all 128 threads reach the
     // named barrier; a warp whose waits failed skips only its own writes.
     if (q_start_t < p.n_q) {
-      uint8_t* stage = smem + C::kQOff + t * C::kTileBytes;
+      uint8_t* stage = smem + C::kStageOff + t * CV::kTileBytes;
       bool have_o = ok && n_t > 0;
       if (have_o) {
         have_o = mbar_wait_warp(bars.o_full + t, static_cast<uint32_t>(n_t - 1) & 1u, ab);
@@ -494,36 +512,36 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
               (have_o && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
 #pragma unroll
-        for (int c = 0; c < D / C::kOChunk; ++c) {
-          uint32_t o[C::kOChunk];
+        for (int c = 0; c < DV / CV::kOChunk; ++c) {
+          uint32_t o[CV::kOChunk];
           if (have_o) {
-            tmem_ld_chunk(lane_base + o_col + c * C::kOChunk, o);
+            tmem_ld_chunk(lane_base + o_col + c * CV::kOChunk, o);
             tmem_ld_wait();
             reg_fence(o);
           } else {
 #pragma unroll
-            for (int e = 0; e < C::kOChunk; ++e) o[e] = 0u;
+            for (int e = 0; e < CV::kOChunk; ++e) o[e] = 0u;
           }
-          const int col0 = c * C::kOChunk;                 // first O column of this chunk
-          uint8_t* box = stage + (col0 / C::kBoxCols) * C::kBoxBytes;
+          const int col0 = c * CV::kOChunk;                // first O column of this chunk
+          uint8_t* box = stage + (col0 / CV::kBoxCols) * CV::kBoxBytes;
 #pragma unroll
-          for (int q4 = 0; q4 < C::kOChunk / 8; ++q4) {
+          for (int q4 = 0; q4 < CV::kOChunk / 8; ++q4) {
             uint4 v;
             v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
             v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
             v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
             v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-            const uint32_t chunk = static_cast<uint32_t>((col0 % C::kBoxCols) / 8 + q4);
+            const uint32_t chunk = static_cast<uint32_t>((col0 % CV::kBoxCols) / 8 + q4);
             *reinterpret_cast<uint4*>(
-                box + swizzle_offset<C::kRowBytes>(static_cast<uint32_t>(row_in_tile), chunk)) = v;
+                box + swizzle_offset<CV::kRowBytes>(static_cast<uint32_t>(row_in_tile), chunk)) = v;
           }
         }
         fence_proxy_async_smem();
       }
       named_bar_sync(1 + t, 128);
       if (quarter == 0 && lane == 0 && !*abort_flag) {
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_store_4d(&p.tm_o, stage + c * C::kBoxBytes, c * C::kBoxCols, q_start_t, hi, bi);
+        for (int c = 0; c < CV::kBoxes; ++c)
+          tma_store_4d(&p.tm_o, stage + c * CV::kBoxBytes, c * CV::kBoxCols, q_start_t, hi, bi);
         tma_store_commit();
         tma_store_wait_read();
       }
@@ -539,26 +557,31 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   }
 }
 
-template <int D>
+template <int DK, int DV>
 cudaError_t launch_impl(const SdpaTcParams& p, cudaStream_t stream) {
-  const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_bf16_tc<D>,
+  const int smem = Plan<DK, DV>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_bf16_tc<DK, DV>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  sdpa_fwd_bf16_tc<D><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
+  sdpa_fwd_bf16_tc<DK, DV><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
-  if (head_dim == 16) return launch_impl<16>(p, stream);
-  if (head_dim == 32) return launch_impl<32>(p, stream);
-  if (head_dim == 64) return launch_impl<64>(p, stream);
-  if (head_dim == 128) return launch_impl<128>(p, stream);
+cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int d_k, int d_v, cudaStream_t stream) {
+  if (d_k == d_v) {
+    if (d_k == 16) return launch_impl<16, 16>(p, stream);
+    if (d_k == 32) return launch_impl<32, 32>(p, stream);
+    if (d_k == 64) return launch_impl<64, 64>(p, stream);
+    if (d_k == 128) return launch_impl<128, 128>(p, stream);
+  }
+  // Table 3, rows (B): smaller keys than values
+  if (d_k == 16 && d_v == 64) return launch_impl<16, 64>(p, stream);
+  if (d_k == 32 && d_v == 64) return launch_impl<32, 64>(p, stream);
   return cudaErrorInvalidValue;
 }
 
