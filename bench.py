@@ -165,6 +165,23 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(value, pg, device):
+    """The largest `value` of all ranks, on every rank (`value` itself with no
+    process group): the job takes as long as its slowest replica."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, flops_per_step, steps, ms):
+    """Whole-job TFLOP/s: every replica's work over the slowest rank's time
+    (weak scaling: each rank runs the full workload on its own GPU)."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------- ours
 def run_ours(args, world, rank, local):
     import torch
@@ -218,10 +235,7 @@ def run_ours(args, world, rank, local):
     sd.sdpa_device_check()
     total_ms = t0.elapsed_time(t1)
     launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
 
     # end to end through the C ABI: pinned host inputs -> device -> attention -> host
     e2e_steps = max(1, min(args.steps, 20))
@@ -249,15 +263,12 @@ def run_ours(args, world, rank, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, pg, dev)
     sd.sdpa_device_check()
 
     flops = metric_flops(w)
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    value = job_throughput(world, flops, args.steps, total_ms)
+    e2e_value = job_throughput(world, flops, e2e_steps, e2e_ms)
     peaks, peak_src = load_peaks()
     mean_launch_ms = float(np.mean(launch_ms))
     achieved = flops / (mean_launch_ms * 1e-3) / 1e12
