@@ -298,7 +298,7 @@ def run_ours(args, world, rank, local):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": "%s bf16_tflops (burst)" % peak_src,
                      "frac_of_sustained": round(achieved / peak_sus, 4),
-                     "traffic": traffic, "kernel": "sdpa_fwd_bf16_tc<128>",
+                     "traffic": traffic, "kernel": "sdpa_fwd_bf16_tc<128, 128>",
                      "launch_ms_mean": round(mean_launch_ms, 4),
                      "launch_ms_min": round(float(np.min(launch_ms)), 4)},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
