@@ -1,7 +1,8 @@
-"""Both tensor-core attention kernels at head sizes 64 and 128, each pinned
+"""Both tensor-core attention kernels at head sizes 16, 32, 64 and 128, each pinned
 with LIBSDPA_ATTENTION_KERNEL, against the oracle (2e-2 of the output scale):
 the two-tile kernel (two 128-row query tiles per CTA, 128-key tiles) and the
-one-tile kernel (one query tile per CTA, 64-key tiles, two CTAs per SM).
+one-tile kernel (one query tile per CTA; 64-key tiles and two CTAs per SM at
+d = 64, 128; 32-key tiles and four CTAs per SM at d = 16, 32).
 The library picks between them by shape; these tests keep both covered on
 the same shapes, masks, windows and ragged tails."""
 import numpy as np
@@ -20,7 +21,7 @@ def _rand(rng, shape, std=1.0):
 
 
 @pytest.mark.parametrize("kernel", ["two_tile", "one_tile"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("mask,r", [(0, 0), (1, 0), (2, 0), (3, 0), (1, 100), (0, 257)])
 def test_kernel_parity(kernel, d, mask, r, monkeypatch):
     monkeypatch.setenv("LIBSDPA_ATTENTION_KERNEL", kernel)
@@ -44,7 +45,7 @@ def test_kernel_parity(kernel, d, mask, r, monkeypatch):
     assert np.abs(got_lse[fin] - ref_lse[fin]).max() <= 1e-3
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 def test_kernels_agree_on_long_causal(d, monkeypatch):
     """b1 h2 n2048 causal: the two kernels agree to bf16 rounding."""
     t = __import__("torch")

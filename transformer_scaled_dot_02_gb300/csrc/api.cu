@@ -181,16 +181,16 @@ float effective_scale(float scale, int d_k) {
 // Kernel choice for tensor-core attention.  LIBSDPA_ATTENTION_KERNEL =
 // "one_tile" / "two_tile" pins it (tests use this to cover both kernels on
 // the same shapes); anything else, or unset, picks by shape.
-// Measured on GB300: the one-tile kernel is as fast or faster at d = 64 for
-// every shape tried, and at d = 128 while a query tile sees at most 2048 keys;
-// beyond that the two-tile kernel keeps the lead (n = 8192 causal).
+// Measured on GB300: the one-tile kernel is as fast or faster at d = 16, 32
+// and 64 for every shape tried, and at d = 128 while a query tile sees at
+// most 2048 keys; beyond that the two-tile kernel keeps the lead (n = 8192
+// causal).
 bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
   if (d > 128) return true;
-  if (d < 64) return false;
   const char* e = std::getenv("LIBSDPA_ATTENTION_KERNEL");
   if (e != nullptr && std::strcmp(e, "one_tile") == 0) return true;
   if (e != nullptr && std::strcmp(e, "two_tile") == 0) return false;
-  if (d == 64) return true;
+  if (d <= 64) return true;
   const long long span = std::min<long long>(n_k, 1ll * win_left + win_right + 128);
   return span <= kOneTileMaxKeys;
 }
@@ -211,9 +211,10 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
                                 int win_left = sdpa::kWindowUnbounded,
                                 int win_right = sdpa::kWindowUnbounded, float* lse = nullptr) {
   SdpaTcParams p;
-  // The one-tile kernel (one 128-row query tile per CTA, 64-key tiles; two
-  // CTAs per SM at d <= 128) takes wide heads, and the short key walks where
-  // the two-tile kernel's longer per-CTA chain would leave SMs idle.
+  // The one-tile kernel (one 128-row query tile per CTA, 32- or 64-key tiles;
+  // two or four CTAs per SM at d <= 128) takes wide heads, small heads, and
+  // the short key walks where the two-tile kernel's longer per-CTA chain
+  // would leave SMs idle.  Unequal key and value sizes take the two-tile one.
   const bool one_tile = d_k == d_v && use_one_tile_kernel(d_k, n_k, win_left, win_right);
   const int kv_rows = one_tile ? sdpa::one_tile_key_tile(d_k) : 128;
   if (!make_map_4d(&p.tm_q, q, d_k, n_q, h, b, sq.n, sq.h, sq.b) ||

@@ -37,14 +37,22 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the 64/128 kerne
 
 template <int DK>
 struct OCfg {
-  static constexpr int BN = DK == 512 ? 32 : 64;            // keys per tile
+  static constexpr int BN = (DK == 512 || DK < 64) ? 32 : 64;   // keys per tile
   static constexpr int kDvc = DK < 256 ? DK : 256;          // O columns per CTA
   static constexpr int kChunks = DK / kDvc;                 // CTAs per query tile
-  static constexpr int kQBox = 128 * 128;                   // 64 columns x 128 rows
-  static constexpr int kKVBox = BN * 128;                   // 64 columns x BN rows
-  static constexpr int kQBytes = (DK / 64) * kQBox;
-  static constexpr int kKBytes = (DK / 64) * kKVBox;
-  static constexpr int kVBytes = (kDvc / 64) * kKVBox;
+  // Tiles move as boxes of kBoxCols columns, rows of kRowBytes swizzled at
+  // that width (128-, 64- or 32-byte swizzle for d >= 64, 32, 16).
+  static constexpr int kBoxCols = DK < 64 ? DK : 64;
+  static constexpr int kRowBytes = kBoxCols * 2;
+  static constexpr uint32_t kLayout = kRowBytes == 128 ? 2u : (kRowBytes == 64 ? 4u : 6u);
+  static constexpr uint32_t kSBO = 8 * kRowBytes;           // 8-row group stride
+  static constexpr int kStepsPerRow = kRowBytes / 32;       // K=16 steps per swizzled row
+  static constexpr int kOChunk = kDvc < 32 ? kDvc : 32;     // O columns per TMEM load
+  static constexpr int kQBox = 128 * kRowBytes;             // kBoxCols columns x 128 rows
+  static constexpr int kKVBox = BN * kRowBytes;             // kBoxCols columns x BN rows
+  static constexpr int kQBytes = (DK / kBoxCols) * kQBox;
+  static constexpr int kKBytes = (DK / kBoxCols) * kKVBox;
+  static constexpr int kVBytes = (kDvc / kBoxCols) * kKVBox;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + 2 * kKBytes;
@@ -56,14 +64,22 @@ struct OCfg {
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, kDvc, false, true);
+  static constexpr uint32_t kDescHi = (kSBO >> 4) | (1u << 14) | (kLayout << 29);
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kKOff % 1024 == 0 && kVOff % 1024 == 0 && kKVBox % 1024 == 0, "alignment");
-  // d <= 128 fits 256 columns, so two CTAs share an SM
-  static constexpr uint32_t kTmemCols = kOCol + kDvc <= 256 ? 256u : 512u;
-  static constexpr int kMinBlocks = kTmemCols == 256 ? 2 : 1;
+  // d <= 128 fits 256 columns (two CTAs per SM), d <= 32 fits 128 (four)
+  static constexpr uint32_t kTmemCols =
+      kOCol + kDvc <= 128 ? 128u : (kOCol + kDvc <= 256 ? 256u : 512u);
+  static constexpr int kMinBlocks = static_cast<int>(512u / kTmemCols);
   static_assert(kOCol + kDvc <= kTmemCols, "tensor memory");
-  static_assert(kTmemCols == 512 || kSmemBytes <= 232448 / 2 - 1024, "two CTAs per SM");
+  static_assert(kSmemBytes * kMinBlocks <= 232448 - 1024 * kMinBlocks, "CTAs per SM");
 };
+
+// TMEM loads / stores of 32 or 16 columns (32x32b shape).
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
+__device__ __forceinline__ void tmem_st_chunk(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
 
 template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
@@ -168,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_o);
       mbar_arrive_expect_tx(q_full, C::kQBytes);
-      for (int c = 0; c < DK / 64; ++c)
-        tma_load_4d(&p.tm_q, q_full, smem + C::kQOff + c * C::kQBox, c * 64, qs, hi, bi);
+      for (int c = 0; c < DK / C::kBoxCols; ++c)
+        tma_load_4d(&p.tm_q, q_full, smem + C::kQOff + c * C::kQBox, c * C::kBoxCols, qs, hi, bi);
       int k_issued = 0, v_issued = 0;
       for (int u = 0; u < n_kv; ++u) {
         const int j = j_lo + u;
@@ -177,15 +193,16 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
         const uint32_t use = static_cast<uint32_t>(u >> 1);
         if (u >= 2 && !mbar_wait(k_empty + s, (use - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(k_full + s, C::kKBytes);
-        for (int c = 0; c < DK / 64; ++c)
-          tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox, c * 64,
+        for (int c = 0; c < DK / C::kBoxCols; ++c)
+          tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox,
+                      c * C::kBoxCols,
                       j * BN, hi, bi);
         k_issued = u + 1;
         if (u >= 2 && !mbar_wait(v_empty + s, (use - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(v_full + s, C::kVBytes);
-        for (int c = 0; c < C::kDvc / 64; ++c)
+        for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
           tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
-                      chunk * C::kDvc + c * 64, j * BN, hi, bi);
+                      chunk * C::kDvc + c * C::kBoxCols, j * BN, hi, bi);
         v_issued = u + 1;
       }
       mbar_wait_drain(q_full, 0);
@@ -197,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      constexpr uint32_t kDescHi = C::kDescHi;
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       const uint32_t q_lo = lo(smem_base + C::kQOff, 16);
       auto issue_s = [&](int u) {
@@ -205,9 +222,10 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
         const uint32_t b0 = lo(smem_base + C::kKOff + (u & 1) * C::kKBytes, 16);
 #pragma unroll
         for (int k = 0; k < DK / 16; ++k) {
-          mma_bf16_ss_lohi(d, q_lo + static_cast<uint32_t>(((k >> 2) * C::kQBox + (k & 3) * 32) >> 4),
+          constexpr int kS = C::kStepsPerRow;
+          mma_bf16_ss_lohi(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
                            kDescHi,
-                           b0 + static_cast<uint32_t>(((k >> 2) * C::kKVBox + (k & 3) * 32) >> 4),
+                           b0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4),
                            kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
@@ -217,7 +235,8 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           mma_bf16_ts_lohi(tmem + C::kOCol, pa + static_cast<uint32_t>(k * 8),
-                           b0 + static_cast<uint32_t>((k * 16 * 128) >> 4), kDescHi, C::kIdescPV,
+                           b0 + static_cast<uint32_t>((k * 16 * C::kRowBytes) >> 4), kDescHi,
+                           C::kIdescPV,
                            (u > 0 || k > 0) ? 1u : 0u);
         }
       };
@@ -347,14 +366,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
       const float2 a = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
       if (rescale_warp) {
 #pragma unroll
-        for (int c = 0; c < C::kDvc / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + C::kOCol + c * 32, o);
+        for (int c = 0; c < C::kDvc / C::kOChunk; ++c) {
+          uint32_t o[C::kOChunk];
+          tmem_ld_chunk(lane_base + C::kOCol + c * C::kOChunk, o);
           tmem_ld_wait();
           reg_fence(o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(lane_base + C::kOCol + c * 32, o);
+          for (int e = 0; e < C::kOChunk; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_chunk(lane_base + C::kOCol + c * C::kOChunk, o);
         }
       }
       l += a.x + a.y;
@@ -378,34 +397,37 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
           p.lse[static_cast<long long>(bh) * p.n_q + row] =
               (have_o && l > 0.f) ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
 #pragma unroll
-        for (int c = 0; c < C::kDvc / 32; ++c) {
-          uint32_t o[32];
+        for (int c = 0; c < C::kDvc / C::kOChunk; ++c) {
+          uint32_t o[C::kOChunk];
           if (have_o) {
-            tmem_ld32(lane_base + C::kOCol + c * 32, o);
+            tmem_ld_chunk(lane_base + C::kOCol + c * C::kOChunk, o);
             tmem_ld_wait();
             reg_fence(o);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
+            for (int e = 0; e < C::kOChunk; ++e) o[e] = 0u;
           }
-          uint8_t* box = stage + (c >> 1) * C::kQBox;
+          const int col0 = c * C::kOChunk;                  // first O column of this chunk
+          uint8_t* box = stage + (col0 / C::kBoxCols) * C::kQBox;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q4 = 0; q4 < C::kOChunk / 8; ++q4) {
             uint4 v;
             v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
             v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
             v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
             v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-            const uint32_t ch = static_cast<uint32_t>((c & 1) * 4 + q4);
-            *reinterpret_cast<uint4*>(box + sw128_offset(static_cast<uint32_t>(row_in_tile), ch)) = v;
+            const uint32_t ch = static_cast<uint32_t>((col0 % C::kBoxCols) / 8 + q4);
+            *reinterpret_cast<uint4*>(
+                box + swizzle_offset<C::kRowBytes>(static_cast<uint32_t>(row_in_tile), ch)) = v;
           }
         }
         fence_proxy_async_smem();
       }
       named_bar_sync(1, kBlockM);
       if (quarter == 0 && lane == 0 && !*abort_flag) {
-        for (int c = 0; c < C::kDvc / 64; ++c)
-          tma_store_4d(&p.tm_o, stage + c * C::kQBox, chunk * C::kDvc + c * 64, qs, hi, bi);
+        for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
+          tma_store_4d(&p.tm_o, stage + c * C::kQBox, chunk * C::kDvc + c * C::kBoxCols, qs, hi,
+                       bi);
         tma_store_commit();
         tma_store_wait_read();
       }
@@ -435,9 +457,13 @@ cudaError_t launch_one_tile_impl(const SdpaTcParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-int one_tile_key_tile(int head_dim) { return head_dim == 512 ? OCfg<512>::BN : OCfg<256>::BN; }
+int one_tile_key_tile(int head_dim) {
+  return (head_dim == 512 || head_dim < 64) ? OCfg<512>::BN : OCfg<256>::BN;
+}
 
 cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
+  if (head_dim == 16) return launch_one_tile_impl<16>(p, stream);
+  if (head_dim == 32) return launch_one_tile_impl<32>(p, stream);
   if (head_dim == 64) return launch_one_tile_impl<64>(p, stream);
   if (head_dim == 128) return launch_one_tile_impl<128>(p, stream);
   if (head_dim == 256) return launch_one_tile_impl<256>(p, stream);
