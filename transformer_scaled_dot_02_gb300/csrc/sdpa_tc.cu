@@ -1,16 +1,20 @@
 // Fused scaled dot-product attention, bf16 in/out, fp32 accumulation, on the
-// GB300 tensor cores (tcgen05 + TMA + tensor memory).
+// GB300 tensor cores (tcgen05 + TMA + tensor memory): the two-tile kernel.
 //
 // Operation ("Attention Is All You Need", section 3.2.1, Eq. (1), with the
-// decoder's -infinity mask of section 3.2.3 and a key-padding mask):
+// decoder's -infinity mask of section 3.2.3, a key-padding mask and the
+// restricted window of section 4):
 //   O[i, :] = sum_j softmax_j(scale * Q[i, :] . K[j, :]) V[j, :]
 // evaluated as an online (streaming) softmax over 128-key tiles, so the
-// n_q x n_k score matrix never leaves the SM.
+// n_q x n_k score matrix never leaves the SM.  The library runs it for long
+// key walks at d = 128 and for keys smaller than values (d_k = 16 or 32 with
+// d_v = 64, Table 3 rows (B)); sdpa_one_tile.cu takes the other shapes.
 //
 // One CTA owns two 128-row query tiles of one (batch, head) and walks the
 // key/value tiles once for both:
 //   warp 8      TMA producer: Q tiles once, then K_j and V_j into a ring of
-//               shared-memory stages (128-byte swizzle, zero fill past n).
+//               shared-memory stages (rows swizzled at their width, zero fill
+//               past n).
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
 //               then O_t += P_t V_j with P_t read from tensor memory.
 //   warps 10-11 idle (they complete the third warpgroup for the register split).
@@ -24,7 +28,7 @@
 //
 // Tensor memory (512 columns): S_0 at 0, S_1 at 128 (fp32, 128 keys each;
 // P_t overwrites the first 64 columns of S_t as packed bf16 pairs), O_0 at 256
-// and O_1 at 256 + D (fp32, D columns each).
+// and O_1 at 256 + d_v (fp32, d_v columns each).
 //
 // Running max: the softmax keeps using a stale maximum m_used until a new
 // row maximum exceeds it by more than 8 (log2 units), so exp2(x - m_used) <=
