@@ -58,7 +58,7 @@ def _check(q, k, v, do, mask, lens, r=0, scale=0.0):
     return errs
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("mask", [0, 1, 2, 3])
 def test_backward_shapes(d, mask):
     b, h, n = 2, 3, 300
@@ -156,6 +156,16 @@ def test_backward_long_causal_sampled():
     assert max(errs.values()) <= TOL_BF16
 
 
+@pytest.mark.parametrize("d", [16, 32])
+@pytest.mark.parametrize("n", [1, 65, 300])
+def test_backward_small_heads(d, n):
+    """Table 3's small heads: causal, padding and a window."""
+    q, k, v, do = _inputs(9700 + d + n, 2, 3, n, n, d)
+    _check(q, k, v, do, 1, None)
+    _check(q, k, v, do, 2, np.array([n, max(1, n // 3)], np.int32))
+    _check(q, k, v, do, 1, None, r=33)
+
+
 def test_backward_rejects_bad_arguments():
     t = __import__("torch")
     x = t.zeros((1, 1, 64, 64), dtype=t.bfloat16, device="cuda")
@@ -163,9 +173,9 @@ def test_backward_rejects_bad_arguments():
     ws = t.empty(sd.sdpa_backward_workspace_size(1, 1, 64, 64), dtype=t.uint8, device="cuda")
     with pytest.raises(sd.SdpaError, match="WORKSPACE"):
         sd.sdpa_backward(x, x, x, x, x, lse, x, x, x, ws, ws.numel() - 16, 1, 1, 64, 64, 64, 64)
-    x32 = t.zeros((1, 1, 64, 32), dtype=t.bfloat16, device="cuda")
+    x256 = t.zeros((1, 1, 64, 256), dtype=t.bfloat16, device="cuda")
     with pytest.raises(sd.SdpaError, match="UNSUPPORTED"):
-        sd.sdpa_backward(x32, x32, x32, x32, x32, lse, x32, x32, x32, ws, ws.numel(), 1, 1, 64, 64,
-                         32, 32)
+        sd.sdpa_backward(x256, x256, x256, x256, x256, lse, x256, x256, x256, ws, ws.numel(), 1, 1,
+                         64, 64, 256, 256)
     with pytest.raises(sd.SdpaError, match="INVALID_ARG"):
         sd.sdpa_backward(x, x, x, x, None, lse, x, x, x, ws, ws.numel(), 1, 1, 64, 64, 64, 64)

@@ -109,9 +109,9 @@ bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D fp32 map over the backward's dQ accumulator [bh][n_q][d]: boxes of 32
-// columns x 64 rows, unswizzled (one 128-byte row per query), for the
-// kernel's tensor reduce-adds; rows past n_q are clipped by the copy engine.
+// 3-D fp32 map over the backward's dQ accumulator [bh][n_q][d]: boxes of
+// min(32, d) columns x 64 rows, unswizzled, for the kernel's tensor
+// reduce-adds; rows past n_q are clipped by the copy engine.
 bool make_map_dq(CUtensorMap* map, const float* base, int d, int n_q, int bh) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
@@ -119,7 +119,7 @@ bool make_map_dq(CUtensorMap* map, const float* base, int d, int n_q, int bh) {
                               static_cast<cuuint64_t>(bh)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                  static_cast<cuuint64_t>(n_q > 0 ? n_q : 1) * d * 4};
-  const cuuint32_t box[3] = {32, 64, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 32 ? d : 32), 64, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -330,7 +330,8 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || r < 0)
     return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || (d_k != 64 && d_k != 128)) return SDPA_ERR_UNSUPPORTED;
+  if (d_k != d_v || (d_k != 16 && d_k != 32 && d_k != 64 && d_k != 128))
+    return SDPA_ERR_UNSUPPORTED;
   const size_t need = sdpa_backward_workspace_size(b, h, n_q, d_k);
   if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return SDPA_ERR_WORKSPACE;
   unsigned* status = nullptr;

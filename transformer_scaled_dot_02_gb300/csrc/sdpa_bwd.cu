@@ -70,35 +70,56 @@ constexpr int kMmaWarp = 9;
 constexpr int kEpilogueWarp0 = 10;       // warps 10-13: dQ^T out of tensor memory
 constexpr int kEpilogue = 128;
 constexpr int kHeadGroup = 4;            // heads whose key tiles run together
-constexpr int kKVBox = 128 * 128;        // 64 columns x 128 rows bf16
-constexpr int kQBox = 64 * 128;          // 64 columns x 64 rows bf16
 constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (128-byte rows)
 constexpr int kVecBytes = 2 * kBN * 4;   // -lse2 and -D of one step
 // kv_full, q_full[3], q_empty[3], s_full[2], p_full[2], dq_full[2],
 // dq_empty[2], acc_full, drain
 constexpr int kNumBars = 1 + 2 * kStages + 8 + 2;
 constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
-// dQ^T = K^T dS^T always with M = 128 lanes of d: for D = 64 the upper 64
-// lanes read the V tile that follows K in shared memory and are discarded.
+// dQ^T = K^T dS^T always with M = 128 lanes of d: for D < 128 the upper lanes
+// read the tiles that follow K in shared memory and are discarded.
 constexpr uint32_t kIdescQ = idesc_bf16(128, kBN, true, true);
+// dS^T rows are 128 bytes (64 queries): 128-byte swizzle, 8-row groups 1024 apart
+constexpr uint32_t kDsHi = (1024u >> 4) | (1u << 14) | (2u << 29);
 
 template <int D>
 struct Cfg {
-  static constexpr int kKVTile = (D / 64) * kKVBox;
-  static constexpr int kQTile = (D / 64) * kQBox;
+  // K, V, Q and dO move as boxes of kBoxCols columns, rows of kRowBytes
+  // swizzled at that width (128-, 64- or 32-byte swizzle for d >= 64, 32, 16).
+  static constexpr int kBoxCols = D < 64 ? D : 64;
+  static constexpr int kRowBytes = kBoxCols * 2;
+  static constexpr uint32_t kLayout = kRowBytes == 128 ? 2u : (kRowBytes == 64 ? 4u : 6u);
+  static constexpr uint32_t kSBO = 8 * kRowBytes;
+  static constexpr int kStepsPerRow = kRowBytes / 32;       // K=16 steps per swizzled row
+  static constexpr uint32_t kDescHi = (kSBO >> 4) | (1u << 14) | (kLayout << 29);
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr int kKVBox = 128 * kRowBytes;            // kBoxCols x 128 keys
+  static constexpr int kQBox = 64 * kRowBytes;              // kBoxCols x 64 queries
+  static constexpr int kKVTile = kBoxes * kKVBox;
+  static constexpr int kQTile = kBoxes * kQBox;
+  static constexpr int kDCols = D < 32 ? D : 32;            // dQ columns per epilogue warp
+  static constexpr int kHalfCols = D / 2;                   // dK / dV columns per compute warp
+  static constexpr int kKVChunk = kHalfCols < 32 ? kHalfCols : 32;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKVTile;
   static constexpr int kStageOff = 2 * kKVTile;                    // Q, dO per stage
   static constexpr int kDsOff = kStageOff + kStages * 2 * kQTile;  // two dS^T buffers
-  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // 4 warps x [64][32] fp32
-  static constexpr int kVecOff = kStagingOff + 4 * kBN * 32 * 4;
+  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // 4 warps x [64][kDCols] fp32
+  static constexpr int kVecOff = kStagingOff + 4 * kBN * kDCols * 4;
   static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);   // dV, dK (A in TMEM)
   static constexpr uint32_t kDkCol = 256 + D;
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
+  static_assert(kQBox % 1024 == 0 && kKVBox % 1024 == 0, "align");
+  // dQ^T's 128 lanes read 128 / kBoxCols boxes from K onward: all inside the CTA's memory
+  static_assert((128 / kBoxCols) * kKVBox <= kBarOff, "dQ^T reads in bounds");
 };
+
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[8]) { tmem_ld8(taddr, r); }
 
 // Adds a [64][32] fp32 box from shared memory into the tensor at (x, y, z).
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
@@ -214,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
       mbar_arrive_expect_tx(kv_full, 2 * C::kKVTile);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * kKVBox, c * 64, key0, hi, bi);
-        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * kKVBox, c * 64, key0, hi, bi);
+      for (int c = 0; c < C::kBoxes; ++c) {
+        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols, key0, hi, bi);
+        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * C::kKVBox, c * C::kBoxCols, key0, hi, bi);
       }
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -226,9 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         uint8_t* st = smem + C::kStageOff + s * 2 * C::kQTile;
         const int q0 = (i_lo + it) * kBN;
         mbar_arrive_expect_tx(q_full + s, 2 * C::kQTile + kVecBytes);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(&p.tm_q, q_full + s, st + c * kQBox, c * 64, q0, hi, bi);
-          tma_load_4d(&p.tm_do, q_full + s, st + C::kQTile + c * kQBox, c * 64, q0, hi, bi);
+        for (int c = 0; c < C::kBoxes; ++c) {
+          tma_load_4d(&p.tm_q, q_full + s, st + c * C::kQBox, c * C::kBoxCols, q0, hi, bi);
+          tma_load_4d(&p.tm_do, q_full + s, st + C::kQTile + c * C::kQBox, c * C::kBoxCols, q0, hi,
+                      bi);
         }
         const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
         uint8_t* vec = smem + C::kVecOff + s * kVecBytes;
@@ -247,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       // Shared-memory descriptors as 32-bit halves: every operand here is
       // 128-byte swizzled with 8-row groups 1024 bytes apart, so the high
       // half is one constant and a k step only adds to the start address.
-      constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+      constexpr uint32_t kDescHi = C::kDescHi;
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       // S^T(it) = K_j Q_i^T and dP^T(it) = V_j dO_i^T into buffer it & 1
       auto issue_s = [&](int it, bool dp) {
@@ -257,9 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          mma_bf16_ss_lohi(d, a0 + static_cast<uint32_t>(((k >> 2) * kKVBox + (k & 3) * 32) >> 4),
+          constexpr int kS = C::kStepsPerRow;
+          mma_bf16_ss_lohi(d, a0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4),
                            kDescHi,
-                           b0 + static_cast<uint32_t>(((k >> 2) * kQBox + (k & 3) * 32) >> 4),
+                           b0 + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
                            kDescHi, kIdescS, k > 0 ? 1u : 0u);
         }
       };
@@ -294,11 +317,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
         // dV += P^T dO_i, dK += dS^T Q_i: 16 queries per step; queries
         // [32h, 32h+32) sit in columns 32h .. 32h+16 of the S^T / dP^T halves
-        const uint32_t bdo = lo(st + C::kQTile, kQBox), bq = lo(st, kQBox);
+        const uint32_t bdo = lo(st + C::kQTile, C::kQBox), bq = lo(st, C::kQBox);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128) >> 4;
+          const uint32_t roff = static_cast<uint32_t>(k * 16 * C::kRowBytes) >> 4;
           mma_bf16_ts_lohi(tmem + 256, buf + col, bdo + roff, kDescHi, C::kIdescKV,
                            (it > 0 || k > 0) ? 1u : 0u);
           mma_bf16_ts_lohi(tmem + C::kDkCol, buf + 64 + col, bq + roff, kDescHi, C::kIdescKV,
@@ -306,11 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         }
         mma_commit(q_empty + it % kStages);
         // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
-        const uint32_t ak = lo(k_smem, kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
+        const uint32_t ak = lo(k_smem, C::kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
 #pragma unroll
         for (int k = 0; k < kBM / 16; ++k) {
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * 128) >> 4;
-          mma_bf16_ss_lohi(buf + 64, ak + roff, kDescHi, bds + roff, kDescHi, kIdescQ,
+          const uint32_t ka = static_cast<uint32_t>(k * 16 * C::kRowBytes) >> 4;   // 16 key rows of K
+          const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;            // of dS^T
+          mma_bf16_ss_lohi(buf + 64, ak + ka, kDescHi, bds + kb, kDsHi, kIdescQ,
                            k > 0 ? 1u : 0u);
         }
         mma_commit(dq_full + b);
@@ -327,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     // reduce; rows past n_q are clipped by the copy engine.
     const int quarter = warp & 3;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff) + quarter * (kBN * 32);
-    const bool active = D == 128 || quarter * 32 < D;   // d = 64: lanes 64..127 are not d
+    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff) + quarter * (kBN * C::kDCols);
+    const bool active = quarter * 32 < D;   // lanes 32 q .. are d values only below D
     for (int j = 0; j < n_it; ++j) {
       const int b = j & 1;
       if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
@@ -345,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       // this warp's previous reduce has finished reading the staging tile
       if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       __syncwarp();
+      if (lane < C::kDCols) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        staging[e * 32 + lane] = __uint_as_float(g0[e]);
-        staging[(32 + e) * 32 + lane] = __uint_as_float(g1[e]);
+        for (int e = 0; e < 32; ++e) {
+          staging[e * C::kDCols + lane] = __uint_as_float(g0[e]);
+          staging[(32 + e) * C::kDCols + lane] = __uint_as_float(g1[e]);
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -447,23 +473,24 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tc_fence_after();
       }
       if (have || n_it == 0) {
-        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D + half * (D / 2);
-        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D + half * (D / 2);
+        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D + half * C::kHalfCols;
+        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D + half * C::kHalfCols;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t a[32], g[32];
+        for (int c = 0; c < C::kHalfCols / C::kKVChunk; ++c) {
+          constexpr int N = C::kKVChunk;
+          uint32_t a[N], g[N];
           if (have) {
-            tmem_ld32(lane_base + 256 + half * (D / 2) + c * 32, a);
-            tmem_ld32(lane_base + C::kDkCol + half * (D / 2) + c * 32, g);
+            tmem_ld_n(lane_base + 256 + half * C::kHalfCols + c * N, a);
+            tmem_ld_n(lane_base + C::kDkCol + half * C::kHalfCols + c * N, g);
             tmem_ld_wait();
             reg_fence(a);
             reg_fence(g);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+            for (int e = 0; e < N; ++e) a[e] = g[e] = 0u;
           }
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q4 = 0; q4 < N / 8; ++q4) {
             uint4 v, w;
             v.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]), __uint_as_float(a[q4 * 8 + 1]));
             v.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]), __uint_as_float(a[q4 * 8 + 3]));
@@ -478,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
             w.w = pack_bf16x2(__uint_as_float(g[q4 * 8 + 6]) * p.scale,
                               __uint_as_float(g[q4 * 8 + 7]) * p.scale);
             if (key < p.n_k) {
-              *reinterpret_cast<uint4*>(dv_row + c * 32 + q4 * 8) = v;
-              *reinterpret_cast<uint4*>(dk_row + c * 32 + q4 * 8) = w;
+              *reinterpret_cast<uint4*>(dv_row + c * N + q4 * 8) = v;
+              *reinterpret_cast<uint4*>(dk_row + c * N + q4 * 8) = w;
             }
           }
         }
@@ -585,6 +612,8 @@ cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cud
 
 cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
                             cudaStream_t stream) {
+  if (head_dim == 16) return launch_n64<16>(bp, pp, stream);
+  if (head_dim == 32) return launch_n64<32>(bp, pp, stream);
   if (head_dim == 64) return launch_n64<64>(bp, pp, stream);
   if (head_dim == 128) return launch_n64<128>(bp, pp, stream);
   return cudaErrorInvalidValue;
