@@ -117,7 +117,8 @@ sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* 
  * P is recomputed from lse, never stored; the products run on the tensor
  * cores with bf16 operands (P and dS rounded to bf16) and fp32 accumulation;
  * dQ is accumulated in fp32 across key tiles, then rounded.  Hidden keys get
- * zero gradient.  Supported: d_k == d_v in {16, 32, 64, 128}.
+ * zero gradient.  Supported: d_k == d_v in {16, 32, 64, 128}, and
+ * (d_k, d_v) in {(16, 64), (32, 64)} (Table 3, rows (B)).
  */
 size_t sdpa_backward_workspace_size(int b, int h, int n_q, int d);
 

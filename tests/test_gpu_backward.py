@@ -166,6 +166,29 @@ def test_backward_small_heads(d, n):
     _check(q, k, v, do, 1, None, r=33)
 
 
+@pytest.mark.parametrize("d_k", [16, 32])
+@pytest.mark.parametrize("mask,n_q,n_k,r", [(0, 70, 200, 0), (1, 300, 300, 0), (2, 129, 257, 0),
+                                            (3, 300, 300, 0), (1, 260, 260, 65)])
+def test_backward_row_b_heads(d_k, mask, n_q, n_k, r):
+    """Table 3, rows (B): keys of 16 or 32 against values of 64; dq and dk
+    have d_k columns, dv has d_v."""
+    rng = np.random.default_rng(9800 + d_k + 7 * mask + r)
+    b, h, d_v = 2, 3, 64
+    q, k = _rand(rng, (b, h, n_q, d_k)), _rand(rng, (b, h, n_k, d_k))
+    v, do = _rand(rng, (b, h, n_k, d_v)), _rand(rng, (b, h, n_q, d_v))
+    lens = np.array([n_k, max(1, n_k // 3)], np.int32) if mask & 2 else None
+    errs = _check(q, k, v, do, mask, lens, r)
+    assert set(errs) == {"dq", "dk", "dv"}
+
+
+def test_backward_row_b_unscaled():
+    """Scale 1 (the unscaled dot product of the paper's comparison) at d_k = 16, d_v = 64."""
+    rng = np.random.default_rng(9850)
+    q, k = _rand(rng, (1, 2, 200, 16), 0.3), _rand(rng, (1, 2, 200, 16))
+    v, do = _rand(rng, (1, 2, 200, 64)), _rand(rng, (1, 2, 200, 64))
+    _check(q, k, v, do, 1, None, scale=1.0)
+
+
 def test_backward_rejects_bad_arguments():
     t = __import__("torch")
     x = t.zeros((1, 1, 64, 64), dtype=t.bfloat16, device="cuda")
@@ -179,3 +202,7 @@ def test_backward_rejects_bad_arguments():
                          64, 64, 256, 256)
     with pytest.raises(sd.SdpaError, match="INVALID_ARG"):
         sd.sdpa_backward(x, x, x, x, None, lse, x, x, x, ws, ws.numel(), 1, 1, 64, 64, 64, 64)
+    # unequal head sizes other than Table 3's rows (B)
+    x32 = t.zeros((1, 1, 64, 32), dtype=t.bfloat16, device="cuda")
+    with pytest.raises(sd.SdpaError, match="UNSUPPORTED"):
+        sd.sdpa_backward(x, x, x32, x32, x32, lse, x, x, x32, ws, ws.numel(), 1, 1, 64, 64, 64, 32)

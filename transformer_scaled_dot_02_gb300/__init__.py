@@ -283,7 +283,7 @@ def attention_backward(q, k, v, out, lse, dout, mask_kind=SDPA_MASK_NONE, kv_len
     calls sdpa_backward; returns (dq, dk, dv)."""
     import torch
     b, h, n_q, d = q.shape
-    n_k = k.shape[2]
+    n_k, d_v = k.shape[2], v.shape[3]
     need = sdpa_backward_workspace_size(b, h, n_q, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -291,7 +291,7 @@ def attention_backward(q, k, v, out, lse, dout, mask_kind=SDPA_MASK_NONE, kv_len
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     sdpa_backward(q, k, v, out, dout, lse, dq, dk, dv, workspace,
-                  workspace.numel() * workspace.element_size(), b, h, n_q, n_k, d, d, mask_kind,
+                  workspace.numel() * workspace.element_size(), b, h, n_q, n_k, d, d_v, mask_kind,
                   kv_lengths, r, scale, stream)
     return dq, dk, dv
 

@@ -174,6 +174,13 @@ bool tc_head_sizes(int d_k, int d_v) {
   return d_v == 64 && (d_k == 16 || d_k == 32);
 }
 
+// Head shapes the backward supports: equal sizes up to 128 and Table 3's
+// rows (B), where the keys are smaller than the values.
+bool bwd_head_sizes(int d_k, int d_v) {
+  if (d_k == d_v) return d_k == 16 || d_k == 32 || d_k == 64 || d_k == 128;
+  return d_v == 64 && (d_k == 16 || d_k == 32);
+}
+
 float effective_scale(float scale, int d_k) {
   return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
 }
@@ -330,15 +337,13 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || r < 0)
     return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || (d_k != 16 && d_k != 32 && d_k != 64 && d_k != 128))
-    return SDPA_ERR_UNSUPPORTED;
+  if (!bwd_head_sizes(d_k, d_v)) return SDPA_ERR_UNSUPPORTED;
   const size_t need = sdpa_backward_workspace_size(b, h, n_q, d_k);
   if (workspace == nullptr || !aligned16(workspace) || ws_bytes < need) return SDPA_ERR_WORKSPACE;
   unsigned* status = nullptr;
   st = current_device(&status);
   if (st != SDPA_OK) return st;
   if (n_q == 0 && n_k == 0) return SDPA_OK;
-  const int d = d_k;
   const int n_q_pad = (n_q + 127) / 128 * 128;
   const size_t rows_pad = static_cast<size_t>(b) * h * n_q_pad;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -346,15 +351,15 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   float* neg_dvec = reinterpret_cast<float*>(ws + round256(rows_pad * 4));
   float* dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows_pad * 4));
   sdpa::SdpaBwdParams bp;
-  const long long dd = d;
+  const long long dk_ = d_k, dv_ = d_v;
   // the backward steps through the queries 64 at a time
   const int q_rows = 64;
-  if (!make_map_4d(&bp.tm_q, q, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd, q_rows) ||
-      !make_map_4d(&bp.tm_k, k, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
-      !make_map_4d(&bp.tm_v, v, d, n_k, h, b, dd, 1ll * n_k * dd, 1ll * h * n_k * dd) ||
-      !make_map_4d(&bp.tm_do, dout, d, n_q, h, b, dd, 1ll * n_q * dd, 1ll * h * n_q * dd, q_rows))
+  if (!make_map_4d(&bp.tm_q, q, d_k, n_q, h, b, dk_, n_q * dk_, h * n_q * dk_, q_rows) ||
+      !make_map_4d(&bp.tm_k, k, d_k, n_k, h, b, dk_, n_k * dk_, h * n_k * dk_) ||
+      !make_map_4d(&bp.tm_v, v, d_v, n_k, h, b, dv_, n_k * dv_, h * n_k * dv_) ||
+      !make_map_4d(&bp.tm_do, dout, d_v, n_q, h, b, dv_, n_q * dv_, h * n_q * dv_, q_rows))
     return SDPA_ERR_CUDA;
-  if (!make_map_dq(&bp.tm_dq, dq_acc, d, n_q, b * h)) return SDPA_ERR_CUDA;
+  if (!make_map_dq(&bp.tm_dq, dq_acc, d_k, n_q, b * h)) return SDPA_ERR_CUDA;
   bp.neg_lse2 = neg_lse2;
   bp.neg_dvec = neg_dvec;
   bp.dq_acc = dq_acc;
@@ -369,7 +374,7 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   bp.n_q_pad = n_q_pad;
   bp.mask_kind = mask_kind;
   bp.num_kv_tiles = (n_k + 127) / 128;
-  const float sc = effective_scale(scale, d);
+  const float sc = effective_scale(scale, d_k);
   bp.scale_log2 = sc * 1.4426950408889634f;
   bp.scale = sc;
   bp.win_left = r > 0 ? (r - 1) / 2 : sdpa::kWindowUnbounded;
@@ -387,7 +392,7 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   pp.n_q = n_q;
   pp.n_q_pad = n_q_pad;
   pp.scale = sc;
-  return sdpa::launch_sdpa_bwd(bp, pp, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return sdpa::launch_sdpa_bwd(bp, pp, d_k, d_v, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SDPA_OK
              : SDPA_ERR_CUDA;
 }

@@ -55,12 +55,12 @@ cudaError_t launch_sdpa_decode(const DecodeParams& p, int head_dim, cudaStream_t
 
 // Gradients of attention (bf16 BHSD tensors, fp32 accumulation).
 struct SdpaBwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 4-D (d, n, h, b) bf16 maps
-  CUtensorMap tm_dq;          // 3-D (d, n_q, b*h) fp32 map of dq_acc, 32 x 64 boxes
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 4-D (d, n, h, b) bf16 maps; d = d_k for Q, K
+  CUtensorMap tm_dq;          // 3-D (d_k, n_q, b*h) fp32 map of dq_acc, 32 x 64 boxes
   const float* neg_lse2;      // [b*h][n_q_pad] -lse_i log2(e) (-inf past n_q)
   const float* neg_dvec;      // [b*h][n_q_pad] -D_i = -dO_i . O_i
-  float* dq_acc;              // [b*h][n_q][d] fp32 accumulator (zeroed by the prep kernel)
-  uint16_t *dk, *dv;          // [b*h][n_k][d] bf16 outputs
+  float* dq_acc;              // [b*h][n_q][d_k] fp32 accumulator (zeroed by the prep kernel)
+  uint16_t *dk, *dv;          // [b*h][n_k][d_k], [b*h][n_k][d_v] bf16 outputs
   const int32_t* kv_lengths;
   unsigned* status;
   int b, h, n_q, n_k, n_q_pad, mask_kind, num_kv_tiles;
@@ -68,14 +68,14 @@ struct SdpaBwdParams {
   int win_left, win_right;
 };
 struct SdpaBwdPrepParams {
-  const uint16_t *out, *dout;  // forward output and its gradient, [b*h][n_q][d]
+  const uint16_t *out, *dout;  // forward output and its gradient, [b*h][n_q][d_v]
   const float* lse;            // [b*h][n_q] natural log-sum-exp
   float *neg_lse2, *neg_dvec, *dq_acc;
-  uint16_t* dq;                // [b*h][n_q][d] bf16 output
+  uint16_t* dq;                // [b*h][n_q][d_k] bf16 output
   int b, h, n_q, n_q_pad;
   float scale;
 };
-cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
+cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int d_k, int d_v,
                             cudaStream_t stream);
 
 // Exact fp32 attention on the CUDA cores, BHSD contiguous.

@@ -10,7 +10,8 @@
 //                        log2 units for every query row (padded to whole
 //                        128-row tiles with 0 and -inf, so padded rows get
 //                        P = 0); zeroes the fp32 dQ accumulator.
-//   sdpa_bwd_tc_n64<D>   one CTA per (128-key tile, batch, head), walking in
+//   sdpa_bwd_tc_n64<DK, DV>
+//                        one CTA per (128-key tile, batch, head), walking in
 //                        steps of 64 the queries that can see its keys; dK
 //                        and dV accumulate in tensor memory, dQ leaves each
 //                        step as a bulk reduce-add into the accumulator.
@@ -56,7 +57,7 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 // Tensor memory: buffer b = step & 1 holds S^T at 128 b (64 columns; P^T in
 // bf16 over columns 128 b + 32 h .. +16 of each half h) and dP^T at
 // 128 b + 64 (dS^T in bf16 the same way; then dQ^T = K^T dS^T, keyed by d),
-// dV at 256, dK at 256 + D.  dQ^T leaves through a 64 x D fp32 staging tile
+// dV at 256, dK at 256 + d_v.  dQ^T leaves through a 64 x d_k fp32 staging tile
 // and one bulk reduce-add into the fp32 dQ accumulator per step.
 namespace n64 {
 
@@ -76,16 +77,17 @@ constexpr int kVecBytes = 2 * kBN * 4;   // -lse2 and -D of one step
 // dq_empty[2], acc_full, drain
 constexpr int kNumBars = 1 + 2 * kStages + 8 + 2;
 constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
-// dQ^T = K^T dS^T always with M = 128 lanes of d: for D < 128 the upper lanes
+// dQ^T = K^T dS^T always with M = 128 lanes of d: for d_k < 128 the upper lanes
 // read the tiles that follow K in shared memory and are discarded.
 constexpr uint32_t kIdescQ = idesc_bf16(128, kBN, true, true);
 // dS^T rows are 128 bytes (64 queries): 128-byte swizzle, 8-row groups 1024 apart
 constexpr uint32_t kDsHi = (1024u >> 4) | (1u << 14) | (2u << 29);
 
+// Layout of an operand whose rows hold D bf16 values (K and Q at d_k; V and
+// dO at d_v): boxes of kBoxCols columns, rows of kRowBytes swizzled at that
+// width (128-, 64- or 32-byte swizzle for d >= 64, 32, 16).
 template <int D>
-struct Cfg {
-  // K, V, Q and dO move as boxes of kBoxCols columns, rows of kRowBytes
-  // swizzled at that width (128-, 64- or 32-byte swizzle for d >= 64, 32, 16).
+struct Lay {
   static constexpr int kBoxCols = D < 64 ? D : 64;
   static constexpr int kRowBytes = kBoxCols * 2;
   static constexpr uint32_t kLayout = kRowBytes == 128 ? 2u : (kRowBytes == 64 ? 4u : 6u);
@@ -97,24 +99,36 @@ struct Cfg {
   static constexpr int kQBox = 64 * kRowBytes;              // kBoxCols x 64 queries
   static constexpr int kKVTile = kBoxes * kKVBox;
   static constexpr int kQTile = kBoxes * kQBox;
-  static constexpr int kDCols = D < 32 ? D : 32;            // dQ columns per epilogue warp
   static constexpr int kHalfCols = D / 2;                   // dK / dV columns per compute warp
-  static constexpr int kKVChunk = kHalfCols < 32 ? kHalfCols : 32;
+  static constexpr int kChunk = kHalfCols < 32 ? kHalfCols : 32;
+  static_assert(kQBox % 1024 == 0 && kKVBox % 1024 == 0, "align");
+};
+
+// Shared memory and tensor memory of one CTA for key size DK and value
+// size DV.  Tensor memory: the two score buffers (256 columns), dV at 256
+// (DV columns), dK at 256 + DV (DK columns).
+template <int DK, int DV>
+struct Cfg {
+  using LK = Lay<DK>;
+  using LV = Lay<DV>;
+  static constexpr int kDCols = DK < 32 ? DK : 32;          // dQ columns per epilogue warp
   static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKVTile;
-  static constexpr int kStageOff = 2 * kKVTile;                    // Q, dO per stage
-  static constexpr int kDsOff = kStageOff + kStages * 2 * kQTile;  // two dS^T buffers
-  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;         // 4 warps x [64][kDCols] fp32
+  static constexpr int kVOff = LK::kKVTile;
+  static constexpr int kStageOff = kVOff + LV::kKVTile;     // Q then dO, per stage
+  static constexpr int kStageBytes = LK::kQTile + LV::kQTile;
+  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;   // two dS^T buffers
+  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;  // 4 warps x [64][kDCols] fp32
   static constexpr int kVecOff = kStagingOff + 4 * kBN * kDCols * 4;
   static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kIdescKV = idesc_bf16(kBM, D, false, true);   // dV, dK (A in TMEM)
-  static constexpr uint32_t kDkCol = 256 + D;
+  static constexpr uint32_t kIdescDV = idesc_bf16(kBM, DV, false, true);  // dV (A in TMEM)
+  static constexpr uint32_t kIdescDK = idesc_bf16(kBM, DK, false, true);  // dK (A in TMEM)
+  static constexpr uint32_t kDkCol = 256 + DV;
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
-  static_assert(kQBox % 1024 == 0 && kKVBox % 1024 == 0, "align");
+  static_assert(kDkCol + DK <= 512, "tensor memory");
   // dQ^T's 128 lanes read 128 / kBoxCols boxes from K onward: all inside the CTA's memory
-  static_assert((128 / kBoxCols) * kKVBox <= kBarOff, "dQ^T reads in bounds");
+  static_assert((128 / LK::kBoxCols) * LK::kKVBox <= kBarOff, "dQ^T reads in bounds");
 };
 
 __device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
@@ -154,9 +168,11 @@ __device__ __forceinline__ int2 query_steps(const SdpaBwdParams& p, int key0, in
   return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
 }
 
-template <int D>
+template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_constant__ SdpaBwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<DK, DV>;
+  using LK = typename C::LK;
+  using LV = typename C::LV;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
@@ -234,24 +250,24 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kKVTile);
-      for (int c = 0; c < C::kBoxes; ++c) {
-        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols, key0, hi, bi);
-        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * C::kKVBox, c * C::kBoxCols, key0, hi, bi);
-      }
+      mbar_arrive_expect_tx(kv_full, LK::kKVTile + LV::kKVTile);
+      for (int c = 0; c < LK::kBoxes; ++c)
+        tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * LK::kKVBox, c * LK::kBoxCols, key0, hi, bi);
+      for (int c = 0; c < LV::kBoxes; ++c)
+        tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * LV::kKVBox, c * LV::kBoxCols, key0, hi, bi);
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t use = static_cast<uint32_t>(it / kStages);
         if (it >= kStages && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
-        uint8_t* st = smem + C::kStageOff + s * 2 * C::kQTile;
+        uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
         const int q0 = (i_lo + it) * kBN;
-        mbar_arrive_expect_tx(q_full + s, 2 * C::kQTile + kVecBytes);
-        for (int c = 0; c < C::kBoxes; ++c) {
-          tma_load_4d(&p.tm_q, q_full + s, st + c * C::kQBox, c * C::kBoxCols, q0, hi, bi);
-          tma_load_4d(&p.tm_do, q_full + s, st + C::kQTile + c * C::kQBox, c * C::kBoxCols, q0, hi,
-                      bi);
-        }
+        mbar_arrive_expect_tx(q_full + s, C::kStageBytes + kVecBytes);
+        for (int c = 0; c < LK::kBoxes; ++c)
+          tma_load_4d(&p.tm_q, q_full + s, st + c * LK::kQBox, c * LK::kBoxCols, q0, hi, bi);
+        for (int c = 0; c < LV::kBoxes; ++c)
+          tma_load_4d(&p.tm_do, q_full + s, st + LK::kQTile + c * LV::kQBox, c * LV::kBoxCols, q0,
+                      hi, bi);
         const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
         uint8_t* vec = smem + C::kVecOff + s * kVecBytes;
         tma_load_1d(vec, p.neg_lse2 + vrow, kBN * 4, q_full + s);
@@ -269,22 +285,27 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       // Shared-memory descriptors as 32-bit halves: every operand here is
       // 128-byte swizzled with 8-row groups 1024 bytes apart, so the high
       // half is one constant and a k step only adds to the start address.
-      constexpr uint32_t kDescHi = C::kDescHi;
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
-      // S^T(it) = K_j Q_i^T and dP^T(it) = V_j dO_i^T into buffer it & 1
+      // S^T(it) = K_j Q_i^T (dp false) or dP^T(it) = V_j dO_i^T (dp true) into buffer it & 1
       auto issue_s = [&](int it, bool dp) {
-        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * 2 * C::kQTile + (dp ? C::kQTile : 0);
-        const uint32_t a0 = lo(dp ? v_smem : k_smem, 16);
-        const uint32_t b0 = lo(st, 16);
+        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * C::kStageBytes;
         const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
+        auto product = [&](auto lay, uint32_t a_addr, uint32_t b_addr, int dsize) {
+          using L = decltype(lay);
+          const uint32_t a0 = lo(a_addr, 16), b0 = lo(b_addr, 16);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          constexpr int kS = C::kStepsPerRow;
-          mma_bf16_ss_lohi(d, a0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4),
-                           kDescHi,
-                           b0 + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
-                           kDescHi, kIdescS, k > 0 ? 1u : 0u);
-        }
+          for (int k = 0; k < dsize / 16; ++k) {
+            constexpr int kS = L::kStepsPerRow;
+            mma_bf16_ss_lohi(d, a0 + static_cast<uint32_t>(((k / kS) * L::kKVBox + (k % kS) * 32) >> 4),
+                             L::kDescHi,
+                             b0 + static_cast<uint32_t>(((k / kS) * L::kQBox + (k % kS) * 32) >> 4),
+                             L::kDescHi, kIdescS, k > 0 ? 1u : 0u);
+          }
+        };
+        if (dp)
+          product(LV{}, v_smem, st + LK::kQTile, DV);
+        else
+          product(LK{}, k_smem, st, DK);
       };
       bool ok = mbar_wait(kv_full, 0, ab) && mbar_wait(q_full, 0, ab);
       tc_fence_after();
@@ -313,28 +334,29 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         ok = mbar_wait(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * 2 * C::kQTile;
+        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * C::kStageBytes;
         const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
         // dV += P^T dO_i, dK += dS^T Q_i: 16 queries per step; queries
         // [32h, 32h+32) sit in columns 32h .. 32h+16 of the S^T / dP^T halves
-        const uint32_t bdo = lo(st + C::kQTile, C::kQBox), bq = lo(st, C::kQBox);
+        const uint32_t bdo = lo(st + LK::kQTile, LV::kQBox), bq = lo(st, LK::kQBox);
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
-          const uint32_t roff = static_cast<uint32_t>(k * 16 * C::kRowBytes) >> 4;
-          mma_bf16_ts_lohi(tmem + 256, buf + col, bdo + roff, kDescHi, C::kIdescKV,
-                           (it > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ts_lohi(tmem + C::kDkCol, buf + 64 + col, bq + roff, kDescHi, C::kIdescKV,
-                           (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts_lohi(tmem + 256, buf + col,
+                           bdo + (static_cast<uint32_t>(k * 16 * LV::kRowBytes) >> 4), LV::kDescHi,
+                           C::kIdescDV, (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts_lohi(tmem + C::kDkCol, buf + 64 + col,
+                           bq + (static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4), LK::kDescHi,
+                           C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(q_empty + it % kStages);
         // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
-        const uint32_t ak = lo(k_smem, C::kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
+        const uint32_t ak = lo(k_smem, LK::kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
 #pragma unroll
         for (int k = 0; k < kBM / 16; ++k) {
-          const uint32_t ka = static_cast<uint32_t>(k * 16 * C::kRowBytes) >> 4;   // 16 key rows of K
+          const uint32_t ka = static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4;  // 16 key rows of K
           const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;            // of dS^T
-          mma_bf16_ss_lohi(buf + 64, ak + ka, kDescHi, bds + kb, kDsHi, kIdescQ,
+          mma_bf16_ss_lohi(buf + 64, ak + ka, LK::kDescHi, bds + kb, kDsHi, kIdescQ,
                            k > 0 ? 1u : 0u);
         }
         mma_commit(dq_full + b);
@@ -352,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     const int quarter = warp & 3;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     float* staging = reinterpret_cast<float*>(smem + C::kStagingOff) + quarter * (kBN * C::kDCols);
-    const bool active = quarter * 32 < D;   // lanes 32 q .. are d values only below D
+    const bool active = quarter * 32 < DK;   // lanes 32 q .. are d values only below d_k
     for (int j = 0; j < n_it; ++j) {
       const int b = j & 1;
       if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
@@ -465,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       tc_fence_before();
       mbar_arrive(p_full + b);
     }
-    // ---- dK (scaled) and dV rows: warp half h takes columns [h D/2, (h+1) D/2)
+    // ---- dK (scaled) and dV rows: warp half h takes the half h of each tensor's columns
     if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
       bool have = ok && n_it > 0;
       if (have) {
@@ -473,43 +495,36 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tc_fence_after();
       }
       if (have || n_it == 0) {
-        uint16_t* dv_row = p.dv + (static_cast<long long>(bh) * p.n_k + key) * D + half * C::kHalfCols;
-        uint16_t* dk_row = p.dk + (static_cast<long long>(bh) * p.n_k + key) * D + half * C::kHalfCols;
+        // one tensor of `cols` columns per row: TMEM at `tcol`, bf16 to `row`, times `mul`
+        auto write_rows = [&](auto lay, uint32_t tcol, uint16_t* row, float mul) {
+          using L = decltype(lay);
+          constexpr int N = L::kChunk;
 #pragma unroll
-        for (int c = 0; c < C::kHalfCols / C::kKVChunk; ++c) {
-          constexpr int N = C::kKVChunk;
-          uint32_t a[N], g[N];
-          if (have) {
-            tmem_ld_n(lane_base + 256 + half * C::kHalfCols + c * N, a);
-            tmem_ld_n(lane_base + C::kDkCol + half * C::kHalfCols + c * N, g);
-            tmem_ld_wait();
-            reg_fence(a);
-            reg_fence(g);
-          } else {
+          for (int c = 0; c < L::kHalfCols / N; ++c) {
+            uint32_t a[N];
+            if (have) {
+              tmem_ld_n(lane_base + tcol + half * L::kHalfCols + c * N, a);
+              tmem_ld_wait();
+              reg_fence(a);
+            } else {
 #pragma unroll
-            for (int e = 0; e < N; ++e) a[e] = g[e] = 0u;
-          }
+              for (int e = 0; e < N; ++e) a[e] = 0u;
+            }
 #pragma unroll
-          for (int q4 = 0; q4 < N / 8; ++q4) {
-            uint4 v, w;
-            v.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]), __uint_as_float(a[q4 * 8 + 1]));
-            v.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]), __uint_as_float(a[q4 * 8 + 3]));
-            v.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]), __uint_as_float(a[q4 * 8 + 5]));
-            v.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]), __uint_as_float(a[q4 * 8 + 7]));
-            w.x = pack_bf16x2(__uint_as_float(g[q4 * 8 + 0]) * p.scale,
-                              __uint_as_float(g[q4 * 8 + 1]) * p.scale);
-            w.y = pack_bf16x2(__uint_as_float(g[q4 * 8 + 2]) * p.scale,
-                              __uint_as_float(g[q4 * 8 + 3]) * p.scale);
-            w.z = pack_bf16x2(__uint_as_float(g[q4 * 8 + 4]) * p.scale,
-                              __uint_as_float(g[q4 * 8 + 5]) * p.scale);
-            w.w = pack_bf16x2(__uint_as_float(g[q4 * 8 + 6]) * p.scale,
-                              __uint_as_float(g[q4 * 8 + 7]) * p.scale);
-            if (key < p.n_k) {
-              *reinterpret_cast<uint4*>(dv_row + c * N + q4 * 8) = v;
-              *reinterpret_cast<uint4*>(dk_row + c * N + q4 * 8) = w;
+            for (int q4 = 0; q4 < N / 8; ++q4) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(a[q4 * 8 + 0]) * mul, __uint_as_float(a[q4 * 8 + 1]) * mul);
+              v.y = pack_bf16x2(__uint_as_float(a[q4 * 8 + 2]) * mul, __uint_as_float(a[q4 * 8 + 3]) * mul);
+              v.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * mul, __uint_as_float(a[q4 * 8 + 5]) * mul);
+              v.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * mul, __uint_as_float(a[q4 * 8 + 7]) * mul);
+              if (key < p.n_k)
+                *reinterpret_cast<uint4*>(row + half * L::kHalfCols + c * N + q4 * 8) = v;
             }
           }
-        }
+        };
+        const long long krow = static_cast<long long>(bh) * p.n_k + key;
+        write_rows(LV{}, 256u, p.dv + krow * DV, 1.f);
+        write_rows(LK{}, C::kDkCol, p.dk + krow * DK, p.scale);
       }
     }
   }
@@ -525,11 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 }  // namespace n64
 
 // -D_i = -dO_i . O_i and -lse_i log2(e) (padded rows: 0 and -inf), dQ accumulator = 0.
-// D / 8 lanes per row, 16 bytes of O and dO per lane.
-template <int D>
+// DV / 8 lanes per row, 16 bytes of O and dO per lane; each lane also zeroes
+// DK / (DV / 8) of the row's fp32 dQ accumulator.
+template <int DK, int DV>
 __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
-  constexpr int kLanes = D / 8;
+  constexpr int kLanes = DV / 8;
   constexpr int kRowsPerBlock = 256 / kLanes;
+  constexpr int kZero = DK / kLanes;   // 2, 4 or 8 accumulator floats per lane
   const int sub = threadIdx.x % kLanes;
   const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanes;
   const long long rows = static_cast<long long>(p.b) * p.h * p.n_q_pad;
@@ -544,7 +561,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
     }
     return;
   }
-  const long long src = (bh * p.n_q + i) * D + sub * 8;
+  const long long src = (bh * p.n_q + i) * DV + sub * 8;
   const uint4 o = *reinterpret_cast<const uint4*>(p.out + src);
   const uint4 g = *reinterpret_cast<const uint4*>(p.dout + src);
   const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
@@ -554,9 +571,9 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
     acc = fmaf(__uint_as_float(ow[w] << 16), __uint_as_float(gw[w] << 16), acc);
     acc = fmaf(__uint_as_float(ow[w] & 0xffff0000u), __uint_as_float(gw[w] & 0xffff0000u), acc);
   }
-  float4* z = reinterpret_cast<float4*>(p.dq_acc + src);
-  z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-  z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float* z = p.dq_acc + (bh * p.n_q + i) * DK + sub * kZero;
+#pragma unroll
+  for (int e = 0; e < kZero; e += 2) *reinterpret_cast<float2*>(z + e) = make_float2(0.f, 0.f);
 #pragma unroll
   for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(group, acc, off);
   if (sub == 0) {
@@ -581,41 +598,46 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const SdpaBwdPrepPara
   *reinterpret_cast<uint4*>(p.dq + idx) = r;
 }
 
-template <int D>
+template <int DK, int DV>
 cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
   const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
   cudaError_t err = cudaSuccess;
   if (rows > 0) {
-    constexpr long long kRowsPerBlock = 256 / (D / 8);
-    sdpa_bwd_prep<D><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0,
-                       stream>>>(pp);
+    constexpr long long kRowsPerBlock = 256 / (DV / 8);
+    sdpa_bwd_prep<DK, DV><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256,
+                            0, stream>>>(pp);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  const int smem = n64::Cfg<D>::kSmemBytes;
-  err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
+  const int smem = n64::Cfg<DK, DV>::kSmemBytes;
+  err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64<DK, DV>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
   if (blocks > 0) {
-    n64::sdpa_bwd_tc_n64<D><<<static_cast<unsigned>(blocks), n64::kThreads, smem, stream>>>(bp);
+    n64::sdpa_bwd_tc_n64<DK, DV><<<static_cast<unsigned>(blocks), n64::kThreads, smem, stream>>>(bp);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
-  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * D;
+  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * DK;
   if (n > 0)
-    sdpa_bwd_dq_convert<D><<<static_cast<unsigned>((n / 8 + 255) / 256), 256, 0, stream>>>(pp);
+    sdpa_bwd_dq_convert<DK><<<static_cast<unsigned>((n / 8 + 255) / 256), 256, 0, stream>>>(pp);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int head_dim,
+cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int d_k, int d_v,
                             cudaStream_t stream) {
-  if (head_dim == 16) return launch_n64<16>(bp, pp, stream);
-  if (head_dim == 32) return launch_n64<32>(bp, pp, stream);
-  if (head_dim == 64) return launch_n64<64>(bp, pp, stream);
-  if (head_dim == 128) return launch_n64<128>(bp, pp, stream);
+  if (d_k == d_v) {
+    if (d_k == 16) return launch_n64<16, 16>(bp, pp, stream);
+    if (d_k == 32) return launch_n64<32, 32>(bp, pp, stream);
+    if (d_k == 64) return launch_n64<64, 64>(bp, pp, stream);
+    if (d_k == 128) return launch_n64<128, 128>(bp, pp, stream);
+  }
+  // Table 3, rows (B): smaller keys than values
+  if (d_k == 16 && d_v == 64) return launch_n64<16, 64>(bp, pp, stream);
+  if (d_k == 32 && d_v == 64) return launch_n64<32, 64>(bp, pp, stream);
   return cudaErrorInvalidValue;
 }
 

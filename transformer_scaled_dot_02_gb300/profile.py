@@ -8,9 +8,11 @@ C ABI, for profiling a single kernel launch under a profiler.
     python -m transformer_scaled_dot_02_gb300.profile --backward --b 4 --h 16 --n 8192 --mask 1
 
 Inputs are seeded N(0,1) bf16 values made on the device; nothing is checked.
-Prints the mean call time measured with CUDA events; for plain attention
-and the backward also TFLOP/s counting 4 (forward) or 10 (backward: five
-products) b h n_q n_k d FLOP per call, halved when causal.
+Prints the mean call time measured with CUDA events after one warm-up call;
+for plain attention and the backward also TFLOP/s, counting
+2 b h n_q n_k (d_k + d_v) FLOP per forward (S, O) and
+2 b h n_q n_k (3 d_k + 2 d_v) per backward (S, dP, dV, dK, dQ), halved when
+causal.
 """
 from __future__ import annotations
 
@@ -28,6 +30,7 @@ def main():
     ap.add_argument("--n", type=int, default=8192, help="query length (and key length)")
     ap.add_argument("--nk", type=int, default=0, help="key length if different (not causal)")
     ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--dv", type=int, default=0, help="value size if different from --d")
     ap.add_argument("--mask", type=int, default=1)
     ap.add_argument("--len-lo", type=int, default=0, help="padding lengths uniform in [lo, nk]")
     ap.add_argument("--mha", action="store_true", help="multi-head attention with projections")
@@ -42,6 +45,7 @@ def main():
     dev = torch.device("cuda", 0)
     n_q = a.n
     n_k = a.nk or a.n
+    d_v = a.dv or a.d
     lens = None
     if (a.mask & 2) or (a.decode and a.len_lo):
         lo = a.len_lo or n_k // 2
@@ -69,8 +73,8 @@ def main():
         def run():
             sd.multi_head_attention(xq, xkv, *ws, a.h, a.mask, lens, workspace=work)
     elif a.backward:
-        q, k, v, dout = (torch.randn(a.b, a.h, n, a.d, device=dev).to(torch.bfloat16)
-                         for n in (n_q, n_k, n_k, n_q))
+        q, k, v, dout = (torch.randn(a.b, a.h, n, d, device=dev).to(torch.bfloat16)
+                         for n, d in ((n_q, a.d), (n_k, a.d), (n_k, d_v), (n_q, d_v)))
         out, lse = sd.attention_with_lse(q, k, v, a.mask, lens, a.restricted)
         grads = [torch.empty_like(x) for x in (q, k, v)]
         work = torch.empty(sd.sdpa_backward_workspace_size(a.b, a.h, n_q, a.d), dtype=torch.uint8,
@@ -78,20 +82,21 @@ def main():
 
         def run():
             sd.sdpa_backward(q, k, v, out, dout, lse, *grads, work, work.numel(), a.b, a.h, n_q,
-                             n_k, a.d, a.d, a.mask, lens, a.restricted)
+                             n_k, a.d, d_v, a.mask, lens, a.restricted)
     else:
         q = torch.randn(a.b, a.h, n_q, a.d, device=dev).to(torch.bfloat16)
         k = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
-        v = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
-        out = torch.empty_like(q[..., : a.d])
+        v = torch.randn(a.b, a.h, n_k, d_v, device=dev).to(torch.bfloat16)
+        out = torch.empty(a.b, a.h, n_q, d_v, dtype=torch.bfloat16, device=dev)
 
         def run():
             if a.restricted:
-                sd.sdpa_forward_restricted(q, k, v, out, a.b, a.h, n_q, n_k, a.d, a.d, a.mask, lens,
+                sd.sdpa_forward_restricted(q, k, v, out, a.b, a.h, n_q, n_k, a.d, d_v, a.mask, lens,
                                            a.restricted)
             else:
-                sd.sdpa_forward(q, k, v, out, a.b, a.h, n_q, n_k, a.d, a.d, a.mask, lens)
+                sd.sdpa_forward(q, k, v, out, a.b, a.h, n_q, n_k, a.d, d_v, a.mask, lens)
 
+    run()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
@@ -103,7 +108,9 @@ def main():
     ms = s.elapsed_time(e) / a.iters
     line = "mean %.4f ms per call over %d calls" % (ms, a.iters)
     if not (a.mha or a.decode or a.restricted):
-        flops = (10 if a.backward else 4) * a.b * a.h * n_q * n_k * a.d * (0.5 if a.mask & 1 else 1)
+        # 2 n_q n_k per unit of head size: S and O in the forward; S, dP, dV, dK, dQ in the backward
+        units = 3 * a.d + 2 * d_v if a.backward else a.d + d_v
+        flops = 2 * units * a.b * a.h * n_q * n_k * (0.5 if a.mask & 1 else 1)
         line += ", %.1f TFLOP/s" % (flops / (ms * 1e-3) / 1e12)
     print(line)
 
