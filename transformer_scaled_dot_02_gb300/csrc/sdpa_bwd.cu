@@ -279,7 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         mbar_wait_drain(q_full + it % kStages, static_cast<uint32_t>(it / kStages) & 1u);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0 && n_it > 0) {
+    // The whole warp runs this loop in step (warp-uniform waits and
+    // descriptors); one elected lane issues every product and commit.
+    if (n_it > 0) {
       const uint32_t k_smem = smem_base + C::kKOff;
       const uint32_t v_smem = smem_base + C::kVOff;
       // Shared-memory descriptors as 32-bit halves: every operand here is
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 #pragma unroll
           for (int k = 0; k < dsize / 16; ++k) {
             constexpr int kS = L::kStepsPerRow;
-            mma_bf16_ss_lohi(d, a0 + static_cast<uint32_t>(((k / kS) * L::kKVBox + (k % kS) * 32) >> 4),
+            mma_bf16_ss_warp(d, a0 + static_cast<uint32_t>(((k / kS) * L::kKVBox + (k % kS) * 32) >> 4),
                              L::kDescHi,
                              b0 + static_cast<uint32_t>(((k / kS) * L::kQBox + (k % kS) * 32) >> 4),
                              L::kDescHi, kIdescS, k > 0 ? 1u : 0u);
@@ -307,31 +309,31 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         else
           product(LK{}, k_smem, st, DK);
       };
-      bool ok = mbar_wait(kv_full, 0, ab) && mbar_wait(q_full, 0, ab);
+      bool ok = mbar_wait_warp(kv_full, 0, ab) && mbar_wait_warp(q_full, 0, ab);
       tc_fence_after();
       if (ok) {
         issue_s(0, false);
         issue_s(0, true);
-        mma_commit(s_full);
+        mma_commit_warp(s_full);
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int b = it & 1;
         if (it + 1 < n_it) {
           const int nx = it + 1;
-          ok = mbar_wait(q_full + nx % kStages, static_cast<uint32_t>(nx / kStages) & 1u, ab);
+          ok = mbar_wait_warp(q_full + nx % kStages, static_cast<uint32_t>(nx / kStages) & 1u, ab);
           if (!ok) break;
           tc_fence_after();
           issue_s(nx, false);
           // dP^T(it+1) lands where dQ^T(it-1) was: its epilogue must have read it
           if (it >= 1) {
-            ok = mbar_wait(dq_empty + (nx & 1), static_cast<uint32_t>((it - 1) >> 1) & 1u, ab);
+            ok = mbar_wait_warp(dq_empty + (nx & 1), static_cast<uint32_t>((it - 1) >> 1) & 1u, ab);
             if (!ok) break;
             tc_fence_after();
           }
           issue_s(nx, true);
-          mma_commit(s_full + (nx & 1));
+          mma_commit_warp(s_full + (nx & 1));
         }
-        ok = mbar_wait(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
+        ok = mbar_wait_warp(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
         const uint32_t st = smem_base + C::kStageOff + (it % kStages) * C::kStageBytes;
@@ -342,27 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k) {
           const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
-          mma_bf16_ts_lohi(tmem + 256, buf + col,
+          mma_bf16_ts_warp(tmem + 256, buf + col,
                            bdo + (static_cast<uint32_t>(k * 16 * LV::kRowBytes) >> 4), LV::kDescHi,
                            C::kIdescDV, (it > 0 || k > 0) ? 1u : 0u);
-          mma_bf16_ts_lohi(tmem + C::kDkCol, buf + 64 + col,
+          mma_bf16_ts_warp(tmem + C::kDkCol, buf + 64 + col,
                            bq + (static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4), LK::kDescHi,
                            C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(q_empty + it % kStages);
+        mma_commit_warp(q_empty + it % kStages);
         // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
         const uint32_t ak = lo(k_smem, LK::kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
 #pragma unroll
         for (int k = 0; k < kBM / 16; ++k) {
           const uint32_t ka = static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4;  // 16 key rows of K
           const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;            // of dS^T
-          mma_bf16_ss_lohi(buf + 64, ak + ka, LK::kDescHi, bds + kb, kDsHi, kIdescQ,
+          mma_bf16_ss_warp(buf + 64, ak + ka, LK::kDescHi, bds + kb, kDsHi, kIdescQ,
                            k > 0 ? 1u : 0u);
         }
-        mma_commit(dq_full + b);
+        mma_commit_warp(dq_full + b);
       }
-      if (ok) mma_commit(acc_full);
-      mma_commit(drain);
+      if (ok) mma_commit_warp(acc_full);
+      mma_commit_warp(drain);
       mbar_wait_drain(drain, 0);
     }
   } else if (warp >= kEpilogueWarp0) {
