@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    // The whole warp runs this loop in step (warp-uniform waits and
+    // descriptors); one elected lane issues every product and commit.
+    if (n_kv > 0) {
       constexpr uint32_t kDescHi = C::kDescHi;
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       const uint32_t q_lo = lo(smem_base + C::kQOff, 16);
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
 #pragma unroll
         for (int k = 0; k < DK / 16; ++k) {
           constexpr int kS = C::kStepsPerRow;
-          mma_bf16_ss_lohi(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
+          mma_bf16_ss_warp(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
                            kDescHi,
                            b0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4),
                            kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
@@ -237,44 +239,44 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
         const uint32_t b0 = lo(smem_base + C::kVOff + (u & 1) * C::kVBytes, C::kKVBox);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
-          mma_bf16_ts_lohi(tmem + C::kOCol, pa + static_cast<uint32_t>(k * 8),
+          mma_bf16_ts_warp(tmem + C::kOCol, pa + static_cast<uint32_t>(k * 8),
                            b0 + static_cast<uint32_t>((k * 16 * C::kRowBytes) >> 4), kDescHi,
                            C::kIdescPV,
                            (u > 0 || k > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(q_full, 0, ab) && mbar_wait(k_full, 0, ab);
+      bool ok = mbar_wait_warp(q_full, 0, ab) && mbar_wait_warp(k_full, 0, ab);
       tc_fence_after();
       if (ok) {
         issue_s(0);
 #ifndef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
-        mma_commit(s_full);
+        mma_commit_warp(s_full);
 #endif
         // (test builds only, never in libsdpa.so: the first score tile is
         // never signalled, so the softmax warps' bounded wait runs out)
-        mma_commit(k_empty);
+        mma_commit_warp(k_empty);
       }
       for (int u = 0; ok && u < n_kv; ++u) {
         if (u + 1 < n_kv) {
           // S(u+1) into the buffer of P(u-1): PV(u-1) was issued before it
           const int nx = u + 1;
-          ok = mbar_wait(k_full + (nx & 1), static_cast<uint32_t>(nx >> 1) & 1u, ab);
+          ok = mbar_wait_warp(k_full + (nx & 1), static_cast<uint32_t>(nx >> 1) & 1u, ab);
           if (!ok) break;
           tc_fence_after();
           issue_s(nx);
-          mma_commit(s_full + (nx & 1));
-          mma_commit(k_empty + (nx & 1));
+          mma_commit_warp(s_full + (nx & 1));
+          mma_commit_warp(k_empty + (nx & 1));
         }
-        ok = mbar_wait(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
-             mbar_wait(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
+        ok = mbar_wait_warp(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
+             mbar_wait_warp(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
         issue_pv(u);
-        mma_commit(o_full);
-        if (u + 1 == n_kv) mma_commit(o_last);
-        mma_commit(v_empty + (u & 1));
+        mma_commit_warp(o_full);
+        if (u + 1 == n_kv) mma_commit_warp(o_last);
+        mma_commit_warp(v_empty + (u & 1));
       }
-      mma_commit(drain);
+      mma_commit_warp(drain);
       mbar_wait_drain(drain, 0);
     }
   } else {

@@ -276,7 +276,9 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    // The whole warp runs this loop in step (warp-uniform waits and
+    // descriptors); one elected lane issues every product and commit.
+    if (n_kv > 0) {
       const uint32_t q_smem = smem_base + C::kQOff;
       const uint32_t k_smem = smem_base + C::kKOff;
       const uint32_t v_smem = smem_base + C::kVOff;
@@ -297,7 +299,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         for (int k = 0; k < DK / 16; ++k) {
           const uint32_t off = static_cast<uint32_t>(
               ((k / CK::kStepsPerRow) * CK::kBoxBytes + (k % CK::kStepsPerRow) * 32) >> 4);
-          mma_bf16_ss_lohi(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, C::kIdescS, k > 0 ? 1u : 0u);
+          mma_bf16_ss_warp(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int stage, bool accumulate) {
@@ -306,13 +308,13 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         const uint32_t b0 = v_lo + static_cast<uint32_t>((stage * CV::kTileBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < kBlockN / 16; ++k) {
-          mma_bf16_ts_lohi(d_tmem, p_tmem + static_cast<uint32_t>(k * 8),
+          mma_bf16_ts_warp(d_tmem, p_tmem + static_cast<uint32_t>(k * 8),
                            b0 + static_cast<uint32_t>((k * 16 * CV::kRowBytes) >> 4), v_hi, C::kIdescPV,
                            (accumulate || k > 0) ? 1u : 0u);
         }
       };
 
-      bool ok = mbar_wait(bars.q_full, 0, ab) && mbar_wait(bars.k_full, 0, ab);
+      bool ok = mbar_wait_warp(bars.q_full, 0, ab) && mbar_wait_warp(bars.k_full, 0, ab);
       tc_fence_after();
       if (ok) {
         const int last_t = active(1, j_first) ? 1 : 0;
@@ -323,17 +325,17 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
           // Test builds only (never in libsdpa.so): the first score tile of
           // query tile 0 is never signalled, so its softmax warps' bounded
           // wait runs out and the kernel reports a timeout.
-          if (t != 0) mma_commit(bars.s_full + t);
+          if (t != 0) mma_commit_warp(bars.s_full + t);
 #else
-          mma_commit(bars.s_full + t);
+          mma_commit_warp(bars.s_full + t);
 #endif
-          if (t == last_t) mma_commit(bars.k_empty);
+          if (t == last_t) mma_commit_warp(bars.k_empty);
         }
       }
       for (int u = 0; ok && u < n_kv; ++u) {
         const int j = j_first + u;
         const int s = u % C::kVStages;
-        ok = mbar_wait(bars.v_full + s, static_cast<uint32_t>(u / C::kVStages) & 1u, ab);
+        ok = mbar_wait_warp(bars.v_full + s, static_cast<uint32_t>(u / C::kVStages) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
         const bool pv_any = active(0, j) || active(1, j);
@@ -345,35 +347,35 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         bool k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (active(t, j)) {
-            ok = mbar_wait(bars.p_full + t, static_cast<uint32_t>(j - lo_of(t)) & 1u, ab);
+            ok = mbar_wait_warp(bars.p_full + t, static_cast<uint32_t>(j - lo_of(t)) & 1u, ab);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, s, j > lo_of(t));
-            mma_commit(bars.o_full + t);
-            if (t == last_pv_t) mma_commit(bars.v_empty + s);
+            mma_commit_warp(bars.o_full + t);
+            if (t == last_pv_t) mma_commit_warp(bars.v_empty + s);
           }
           if (active(t, j + 1)) {
             if (!k_next_ready) {
-              ok = mbar_wait(bars.k_full + sn, kn_phase, ab);
+              ok = mbar_wait_warp(bars.k_full + sn, kn_phase, ab);
               if (!ok) break;
               tc_fence_after();
               k_next_ready = true;
             }
             issue_s(t, sn);
-            mma_commit(bars.s_full + t);
-            if (t == last_s_t) mma_commit(bars.k_empty + sn);
+            mma_commit_warp(bars.s_full + t);
+            if (t == last_s_t) mma_commit_warp(bars.k_empty + sn);
           }
         }
         // A key tile inside the walked range that no query tile uses is still
         // released, so the producer's ring keeps turning.
-        if (ok && !pv_any) mma_commit(bars.v_empty + s);
+        if (ok && !pv_any) mma_commit_warp(bars.v_empty + s);
         if (ok && !s_any && u + 1 < n_kv) {
-          ok = mbar_wait(bars.k_full + sn, kn_phase, ab);
-          if (ok) mma_commit(bars.k_empty + sn);
+          ok = mbar_wait_warp(bars.k_full + sn, kn_phase, ab);
+          if (ok) mma_commit_warp(bars.k_empty + sn);
         }
       }
       // Every MMA issued above has finished once this barrier completes.
-      mma_commit(bars.drain);
+      mma_commit_warp(bars.drain);
       mbar_wait_drain(bars.drain, 0);
     }
    }
