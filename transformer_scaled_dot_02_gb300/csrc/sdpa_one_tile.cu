@@ -60,9 +60,8 @@ struct OCfg {
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + 2 * kKBytes;
   static constexpr int kBarOff = kVOff + 2 * kVBytes;
-  // q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_full,
-  // o_last, drain
-  static constexpr int kNumBars = 1 + 8 + 4 + 3;
+  // q_full, k_full[2], v_full[2], s_full[2], p_full[2], o_full[2], o_last, drain
+  static constexpr int kNumBars = 1 + 10 + 2;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
@@ -102,13 +101,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* q_full = bar;
   uint64_t* k_full = bar + 1;
-  uint64_t* k_empty = k_full + 2;
-  uint64_t* v_full = k_empty + 2;
-  uint64_t* v_empty = v_full + 2;
-  uint64_t* s_full = v_empty + 2;
+  // A K stage is free again once the scores that read it are done (s_full),
+  // a V stage once the O += P V that read it is done (o_full): no separate
+  // "empty" barriers, so each key tile costs two commits instead of four.
+  uint64_t* v_full = k_full + 2;
+  uint64_t* s_full = v_full + 2;
   uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;   // one phase per O += P V
-  uint64_t* o_last = o_full + 1;   // once, after the last O += P V
+  uint64_t* o_full = p_full + 2;   // o_full[u & 1]: one phase per O += P(u) V_u
+  uint64_t* o_last = o_full + 2;   // once, after the last O += P V
   uint64_t* drain = o_last + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -161,13 +161,11 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(k_full + s, 1);
-      mbar_init(k_empty + s, 1);
       mbar_init(v_full + s, 1);
-      mbar_init(v_empty + s, 1);
+      mbar_init(o_full + s, 1);
       mbar_init(s_full + s, 1);
       mbar_init(p_full + s, kBlockM);
     }
-    mbar_init(o_full, 1);
     mbar_init(o_last, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -194,14 +192,18 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
         const int j = j_lo + u;
         const int s = u & 1;
         const uint32_t use = static_cast<uint32_t>(u >> 1);
-        if (u >= 2 && !mbar_wait(k_empty + s, (use - 1) & 1u, ab)) break;
+        // S(u-2) read this stage last.  s_full[s] cannot be two phases
+        // ahead: S(u) needs the K_u loaded below.
+        if (u >= 2 && !mbar_wait(s_full + s, (use - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(k_full + s, C::kKBytes);
         for (int c = 0; c < DK / C::kBoxCols; ++c)
           tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox,
                       c * C::kBoxCols,
                       j * BN, hi, bi);
         k_issued = u + 1;
-        if (u >= 2 && !mbar_wait(v_empty + s, (use - 1) & 1u, ab)) break;
+        // O += P(u-2) V(u-2) read this stage last; o_full[s] cannot be two
+        // phases ahead either (O += P(u) V_u needs V_u).
+        if (u >= 2 && !mbar_wait(o_full + s, (use - 1) & 1u, ab)) break;
         mbar_arrive_expect_tx(v_full + s, C::kVBytes);
         for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
           tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
@@ -253,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
         mma_commit_warp(s_full);
 #endif
         // (test builds only, never in libsdpa.so: the first score tile is
-        // never signalled, so the softmax warps' bounded wait runs out)
-        mma_commit_warp(k_empty);
+        // never signalled, so the bounded waits of the softmax warps, and of
+        // the producer once it needs that K stage again, run out)
       }
       for (int u = 0; ok && u < n_kv; ++u) {
         if (u + 1 < n_kv) {
@@ -265,16 +267,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
           tc_fence_after();
           issue_s(nx);
           mma_commit_warp(s_full + (nx & 1));
-          mma_commit_warp(k_empty + (nx & 1));
         }
         ok = mbar_wait_warp(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
              mbar_wait_warp(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
         if (!ok) break;
         tc_fence_after();
         issue_pv(u);
-        mma_commit_warp(o_full);
+        mma_commit_warp(o_full + (u & 1));
         if (u + 1 == n_kv) mma_commit_warp(o_last);
-        mma_commit_warp(v_empty + (u & 1));
       }
       mma_commit_warp(drain);
       mbar_wait_drain(drain, 0);
@@ -339,12 +339,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
           m_used = m_new;
           l *= alpha;
         }
-        // Only a rescale touches O, and it must follow O += P(u-1) V(u-1).
-        // Holding S(u) means O += P(u-2) V(u-2) has landed (S(u) was issued
-        // after it), so o_full is in phase u-1 or u and its parity wait for
-        // phase u-1 is exact even though earlier phases were not waited on.
+        // Only a rescale touches O, and it must follow O += P(u-1) V(u-1),
+        // whose barrier is o_full[(u-1) & 1].  Holding S(u) means
+        // O += P(u-2) V(u-2) has landed (S(u) was issued after it), so the
+        // barrier's previous phase, u-3, is complete; and O += P(u+1) V(u+1)
+        // needs this softmax's next P.  Its parity wait for the phase of u-1
+        // is therefore exact even though earlier phases were not waited on.
         if (rescale_warp) {
-          ok = mbar_wait_warp(o_full, static_cast<uint32_t>(u - 1) & 1u, ab);
+          ok = mbar_wait_warp(o_full + ((u - 1) & 1), static_cast<uint32_t>((u - 1) >> 1) & 1u, ab);
           if (!ok) break;
           tc_fence_after();
         }
