@@ -52,7 +52,8 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 //                query half w / 4 (32 queries) of each step; at the end they
 //                write dK and dV.
 //   warp 8       TMA producer (K_j, V_j once; Q_i, dO_i, lse2, D in 3 stages).
-//   warp 9       MMA issuer, in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T(i).
+//   warp 9       MMA issuer (the whole warp; one elected lane issues each
+//                instruction), in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T(i).
 //   warps 10-13  dQ^T of each step out of tensor memory into the staging tile.
 // Tensor memory: buffer b = step & 1 holds S^T at 128 b (64 columns; P^T in
 // bf16 over columns 128 b + 32 h .. +16 of each half h) and dP^T at

@@ -18,7 +18,8 @@
 // Roles:
 //   warp 4      TMA producer: Q once, K_j and V_j (this CTA's d_v slice) in
 //               two stages each.
-//   warp 5      MMA issuer: S(j+1) = Q K_{j+1}^T into the free score buffer,
+//   warp 5      MMA issuer (the whole warp; one elected lane issues each
+//               instruction): S(j+1) = Q K_{j+1}^T into the free score buffer,
 //               then O += P(j) V_j with P(j) read from tensor memory.
 //   warps 0-3   softmax, one thread per query row (tensor-memory lane): the
 //               running max / sum, P in bf16 over the scores it replaces, the

@@ -15,7 +15,8 @@
 //   warp 8      TMA producer: Q tiles once, then K_j and V_j into a ring of
 //               shared-memory stages (rows swizzled at their width, zero fill
 //               past n).
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into tensor memory,
+//   warp 9      MMA issuer (the whole warp; one elected lane issues each
+//               instruction): S_t = Q_t K_j^T into tensor memory,
 //               then O_t += P_t V_j with P_t read from tensor memory.
 //   warps 10-11 idle (they complete the third warpgroup for the register split).
 //   warps 0-7   two softmax warpgroups, one per query tile, one thread per
