@@ -6,9 +6,13 @@
 //   - wide heads, d_k = d_v in {256, 512} (Table 3, rows (A)), whose 128 x d
 //     fp32 O does not fit the two-tile plan in 512 tensor-memory columns:
 //       d = 256: key tiles of 64; one CTA per query tile.
-//       d = 512: key tiles of 32; two CTAs per query tile, one per half of
+//       d = 512: key tiles of 64; two CTAs per query tile, one per half of
 //                d_v, each recomputing the scores (Q, 128 KB, stays in
-//                shared memory).
+//                shared memory).  K and V have one stage each; K comes
+//                in two halves, and the next tile's first half loads
+//                while the scores run over the second.  The scores of the
+//                next tile are issued in two parts around O += P V, so
+//                that product never waits for a K load.
 //   - d = 64 and 128 where the key walk is short: key tiles of 64, 256
 //     tensor-memory columns, two CTAs per SM, so short sequences get twice
 //     the CTAs in flight and half the serial chain per CTA.
@@ -41,7 +45,12 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the 64/128 kerne
 
 template <int DK>
 struct OCfg {
-  static constexpr int BN = (DK == 512 || DK < 64) ? 32 : 64;   // keys per tile
+  static constexpr int BN = DK < 64 ? 32 : 64;             // keys per tile
+  // d = 512: one K stage and one V stage (Q alone takes 128 KB), K loaded
+  // and released in two halves so that the next tile's first half lands
+  // while the scores still run over the second.
+  static constexpr bool kOneStage = DK == 512;
+  static constexpr int kStages = kOneStage ? 1 : 2;
   static constexpr int kDvc = DK < 256 ? DK : 256;          // O columns per CTA
   static constexpr int kChunks = DK / kDvc;                 // CTAs per query tile
   // Tiles move as boxes of kBoxCols columns, rows of kRowBytes swizzled at
@@ -59,10 +68,11 @@ struct OCfg {
   static constexpr int kVBytes = (kDvc / kBoxCols) * kKVBox;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
-  static constexpr int kVOff = kKOff + 2 * kKBytes;
-  static constexpr int kBarOff = kVOff + 2 * kVBytes;
-  // q_full, k_full[2], v_full[2], s_full[2], p_full[2], o_full[2], o_last, drain
-  static constexpr int kNumBars = 1 + 10 + 2;
+  static constexpr int kVOff = kKOff + kStages * kKBytes;
+  static constexpr int kBarOff = kVOff + kStages * kVBytes;
+  // q_full, k_full[2], v_full[2], s_full[2], p_full[2], o_full[2], o_last, drain,
+  // kh_free
+  static constexpr int kNumBars = 1 + 10 + 3;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
@@ -111,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   uint64_t* o_full = p_full + 2;   // o_full[u & 1]: one phase per O += P(u) V_u
   uint64_t* o_last = o_full + 2;   // once, after the last O += P V
   uint64_t* drain = o_last + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* kh_free = drain + 1;   // one stage: the first half of S(u) is done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kh_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const AbortState ab{abort_flag, p.status};
 
@@ -169,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
     }
     mbar_init(o_last, 1);
     mbar_init(drain, 1);
+    mbar_init(kh_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -189,33 +201,70 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
       for (int c = 0; c < DK / C::kBoxCols; ++c)
         tma_load_4d(&p.tm_q, q_full, smem + C::kQOff + c * C::kQBox, c * C::kBoxCols, qs, hi, bi);
       int k_issued = 0, v_issued = 0;
-      for (int u = 0; u < n_kv; ++u) {
-        const int j = j_lo + u;
-        const int s = u & 1;
-        const uint32_t use = static_cast<uint32_t>(u >> 1);
-        // S(u-2) read this stage last.  s_full[s] cannot be two phases
-        // ahead: S(u) needs the K_u loaded below.
-        if (u >= 2 && !mbar_wait(s_full + s, (use - 1) & 1u, ab)) break;
-        mbar_arrive_expect_tx(k_full + s, C::kKBytes);
-        for (int c = 0; c < DK / C::kBoxCols; ++c)
-          tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox,
-                      c * C::kBoxCols,
-                      j * BN, hi, bi);
-        k_issued = u + 1;
-        // O += P(u-2) V(u-2) read this stage last; o_full[s] cannot be two
-        // phases ahead either (O += P(u) V_u needs V_u).
-        if (u >= 2 && !mbar_wait(o_full + s, (use - 1) & 1u, ab)) break;
-        mbar_arrive_expect_tx(v_full + s, C::kVBytes);
-        for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
-          tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
-                      chunk * C::kDvc + c * C::kBoxCols, j * BN, hi, bi);
-        v_issued = u + 1;
+      if constexpr (C::kOneStage) {
+        // k_full[h]: half h of the K tile (one phase per tile); v_full[0]: V.
+        constexpr int kHalfBoxes = DK / C::kBoxCols / 2;
+        int k0_issued = 0;
+        for (int u = 0; u < n_kv; ++u) {
+          const int j = j_lo + u;
+          const uint32_t prev = static_cast<uint32_t>(u - 1);
+          // S(u-1)'s first half read this half last; kh_free cannot be a
+          // phase ahead of it, since S(u) needs the half loaded here.
+          if (u >= 1 && !mbar_wait(kh_free, prev & 1u, ab)) break;
+          mbar_arrive_expect_tx(k_full, C::kKBytes / 2);
+          for (int c = 0; c < kHalfBoxes; ++c)
+            tma_load_4d(&p.tm_k, k_full, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols, j * BN,
+                        hi, bi);
+          k0_issued = u + 1;
+          // all of S(u-1) read the second half (s_full of its buffer)
+          if (u >= 1 && !mbar_wait(s_full + (prev & 1u), (prev >> 1) & 1u, ab)) break;
+          mbar_arrive_expect_tx(k_full + 1, C::kKBytes / 2);
+          for (int c = kHalfBoxes; c < 2 * kHalfBoxes; ++c)
+            tma_load_4d(&p.tm_k, k_full + 1, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols,
+                        j * BN, hi, bi);
+          k_issued = u + 1;
+          // O += P(u-1) V(u-1) read V last (o_full of its parity)
+          if (u >= 1 && !mbar_wait(o_full + (prev & 1u), (prev >> 1) & 1u, ab)) break;
+          mbar_arrive_expect_tx(v_full, C::kVBytes);
+          for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
+            tma_load_4d(&p.tm_v, v_full, smem + C::kVOff + c * C::kKVBox,
+                        chunk * C::kDvc + c * C::kBoxCols, j * BN, hi, bi);
+          v_issued = u + 1;
+        }
+        mbar_wait_drain(q_full, 0);
+        // each load was issued only after the previous one into the same
+        // place had been consumed, so only the last of each can be in flight
+        if (k0_issued > 0) mbar_wait_drain(k_full, static_cast<uint32_t>(k0_issued - 1) & 1u);
+        if (k_issued > 0) mbar_wait_drain(k_full + 1, static_cast<uint32_t>(k_issued - 1) & 1u);
+        if (v_issued > 0) mbar_wait_drain(v_full, static_cast<uint32_t>(v_issued - 1) & 1u);
+      } else {
+        for (int u = 0; u < n_kv; ++u) {
+          const int j = j_lo + u;
+          const int s = u & 1;
+          const uint32_t use = static_cast<uint32_t>(u >> 1);
+          // S(u-2) read this stage last.  s_full[s] cannot be two phases
+          // ahead: S(u) needs the K_u loaded below.
+          if (u >= 2 && !mbar_wait(s_full + s, (use - 1) & 1u, ab)) break;
+          mbar_arrive_expect_tx(k_full + s, C::kKBytes);
+          for (int c = 0; c < DK / C::kBoxCols; ++c)
+            tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox,
+                        c * C::kBoxCols, j * BN, hi, bi);
+          k_issued = u + 1;
+          // O += P(u-2) V(u-2) read this stage last; o_full[s] cannot be two
+          // phases ahead either (O += P(u) V_u needs V_u).
+          if (u >= 2 && !mbar_wait(o_full + s, (use - 1) & 1u, ab)) break;
+          mbar_arrive_expect_tx(v_full + s, C::kVBytes);
+          for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
+            tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
+                        chunk * C::kDvc + c * C::kBoxCols, j * BN, hi, bi);
+          v_issued = u + 1;
+        }
+        mbar_wait_drain(q_full, 0);
+        for (int u = max(0, k_issued - 2); u < k_issued; ++u)
+          mbar_wait_drain(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
+        for (int u = max(0, v_issued - 2); u < v_issued; ++u)
+          mbar_wait_drain(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
       }
-      mbar_wait_drain(q_full, 0);
-      for (int u = max(0, k_issued - 2); u < k_issued; ++u)
-        mbar_wait_drain(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
-      for (int u = max(0, v_issued - 2); u < v_issued; ++u)
-        mbar_wait_drain(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -225,21 +274,45 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
       constexpr uint32_t kDescHi = C::kDescHi;
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       const uint32_t q_lo = lo(smem_base + C::kQOff, 16);
-      auto issue_s = [&](int u) {
+      // S(u) = Q K_u^T into score buffer u & 1, part `part` of `parts`: waits
+      // for that part of K_u, issues its k steps, and commits kh_free after a
+      // first half or s_full after the last part.  One stage: K_u comes in
+      // two halves; two stages: in one piece.
+      auto issue_s = [&](int u, int part, int parts) -> bool {
         const uint32_t d = tmem + static_cast<uint32_t>((u & 1) * BN);
-        const uint32_t b0 = lo(smem_base + C::kKOff + (u & 1) * C::kKBytes, 16);
+        const int stage = C::kOneStage ? 0 : (u & 1);
+        const uint32_t b0 = lo(smem_base + C::kKOff + stage * C::kKBytes, 16);
+        const uint32_t ph = static_cast<uint32_t>(C::kOneStage ? u : (u >> 1)) & 1u;
+        if (!mbar_wait_warp(k_full + (C::kOneStage ? part : (u & 1)), ph, ab)) return false;
+        tc_fence_after();
+        constexpr int kSteps = DK / 16;
+        const int k_begin = part * (kSteps / parts);
 #pragma unroll
-        for (int k = 0; k < DK / 16; ++k) {
+        for (int k = 0; k < kSteps; ++k) {
+          if (k < k_begin || k >= k_begin + kSteps / parts) continue;
           constexpr int kS = C::kStepsPerRow;
           mma_bf16_ss_warp(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
                            kDescHi,
                            b0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4),
                            kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
         }
+        if (part + 1 < parts) {
+          mma_commit_warp(kh_free);
+          return true;
+        }
+#ifdef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
+        // (test builds only, never in libsdpa.so: the first score tile is
+        // never signalled, so the bounded waits of the softmax warps, and of
+        // the producer once it needs that K stage again, run out)
+        if (u == 0) return true;
+#endif
+        mma_commit_warp(s_full + (u & 1));
+        return true;
       };
       auto issue_pv = [&](int u) {
         const uint32_t pa = tmem + static_cast<uint32_t>((u & 1) * BN);
-        const uint32_t b0 = lo(smem_base + C::kVOff + (u & 1) * C::kVBytes, C::kKVBox);
+        const int stage = C::kOneStage ? 0 : (u & 1);
+        const uint32_t b0 = lo(smem_base + C::kVOff + stage * C::kVBytes, C::kKVBox);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           mma_bf16_ts_warp(tmem + C::kOCol, pa + static_cast<uint32_t>(k * 8),
@@ -248,34 +321,27 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
                            (u > 0 || k > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait_warp(q_full, 0, ab) && mbar_wait_warp(k_full, 0, ab);
+      constexpr int kParts = C::kOneStage ? 2 : 1;
+      bool ok = mbar_wait_warp(q_full, 0, ab);
       tc_fence_after();
-      if (ok) {
-        issue_s(0);
-#ifndef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
-        mma_commit_warp(s_full);
-#endif
-        // (test builds only, never in libsdpa.so: the first score tile is
-        // never signalled, so the bounded waits of the softmax warps, and of
-        // the producer once it needs that K stage again, run out)
-      }
+      for (int part = 0; ok && part < kParts; ++part) ok = issue_s(0, part, kParts);
       for (int u = 0; ok && u < n_kv; ++u) {
-        if (u + 1 < n_kv) {
-          // S(u+1) into the buffer of P(u-1): PV(u-1) was issued before it
-          const int nx = u + 1;
-          ok = mbar_wait_warp(k_full + (nx & 1), static_cast<uint32_t>(nx >> 1) & 1u, ab);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(nx);
-          mma_commit_warp(s_full + (nx & 1));
-        }
+        // S(u+1) into the buffer of P(u-1): PV(u-1) was issued before it.
+        // One stage: only its first half goes ahead of O += P(u) V_u; the
+        // second half waits for K data that is loaded once S(u) is done, and
+        // O += P(u) V_u should not queue behind that load.
+        const bool next = u + 1 < n_kv;
+        if (next && !(ok = issue_s(u + 1, 0, kParts))) break;
+        const uint32_t vs = C::kOneStage ? 0u : static_cast<uint32_t>(u & 1);
+        const uint32_t vph = static_cast<uint32_t>(C::kOneStage ? u : (u >> 1)) & 1u;
         ok = mbar_wait_warp(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
-             mbar_wait_warp(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
+             mbar_wait_warp(v_full + vs, vph, ab);
         if (!ok) break;
         tc_fence_after();
         issue_pv(u);
         mma_commit_warp(o_full + (u & 1));
         if (u + 1 == n_kv) mma_commit_warp(o_last);
+        if (kParts == 2 && next && !(ok = issue_s(u + 1, 1, kParts))) break;
       }
       mma_commit_warp(drain);
       mbar_wait_drain(drain, 0);
@@ -466,7 +532,7 @@ cudaError_t launch_one_tile_impl(const SdpaTcParams& p, cudaStream_t stream) {
 }  // namespace
 
 int one_tile_key_tile(int head_dim) {
-  return (head_dim == 512 || head_dim < 64) ? OCfg<512>::BN : OCfg<256>::BN;
+  return head_dim < 64 ? OCfg<32>::BN : OCfg<256>::BN;
 }
 
 cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
