@@ -30,6 +30,24 @@ def test_linear(m, n, k):
     assert rel_err(host(y), ref) <= 1e-2
 
 
+@pytest.mark.parametrize("bn", ["256", "128"])
+@pytest.mark.parametrize("m,n,k", [(300, 520, 136), (257, 64, 1024), (1000, 712, 200), (128, 256, 64),
+                                   (4096, 512, 512)])
+def test_linear_each_tile_width(bn, m, n, k, monkeypatch):
+    """The projection GEMM with its tile width pinned (LIBSDPA_GEMM_BN) to
+    256 and 128 columns: ragged edges in m, n and k for both widths."""
+    monkeypatch.setenv("LIBSDPA_GEMM_BN", bn)
+    rng = np.random.default_rng(7 * m + n + k)
+    x = synthetic.round_to_bf16(rng.standard_normal((m, k)).astype(np.float32))
+    w = synthetic.round_to_bf16((rng.standard_normal((k, n)) / np.sqrt(k)).astype(np.float32))
+    t = __import__("torch")
+    y = t.full((m, n), 3.0, dtype=t.bfloat16, device="cuda")
+    sd.linear_forward(dev(x), dev(w), y, m, n, k)
+    sd.sdpa_device_check()
+    ref = x.astype(np.float64) @ w.astype(np.float64)
+    assert rel_err(host(y), ref) <= 1e-2
+
+
 def _mha_gpu(w, xq, xkv, wq, wk, wv, wo, lens):
     y = sd.multi_head_attention(dev(xq), dev(xkv), dev(wq), dev(wk), dev(wv), dev(wo), w.h,
                                 w.mask_kind, None if lens is None else dev_int(lens))

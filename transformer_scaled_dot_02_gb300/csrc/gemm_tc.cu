@@ -2,15 +2,23 @@
 // attention ("Attention Is All You Need", section 3.2.2: Q W^Q, K W^K, V W^V
 // and Concat(heads) W^O), Y = X W with X [m, k], W [k, n], Y [m, n] row-major.
 //
-// One CTA computes a 128 x 256 tile of Y with a single accumulator of 256
-// fp32 columns in tensor memory:
+// One CTA computes a 128 x BN tile of Y (BN = 256 or 128) with a single
+// accumulator of BN fp32 columns in tensor memory; two CTAs share an SM, so
+// one CTA's epilogue overlaps the other's products:
 //   warp 0      TMA producer: 64-wide k-slices of X (K-major) and W (N
-//               contiguous, i.e. MN-major for the MMA) into a 4-stage ring.
-//   warp 1      MMA issuer: tcgen05.mma M=128, N=256, K=16, four per slice.
+//               contiguous, i.e. MN-major for the MMA) into a ring of 2 or 3
+//               stages (48 or 32 KB each).
+//   warp 1      MMA issuer: tcgen05.mma M=128, N=BN, K=16, four per slice.
 //   warps 2-5   epilogue: tensor memory -> registers -> bf16 -> swizzled
 //               shared memory -> TMA store (clipped at the matrix edge).
 // Up to three independent problems share one launch (blockIdx.z), which runs
-// the Q, K and V projections together.
+// the Q, K and V projections together.  Measured on GB300, 128 x 256 tiles
+// with two CTAs per SM are the fastest or within 1 us of it on every
+// projection shape of the base and big models; 128-column tiles win only
+// when 256-column ones would leave half the SMs idle (the base model's
+// W^O, 4096 x 512 x 512).
+#include <cstdlib>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -18,19 +26,25 @@ namespace sdpa {
 namespace {
 
 constexpr int BM = kGemmBlockM;   // 128
-constexpr int BN = kGemmBlockN;   // 256
 constexpr int BK = 64;            // one 128-byte swizzle span of bf16
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kABytes = BM * BK * 2;           // 16 KB
 constexpr int kBBoxBytes = BK * 64 * 2;        // 8 KB: 64 k-rows x 64 n
-constexpr int kBBytes = BN * BK * 2;           // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kSmemBytes = kBarOff + (2 * kStages + 2) * 8 + 16 + 1024;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kIdesc = idesc_bf16(BM, BN, false, true);
 constexpr int kCBoxBytes = BM * 64 * 2;        // 16 KB staging box (128 rows x 64 cols)
+constexpr int kMinBlocks = 2;                  // CTAs per SM
+
+template <int BN>
+struct GCfg {
+  static constexpr int kStages = BN == 256 ? 2 : 3;
+  static constexpr int kBBytes = BN * BK * 2;  // 32 or 16 KB
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOff + (2 * kStages + 2) * 8 + 16 + 1024;
+  static constexpr uint32_t kTmemCols = BN;
+  static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, false, true);
+  static_assert(kSmemBytes * kMinBlocks <= 232448, "two CTAs per SM");
+  static_assert((BN / 64) * kCBoxBytes <= kBarOff, "the epilogue stages Y over the ring");
+};
 
 template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
@@ -38,12 +52,17 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gemm_bf16_tc(const __grid_constant__ GemmParams p) {
+template <int BN>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    gemm_bf16_tc(const __grid_constant__ GemmParams p) {
+  using C = GCfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr int kStageBytes = C::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   const uint32_t smem_base = smem_u32(smem);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
   uint64_t* drain = acc_full + 1;
@@ -77,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_tc(const __grid_constan
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -120,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_tc(const __grid_constan
           const uint64_t a = smem_desc_sw128(a_base + k * 32, 16, 1024);
           // W slice: 64 k-rows of 128 bytes per 64-column box; k step = 16 rows.
           const uint64_t b = smem_desc_sw128(b_base + k * 16 * 128, kBBoxBytes, 1024);
-          mma_bf16_ss(tmem, a, b, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ss(tmem, a, b, C::kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(empty + s);
       }
@@ -181,21 +200,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_bf16_tc(const __grid_constan
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmParams& p, int max_m, int max_n, cudaStream_t stream) {
+  cudaError_t err = cudaFuncSetAttribute(gemm_bf16_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GCfg<BN>::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  dim3 grid((max_n + BN - 1) / BN, (max_m + BM - 1) / BM, p.num_problems);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  gemm_bf16_tc<BN><<<grid, kThreads, GCfg<BN>::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Tile width: 256 columns, or 128 when 256-column tiles would not reach
+// half the SMs.  LIBSDPA_GEMM_BN = 256 | 128 pins it.
+int gemm_tile_n(const GemmParams& p) {
+  if (const char* e = std::getenv("LIBSDPA_GEMM_BN")) {
+    const int v = std::atoi(e);
+    if (v == 256 || v == 128) return v;
+  }
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    sms = 148;
+  long long tiles = 0;
+  for (int i = 0; i < p.num_problems; ++i)
+    tiles += 1ll * ((p.prob[i].m + BM - 1) / BM) * ((p.prob[i].n + 255) / 256);
+  return 2 * tiles >= sms ? 256 : 128;
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_tc(const GemmParams& p, int max_m, int max_n, cudaStream_t stream) {
-  cudaError_t err =
-      cudaFuncSetAttribute(gemm_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (err != cudaSuccess) return err;
   if (max_m <= 0 || max_n <= 0 || p.num_problems <= 0) return cudaSuccess;
-  dim3 grid((max_n + BN - 1) / BN, (max_m + BM - 1) / BM, p.num_problems);
-  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  gemm_bf16_tc<<<grid, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  const int bn = gemm_tile_n(p);
+  if (bn == 256) return launch_bn<256>(p, max_m, max_n, stream);
+  return launch_bn<128>(p, max_m, max_n, stream);
 }
 
 }  // namespace sdpa

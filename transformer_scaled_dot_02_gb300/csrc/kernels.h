@@ -103,7 +103,6 @@ struct GemmParams {
   unsigned* status;
 };
 constexpr int kGemmBlockM = 128;
-constexpr int kGemmBlockN = 256;
 cudaError_t launch_gemm_tc(const GemmParams& p, int max_m, int max_n, cudaStream_t stream);
 
 }  // namespace sdpa
