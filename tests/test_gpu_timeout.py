@@ -1,10 +1,11 @@
 """Failure detection without a GPU fault: a bounded wait that runs out.
 
-A test-only copy of the attention kernel, compiled here with
+A test-only copy of the attention kernels, compiled here with
 SDPA_TEST_WITHHOLD_FIRST_S_COMMIT, never signals the first score tile of a
-query tile.  The softmax warps' wait on it gives up after its limit (about a
-second), the CTA aborts cleanly (copies and MMAs in flight are drained, tensor
-memory is freed) and sdpa_device_check() reports SDPA_ERR_DEVICE_TIMEOUT.  The
+query tile (forward) or of a key tile (backward).  The softmax or compute
+warps' wait on it gives up after its limit (about a second), the CTA aborts
+cleanly (copies and MMAs in flight are drained, tensor memory is freed) and
+sdpa_device_check() reports SDPA_ERR_DEVICE_TIMEOUT.  The
 context stays usable: the same library then returns to normal operation and
 the product library computes correct results.
 """
@@ -30,7 +31,7 @@ def faulty_lib():
     sd_build.build()
     d = tempfile.mkdtemp(prefix="sdpa_timeout_")
     nvcc = sd_build._nvcc()
-    hooked = ["sdpa_tc.cu", "sdpa_one_tile.cu"]   # both attention kernels carry the hook
+    hooked = ["sdpa_tc.cu", "sdpa_one_tile.cu", "sdpa_bwd.cu"]   # every attention kernel carries the hook
     objs = []
     for src in hooked:
         obj = os.path.join(d, src.replace(".cu", "_withhold.o"))
@@ -71,3 +72,34 @@ def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, monkeypatch):
     got = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL))
     sd.sdpa_device_check()
     assert rel_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
+
+
+def test_backward_bounded_wait_times_out_and_reports(faulty_lib):
+    import ctypes
+    import torch
+    rng = np.random.default_rng(2)
+    b, h, n, d = 1, 1, 128, 64   # one key tile: one CTA of the backward
+    q, k, v, do = (synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
+                   for _ in range(4))
+    qd, kd, vd, dod = dev(q), dev(k), dev(v), dev(do)
+    out, lse = sd.attention_with_lse(qd, kd, vd, sd.SDPA_MASK_CAUSAL)   # product library
+    sd.sdpa_device_check()
+    ws = torch.empty(sd.sdpa_backward_workspace_size(b, h, n, d), dtype=torch.uint8, device="cuda")
+    g = [torch.empty_like(x) for x in (qd, kd, vd)]
+    stream = torch.cuda.current_stream().cuda_stream
+    t0 = time.time()
+    rc = faulty_lib.sdpa_backward(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(),
+                                  dod.data_ptr(), lse.data_ptr(), g[0].data_ptr(), g[1].data_ptr(),
+                                  g[2].data_ptr(), ws.data_ptr(), ws.numel(), b, h, n, n, d, d,
+                                  sd.SDPA_MASK_CAUSAL, None, 0, ctypes.c_float(0.0), stream)
+    assert rc == 0
+    st = faulty_lib.sdpa_device_check()
+    assert st == 6, sd.STATUS_NAMES.get(st, st)   # SDPA_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 30.0
+    assert faulty_lib.sdpa_device_check() == 0
+    # the context still works: the product library's backward matches the oracle
+    dq, dk, dv = sd.attention_backward(qd, kd, vd, out, lse, dod, sd.SDPA_MASK_CAUSAL)
+    sd.sdpa_device_check()
+    rq, rk, rv = oracle.backward(q, k, v, do, sd.SDPA_MASK_CAUSAL)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert rel_err(host(got), ref) <= TOL_BF16

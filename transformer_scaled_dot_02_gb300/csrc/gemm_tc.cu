@@ -17,6 +17,7 @@
 // projection shape of the base and big models; 128-column tiles win only
 // when 256-column ones would leave half the SMs idle (the base model's
 // W^O, 4096 x 512 x 512).
+#include <atomic>
 #include <cstdlib>
 
 #include "kernels.h"
@@ -215,6 +216,26 @@ cudaError_t launch_bn(const GemmParams& p, int max_m, int max_n, cudaStream_t st
   return cudaGetLastError();
 }
 
+// SMs of the current device, read once per device.
+int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return 148;
+  }
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      return 148;
+    }
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 // Tile width: 256 columns, or 128 when 256-column tiles would not reach
 // half the SMs.  LIBSDPA_GEMM_BN = 256 | 128 pins it.
 int gemm_tile_n(const GemmParams& p) {
@@ -222,10 +243,7 @@ int gemm_tile_n(const GemmParams& p) {
     const int v = std::atoi(e);
     if (v == 256 || v == 128) return v;
   }
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-    sms = 148;
+  const int sms = sm_count();
   long long tiles = 0;
   for (int i = 0; i < p.num_problems; ++i)
     tiles += 1ll * ((p.prob[i].m + BM - 1) / BM) * ((p.prob[i].n + 255) / 256);

@@ -315,7 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       if (ok) {
         issue_s(0, false);
         issue_s(0, true);
+#ifndef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
         mma_commit_warp(s_full);
+#endif
+        // (test builds only, never in libsdpa.so: the first S^T / dP^T tile
+        // is never signalled, so the compute warps' bounded wait runs out and
+        // every other role leaves through the abort flag or its own limit)
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int b = it & 1;
