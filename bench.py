@@ -8,10 +8,16 @@ attention forward TFLOP/s with 4 b h n_q n_k d_k FLOP per pass, halved for the
 causal mask, whole job (all ranks).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload long_causal|restricted|decode|wide512|backward]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (no data-path collective); the timed region is bracketed by a barrier and the
 maximum over ranks is reported.  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload on the host cores (rank 0 only).
+
+`--workload` other than the default measures one of the widened rows with the
+same JSON line (value, roofline, e2e, clocks, an oracle baseline on a bounded
+sample): restricted self-attention (r = 1024), one decoding step against
+8192-token caches, Table 3's single 512-wide head, and the backward pass.
 """
 from __future__ import annotations
 
@@ -325,6 +331,263 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------ the widened rows (--workload)
+ROW_WORKLOADS = ("restricted", "decode", "wide512", "backward")
+
+
+def _visible_restricted(w, rows):
+    """Keys each query row i sees under the causal mask and window r."""
+    i = rows % w.n_q
+    left = (w.window - 1) // 2
+    return np.minimum(i, left) + 1
+
+
+def _time_steps(step, args, stream, pg, dev, local):
+    """W warm-up steps, then K steps between a barrier and a synchronize on
+    both sides, with an event pair around each step on the launching stream."""
+    import torch
+    import transformer_scaled_dot_02_gb300 as sd
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    sd.sdpa_device_check()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    with sampler:
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    sd.sdpa_device_check()
+    total = max_over_ranks(t0.elapsed_time(t1), pg, dev)
+    return total, [a.elapsed_time(b) for a, b in zip(starts, ends)], sampler.summary()
+
+
+def _time_e2e(e2e_step, args, stream, pg, dev):
+    import torch
+    import transformer_scaled_dot_02_gb300 as sd
+    steps = max(1, min(args.steps, 20))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    sd.sdpa_device_check()
+    return max_over_ranks(e0.elapsed_time(e1), pg, dev), steps
+
+
+def _pinned(a, dtype):
+    import torch
+    return torch.from_numpy(a).to(dtype).pin_memory()
+
+
+def run_row(args, world, rank, local):
+    """One of the widened rows: restricted, decode, wide512 or backward."""
+    import torch
+    import transformer_scaled_dot_02_gb300 as sd
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    sd.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    bf = torch.bfloat16
+    kind = args.workload
+    peaks, peak_src = load_peaks()
+
+    if kind == "backward":
+        w = synthetic.WORKLOADS["long_causal"]
+    else:
+        w = synthetic.WORKLOADS[{"restricted": "long_restricted", "decode": "decode_big",
+                                 "wide512": "wide_d512"}[kind]]
+    q, k, v, _ = synthetic.sdpa_inputs(w)
+    hq, hk, hv = _pinned(q, bf), _pinned(k, bf), _pinned(v, bf)
+    qd, kd, vd = hq.to(dev), hk.to(dev), hv.to(dev)
+    od = torch.empty((w.b, w.h, w.n_q, w.d_v), dtype=bf, device=dev)
+    ho = torch.empty(od.shape, dtype=bf).pin_memory()
+    bh = w.b * w.h
+
+    if kind in ("restricted", "wide512"):
+        r = w.window
+
+        def step():
+            if r:
+                sd.sdpa_forward_restricted(qd, kd, vd, od, w.b, w.h, w.n_q, w.n_k, w.d_k, w.d_v,
+                                           w.mask_kind, None, r, 0.0, sp)
+            else:
+                sd.sdpa_forward(qd, kd, vd, od, w.b, w.h, w.n_q, w.n_k, w.d_k, w.d_v,
+                                w.mask_kind, None, 0.0, sp)
+
+        ins, outs = [(qd, hq), (kd, hk), (vd, hv)], [(ho, od)]
+        if r:
+            all_rows = np.arange(bh * w.n_q, dtype=np.int64)
+            work = float(np.sum(4.0 * w.d_k * _visible_restricted(w, all_rows)))
+            metric = "restricted self-attention fwd TFLOP/s over visible pairs (1 GPU)"
+            desc = ("restricted causal self-attention b4 h16 n8192 d128 bf16, window r=%d "
+                    "(keys i-(r-1)/2 .. i)" % r)
+            kernel = "sdpa_fwd_one_tile<128>"
+        else:
+            work = metric_flops(w)
+            metric = "attention fwd TFLOP/s, one 512-wide head (Table 3 row A) (1 GPU)"
+            desc = "long causal self-attention b4 h1 n8192 d_k=d_v=512 bf16"
+            kernel = "sdpa_fwd_one_tile<512>"
+        unit, bound, peak = "TFLOP/s", "tensor", float(peaks["bf16_tflops"])
+        launches = 1
+        # every row of the workload: a few seconds of the fp64 oracle
+        sample_rows = min(args.cpu_rows or bh * w.n_q, bh * w.n_q)
+
+        def oracle_sample():
+            import oracle
+            threads = oracle.default_threads()
+            rows = _sample_rows(w, sample_rows, 99)
+            t = time.perf_counter()
+            oracle.sdpa(q, k, v, w.mask_kind, None, rows=rows, threads=threads, window=r or None)
+            dt = time.perf_counter() - t
+            i = rows % w.n_q
+            vis = _visible_restricted(w, rows) if r else (i + 1)
+            return (float(np.sum(4.0 * w.d_k * vis)) / dt / 1e12, threads,
+                    "%d of the %d query rows of the workload (fp64 C oracle, %.1f s)"
+                    % (len(rows), bh * w.n_q, dt))
+    elif kind == "decode":
+        ws_bytes = sd.sdpa_decode_workspace_size(w.b, w.h, w.n_q, w.n_k, w.d_v)
+        ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device=dev)
+
+        def step():
+            sd.sdpa_decode(qd, kd, vd, od, ws, ws.numel(), w.b, w.h, w.n_q, w.n_k, w.d_k, w.d_v,
+                           None, 0.0, sp)
+
+        # a serving loop keeps the caches resident: each step brings in the new
+        # queries and reads back their outputs
+        ins, outs = [(qd, hq)], [(ho, od)]
+        work = 2.0 * bh * w.n_k * (w.d_k + w.d_v)    # K and V caches, bf16, read once
+        metric = "decode step: K/V cache read GB/s (1 GPU)"
+        desc = "one decoding step, b32 h16, 1 query against 8192-token K/V caches, d128 bf16"
+        kernel = "sdpa_decode_split + sdpa_decode_combine"
+        unit, bound, peak = "GB/s", "hbm", float(peaks["hbm_gbs"])
+        launches = 2
+        sample_rows = min(args.cpu_rows or bh * w.n_q, bh * w.n_q)   # every (sequence, head)
+
+        def oracle_sample():
+            import oracle
+            threads = oracle.default_threads()
+            rows = np.sort(np.random.default_rng(99).choice(bh * w.n_q, size=sample_rows,
+                                                            replace=False)).astype(np.int64)
+            t = time.perf_counter()
+            oracle.decode(q, k, v, None, rows=rows, threads=threads)
+            dt = time.perf_counter() - t
+            return (2.0 * len(rows) * w.n_k * (w.d_k + w.d_v) / dt / 1e9, threads,
+                    "%d of the %d (sequence, head) decode rows (fp64 C oracle, %.1f s)"
+                    % (len(rows), bh * w.n_q, dt))
+    else:   # backward
+        do = synthetic.dout_input(w)
+        hdo = _pinned(do, bf)
+        dod = hdo.to(dev)
+        fwd_out, lse = sd.attention_with_lse(qd, kd, vd, w.mask_kind)
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        hlse.copy_(lse)
+        hfo = torch.empty(fwd_out.shape, dtype=bf).pin_memory()
+        hfo.copy_(fwd_out)
+        grads = [torch.empty_like(x) for x in (qd, kd, vd)]
+        hgrads = [torch.empty(x.shape, dtype=bf).pin_memory() for x in grads]
+        ws = torch.empty(sd.sdpa_backward_workspace_size(w.b, w.h, w.n_q, w.d_k),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            sd.sdpa_backward(qd, kd, vd, fwd_out, dod, lse, *grads, ws, ws.numel(), w.b, w.h,
+                             w.n_q, w.n_k, w.d_k, w.d_v, w.mask_kind, None, 0, 0.0, sp)
+
+        ins = [(qd, hq), (kd, hk), (vd, hv), (fwd_out, hfo), (dod, hdo), (lse, hlse)]
+        outs = list(zip(hgrads, grads))
+        work = 2.0 * bh * w.n_q * w.n_k * (3 * w.d_k + 2 * w.d_v) / 2
+        metric = "attention backward TFLOP/s (dQ, dK, dV: five products) (1 GPU)"
+        desc = "backward of long causal self-attention b4 h16 n8192 d128 bf16"
+        kernel = "sdpa_bwd_tc_n64<128, 128> (with its prep and convert kernels)"
+        unit, bound, peak = "TFLOP/s", "tensor", float(peaks["bf16_tflops"])
+        launches = 3
+        prefix = min(args.cpu_rows or w.n_q, w.n_q)   # one whole head of the workload
+
+        def oracle_sample():
+            import oracle
+            threads = oracle.default_threads()
+            sl = (slice(0, 1), slice(0, 1), slice(0, prefix))
+            t = time.perf_counter()
+            oracle.backward(q[sl], k[sl], v[sl], do[sl], w.mask_kind, threads=threads)
+            dt = time.perf_counter() - t
+            flops = 2.0 * prefix * prefix * (3 * w.d_k + 2 * w.d_v) / 2
+            what = ("one whole head of the workload" if prefix == w.n_q else
+                    "the first %d query and key rows of one head: itself a causal problem" % prefix)
+            return flops / dt / 1e12, threads, "%s (fp64 C oracle, %.1f s)" % (what, dt)
+
+    total_ms, launch_ms, clocks = _time_steps(step, args, stream, pg, dev, local)
+
+    def e2e_step():
+        for dst, src in ins:
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in outs:
+            dst.copy_(src, non_blocking=True)
+
+    e2e_ms, e2e_steps = _time_e2e(e2e_step, args, stream, pg, dev)
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    value = world * work * args.steps / (total_ms * 1e-3) / scale
+    mean_ms = float(np.mean(launch_ms))
+    achieved = work / (mean_ms * 1e-3) / scale
+    line = {
+        "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": desc, "b": w.b, "h": w.h, "n_q": w.n_q, "n_k": w.n_k,
+                   "d_k": w.d_k, "d_v": w.d_v, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4),
+                     "peak_source": "%s %s" % (peak_src, "hbm_gbs" if bound == "hbm"
+                                               else "bf16_tflops (burst)"),
+                     "traffic": None, "kernel": kernel,
+                     "launch_ms_mean": round(mean_ms, 4),
+                     "launch_ms_min": round(float(np.min(launch_ms)), 4)},
+        "e2e": {"value": round(world * work * e2e_steps / (e2e_ms * 1e-3) / scale, 3), "unit": unit,
+                "h2d_bytes_per_step": int(sum(d.numel() * d.element_size() for d, _ in ins)),
+                "d2h_bytes_per_step": int(sum(d.numel() * d.element_size() for d, _ in outs)),
+                "steps": e2e_steps, "path": "pinned host inputs copied in, the C-ABI call, "
+                                            "outputs copied back, one stream"},
+        "gpu_launches": args.steps * launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, threads, sample = oracle_sample()
+        line["cpu_baseline"] = {"value": val, "unit": unit, "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------- oracle timing
 def _sample_rows(w, n_rows, seed):
     rng = np.random.default_rng(seed)
@@ -395,18 +658,27 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=32768,
-                    help="query rows in the oracle's timed CPU sample")
+    ap.add_argument("--workload", choices=("long_causal",) + ROW_WORKLOADS, default="long_causal",
+                    help="the headline workload, or one of the widened rows")
+    ap.add_argument("--cpu-rows", type=int, default=None,
+                    help="size of the oracle's timed CPU sample (query rows; the backward: "
+                         "a causal prefix length)")
     ap.add_argument("--ref-rows", type=int, default=2048,
                     help="query rows per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.impl == "reference" and args.workload != "long_causal":
+        ap.error("the reference arm runs the default workload")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+    elif args.workload != "long_causal":
+        run_row(args, world, rank, local)
     else:
+        if args.cpu_rows is None:
+            args.cpu_rows = 32768
         run_ours(args, world, rank, local)
 
 

@@ -24,7 +24,7 @@ MASK_PADDING = 2
 
 # Stream ids inside one config's seed.
 _STREAM = {"q": 1, "k": 2, "v": 3, "xq": 4, "xkv": 5, "wq": 6, "wk": 7,
-           "wv": 8, "wo": 9, "len": 10}
+           "wv": 8, "wo": 9, "len": 10, "dout": 11}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -42,6 +42,7 @@ class Workload:
     len_range: tuple | None = None   # key-padding lengths, closed range
     d_model: int | None = None       # set for the multi-head (projection) form
     seed: int = 0
+    window: int = 0                  # r of restricted self-attention (0: none)
 
     @property
     def causal(self) -> bool:
@@ -60,6 +61,13 @@ WORKLOADS = {
                           len_range=(192, 384), d_model=1024, seed=1003),
     "long_causal": Workload("long_causal", 4, 16, 8192, 8192, 128, 128, MASK_CAUSAL, "bf16",
                             value_scale=0.5, seed=1004),
+    # the widened rows: restricted self-attention (section 4's r), one
+    # decoding step against 8192-token caches, and Table 3's single 512-wide head
+    "long_restricted": Workload("long_restricted", 4, 16, 8192, 8192, 128, 128, MASK_CAUSAL,
+                                "bf16", value_scale=0.5, seed=1005, window=1024),
+    "decode_big": Workload("decode_big", 32, 16, 1, 8192, 128, 128, MASK_NONE, "bf16", seed=1006),
+    "wide_d512": Workload("wide_d512", 4, 1, 8192, 8192, 512, 512, MASK_CAUSAL, "bf16",
+                          value_scale=0.5, seed=1007),
 }
 
 
@@ -105,6 +113,14 @@ def sdpa_inputs(w: Workload, seed: int | None = None, b: int | None = None, h: i
     v = normal(s, "v", (b, h, w.n_k, w.d_v), w.value_scale, w.dtype)
     lens = kv_lengths(dataclasses.replace(w, seed=s), b)
     return q, k, v, lens
+
+
+def dout_input(w: Workload, seed: int | None = None, b: int | None = None, h: int | None = None,
+               n_q: int | None = None) -> np.ndarray:
+    """Upstream gradient dO [b,h,n_q,d_v] ~ N(0,1) in the workload's storage type."""
+    s = w.seed if seed is None else seed
+    return normal(s, "dout", (w.b if b is None else b, w.h if h is None else h,
+                              w.n_q if n_q is None else n_q, w.d_v), 1.0, w.dtype)
 
 
 def mha_inputs(w: Workload, seed: int | None = None):
