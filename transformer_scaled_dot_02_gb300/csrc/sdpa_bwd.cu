@@ -81,6 +81,7 @@ constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
 // dQ^T = K^T dS^T always with M = 128 lanes of d: for d_k < 128 the upper lanes
 // read the tiles that follow K in shared memory and are discarded.
 constexpr uint32_t kIdescQ = idesc_bf16(128, kBN, true, true);
+constexpr uint32_t kIdescQ2 = idesc_bf16(128, 2 * kBN, true, true);   // a pair of steps
 // dS^T rows are 128 bytes (64 queries): 128-byte swizzle, 8-row groups 1024 apart
 constexpr uint32_t kDsHi = (1024u >> 4) | (1u << 14) | (2u << 29);
 
@@ -107,19 +108,26 @@ struct Lay {
 
 // Shared memory and tensor memory of one CTA for key size DK and value
 // size DV.  Tensor memory: the two score buffers (256 columns), dV at 256
-// (DV columns), dK at 256 + DV (DK columns).
+// (DV columns), dK at 256 + DV (DK columns).  When DK + DV <= 128 the last
+// 128 columns are free: dQ^T then goes there, one product of N = 128 per
+// pair of query steps (four dS^T buffers, so that a pair's two are
+// adjacent) instead of one N = 64 product per step into the dP^T half.
 template <int DK, int DV>
 struct Cfg {
   using LK = Lay<DK>;
   using LV = Lay<DV>;
+  static constexpr bool kPairDq = DK + DV <= 128;
+  static constexpr int kDsBufs = kPairDq ? 4 : 2;
+  static constexpr int kDqRows = kPairDq ? 2 * kBN : kBN;   // staged dQ rows per epilogue warp
+  static constexpr uint32_t kDqCol = 384;                   // paired dQ^T: 128 columns
   static constexpr int kDCols = DK < 32 ? DK : 32;          // dQ columns per epilogue warp
   static constexpr int kKOff = 0;
   static constexpr int kVOff = LK::kKVTile;
   static constexpr int kStageOff = kVOff + LV::kKVTile;     // Q then dO, per stage
   static constexpr int kStageBytes = LK::kQTile + LV::kQTile;
-  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;   // two dS^T buffers
-  static constexpr int kStagingOff = kDsOff + 2 * kDsTile;  // 4 warps x [64][kDCols] fp32
-  static constexpr int kVecOff = kStagingOff + 4 * kBN * kDCols * 4;
+  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;   // dS^T buffers
+  static constexpr int kStagingOff = kDsOff + kDsBufs * kDsTile;  // 4 warps x [kDqRows][kDCols] fp32
+  static constexpr int kVecOff = kStagingOff + 4 * kDqRows * kDCols * 4;
   static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescDV = idesc_bf16(kBM, DV, false, true);  // dV (A in TMEM)
@@ -127,7 +135,7 @@ struct Cfg {
   static constexpr uint32_t kDkCol = 256 + DV;
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
-  static_assert(kDkCol + DK <= 512, "tensor memory");
+  static_assert(kDkCol + DK <= (kPairDq ? kDqCol : 512u), "tensor memory");
   // dQ^T's 128 lanes read 128 / kBoxCols boxes from K onward: all inside the CTA's memory
   static_assert((128 / LK::kBoxCols) * LK::kKVBox <= kBarOff, "dQ^T reads in bounds");
 };
@@ -331,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
           tc_fence_after();
           issue_s(nx, false);
           // dP^T(it+1) lands where dQ^T(it-1) was: its epilogue must have read it
-          if (it >= 1) {
+          // (paired dQ^T has columns of its own)
+          if (!C::kPairDq && it >= 1) {
             ok = mbar_wait_warp(dq_empty + (nx & 1), static_cast<uint32_t>((it - 1) >> 1) & 1u, ab);
             if (!ok) break;
             tc_fence_after();
@@ -358,16 +367,42 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
                            C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit_warp(q_empty + it % kStages);
-        // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
-        const uint32_t ak = lo(k_smem, LK::kKVBox), bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
+        const uint32_t ak = lo(k_smem, LK::kKVBox);
+        if constexpr (C::kPairDq) {
+          // dQ^T of steps (it-1, it) at odd it, or of a last step alone:
+          // K_j^T [dS^T(it-1) | dS^T(it)] into columns kDqCol .. +128
+          const bool last = it + 1 == n_it;
+          if ((it & 1) || last) {
+            const int grp = it >> 1;
+            if (grp >= 1) {
+              ok = mbar_wait_warp(dq_empty, static_cast<uint32_t>(grp - 1) & 1u, ab);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const int first = (it & 1) ? it - 1 : it;
+            const uint32_t bds = lo(smem_base + C::kDsOff + (first & 3) * kDsTile, kDsTile);
+            const uint32_t idq = (it & 1) ? kIdescQ2 : kIdescQ;
 #pragma unroll
-        for (int k = 0; k < kBM / 16; ++k) {
-          const uint32_t ka = static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4;  // 16 key rows of K
-          const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;            // of dS^T
-          mma_bf16_ss_warp(buf + 64, ak + ka, LK::kDescHi, bds + kb, kDsHi, kIdescQ,
-                           k > 0 ? 1u : 0u);
+            for (int k = 0; k < kBM / 16; ++k) {
+              const uint32_t ka = static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4;
+              const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;
+              mma_bf16_ss_warp(tmem + C::kDqCol, ak + ka, LK::kDescHi, bds + kb, kDsHi, idq,
+                               k > 0 ? 1u : 0u);
+            }
+            mma_commit_warp(dq_full);
+          }
+        } else {
+          // dQ^T(it) = K_j^T dS^T(it): 16 keys per step, into the dP^T half of buffer b
+          const uint32_t bds = lo(smem_base + C::kDsOff + b * kDsTile, kDsTile);
+#pragma unroll
+          for (int k = 0; k < kBM / 16; ++k) {
+            const uint32_t ka = static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4;  // 16 key rows of K
+            const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;            // of dS^T
+            mma_bf16_ss_warp(buf + 64, ak + ka, LK::kDescHi, bds + kb, kDsHi, kIdescQ,
+                             k > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(dq_full + b);
         }
-        mma_commit_warp(dq_full + b);
       }
       if (ok) mma_commit_warp(acc_full);
       mma_commit_warp(drain);
@@ -381,36 +416,77 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     // reduce; rows past n_q are clipped by the copy engine.
     const int quarter = warp & 3;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff) + quarter * (kBN * C::kDCols);
+    float* staging = reinterpret_cast<float*>(smem + C::kStagingOff) + quarter * (C::kDqRows * C::kDCols);
     const bool active = quarter * 32 < DK;   // lanes 32 q .. are d values only below d_k
-    for (int j = 0; j < n_it; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
-      tc_fence_after();
-      uint32_t g0[32], g1[32];
-      tmem_ld32(lane_base + static_cast<uint32_t>(b * 128 + 64), g0);
-      tmem_ld32(lane_base + static_cast<uint32_t>(b * 128 + 96), g1);
+    // Stages 64 query rows (two 32-column TMEM loads from `col`) at row `row0`
+    // of this warp's staging tile.
+    auto load_half = [&](uint32_t col, uint32_t (&g0)[32], uint32_t (&g1)[32]) {
+      tmem_ld32(lane_base + col, g0);
+      tmem_ld32(lane_base + col + 32, g1);
       tmem_ld_wait();
       reg_fence(g0);
       reg_fence(g1);
-      tc_fence_before();
-      mbar_arrive(dq_empty + b);
-      if (!active) continue;
-      // this warp's previous reduce has finished reading the staging tile
-      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      __syncwarp();
+    };
+    auto stage_half = [&](int row0, const uint32_t (&g0)[32], const uint32_t (&g1)[32]) {
       if (lane < C::kDCols) {
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          staging[e * C::kDCols + lane] = __uint_as_float(g0[e]);
-          staging[(32 + e) * C::kDCols + lane] = __uint_as_float(g1[e]);
+          staging[(row0 + e) * C::kDCols + lane] = __uint_as_float(g0[e]);
+          staging[(row0 + 32 + e) * C::kDCols + lane] = __uint_as_float(g1[e]);
         }
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_3d(&p.tm_dq, staging, quarter * 32, (i_lo + j) * kBN, bh);
-        tma_store_commit();
+    };
+    if constexpr (C::kPairDq) {
+      // one group per pair of steps (the last may be a single step)
+      for (int grp = 0; 2 * grp < n_it; ++grp) {
+        const bool two = 2 * grp + 1 < n_it;
+        if (!mbar_wait_warp(dq_full, static_cast<uint32_t>(grp) & 1u, ab)) break;
+        tc_fence_after();
+        uint32_t g0[32], g1[32];
+        load_half(C::kDqCol, g0, g1);
+        if (active) {
+          // this warp's previous reduces have finished reading the staging tile
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+          stage_half(0, g0, g1);
+        }
+        if (two) {
+          load_half(C::kDqCol + 64, g0, g1);
+          if (active) stage_half(kBN, g0, g1);
+        }
+        tc_fence_before();
+        mbar_arrive(dq_empty);
+        if (!active) continue;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&p.tm_dq, staging, quarter * 32, (i_lo + 2 * grp) * kBN, bh);
+          if (two)
+            tma_reduce_add_3d(&p.tm_dq, staging + kBN * C::kDCols, quarter * 32,
+                              (i_lo + 2 * grp + 1) * kBN, bh);
+          tma_store_commit();
+        }
+      }
+    } else {
+      for (int j = 0; j < n_it; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
+        tc_fence_after();
+        uint32_t g0[32], g1[32];
+        load_half(static_cast<uint32_t>(b * 128 + 64), g0, g1);
+        tc_fence_before();
+        mbar_arrive(dq_empty + b);
+        if (!active) continue;
+        // this warp's previous reduce has finished reading the staging tile
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        stage_half(0, g0, g1);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&p.tm_dq, staging, quarter * 32, (i_lo + j) * kBN, bh);
+          tma_store_commit();
+        }
       }
     }
     if (lane == 0) bulk_wait_all();   // this warp's last reduce has finished
@@ -483,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       tmem_st16(lane_base + s_col, pk);
       tmem_st16(lane_base + s_col + 64, dk);
       // dS^T row r, queries [32 half, +32): 16-byte chunks 4 half .. +4 of the 128-byte row
-      uint8_t* dsb = smem + C::kDsOff + b * kDsTile;
+      uint8_t* dsb = smem + C::kDsOff + (it & (C::kDsBufs - 1)) * kDsTile;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint4 v = make_uint4(dk[c * 4 + 0], dk[c * 4 + 1], dk[c * 4 + 2], dk[c * 4 + 3]);
