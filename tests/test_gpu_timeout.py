@@ -46,12 +46,15 @@ def faulty_lib():
     return sd.load_library(lib_path)
 
 
-@pytest.mark.parametrize("kernel", ["two_tile", "one_tile"])
-def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, monkeypatch):
+@pytest.mark.parametrize("kernel,d", [("two_tile", 64), ("one_tile", 64), ("one_tile", 512)])
+def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, d, monkeypatch):
+    """d = 512 runs the one-tile kernel's single-stage path (K in two
+    halves): its producer also waits on the withheld commit and must drain
+    its own copies before the CTA leaves."""
     import torch
     monkeypatch.setenv("LIBSDPA_ATTENTION_KERNEL", kernel)
     rng = np.random.default_rng(1)
-    b, h, n, d = 1, 1, 128, 64   # one CTA, one query tile
+    b, h, n = 1, 1, 128   # one query tile (two CTAs at d = 512, one per half of d_v)
     q = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
     qd = dev(q)
     out = torch.zeros((b, h, n, d), dtype=torch.bfloat16, device="cuda")
