@@ -220,8 +220,10 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
                                 Strides sv, Strides so, int mask_kind, const int32_t* kv_lengths,
                                 float scale, unsigned* status, cudaStream_t stream,
                                 int win_left = sdpa::kWindowUnbounded,
-                                int win_right = sdpa::kWindowUnbounded, float* lse = nullptr) {
+                                int win_right = sdpa::kWindowUnbounded, float* lse = nullptr,
+                                bool pdl = false) {
   SdpaTcParams p;
+  p.pdl = pdl ? 1 : 0;
   // The one-tile kernel (one 128-row query tile per CTA, 32- or 64-key tiles;
   // two or four CTAs per SM at d <= 128) takes wide heads, small heads, and
   // the short key walks where the two-tile kernel's longer per-CTA chain
@@ -546,15 +548,20 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
     return SDPA_ERR_CUDA;
 
   // Heads: strides of [b, n, h, d]; the output lands in Concat order.
+  // The attention and the W^O product each launch with a programmatic
+  // dependency on the kernel before them: their CTAs start, allocate and set
+  // up while that kernel's last CTAs finish, then wait for its results.
   st = launch_attention_tc(qp, kp, vp, op, b, h, n_q, n_k, d_k, d_v, bshd(h, n_q, d_k),
                            bshd(h, n_k, d_k), bshd(h, n_k, d_v), bshd(h, n_q, d_v), mask_kind,
-                           kv_lengths, scale, status, s);
+                           kv_lengths, scale, status, s, sdpa::kWindowUnbounded,
+                           sdpa::kWindowUnbounded, nullptr, true);
   if (st != SDPA_OK) return st;
 
   // Y = Concat(heads) W^O
   GemmParams go;
   go.status = status;
   go.num_problems = 1;
+  go.pdl = 1;
   if (!fill_gemm_problem(&go.prob[0], op, wo, y, m_q, d_model, h * d_v)) return SDPA_ERR_CUDA;
   return sdpa::launch_gemm_tc(go, m_q, d_model, s) == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }

@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every CTA holds its tensor memory now: the next kernel in the stream may
+  // launch; this grid's inputs may come from the previous one, so wait for it.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -212,8 +216,8 @@ cudaError_t launch_bn(const GemmParams& p, int max_m, int max_n, cudaStream_t st
   if (err != cudaSuccess) return err;
   dim3 grid((max_n + BN - 1) / BN, (max_m + BM - 1) / BM, p.num_problems);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-  gemm_bf16_tc<BN><<<grid, kThreads, GCfg<BN>::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(gemm_bf16_tc<BN>, grid, dim3(kThreads), GCfg<BN>::kSmemBytes, stream,
+                       p.pdl != 0, p);
 }
 
 // SMs of the current device, read once per device.

@@ -26,8 +26,33 @@ struct SdpaTcParams {
   // (kWindowUnbounded for plain attention).
   int win_left, win_right;
   float* lse;                 // optional [b, h, n_q] natural log-sum-exp per row
+  int pdl = 0;                // launched with a programmatic dependency on the previous kernel
 };
 constexpr int kWindowUnbounded = 1 << 30;
+
+// Launches `kernel` on `stream`; with `pdl` it may start (and run its set-up)
+// while the previous kernel in the stream finishes: the kernels call
+// griddep_launch_dependents() once their tensor memory is allocated and
+// griddep_wait() before touching global memory the previous kernel writes.
+template <typename Params>
+inline cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, const Params& p) {
+  if (!pdl) {
+    kernel<<<grid, block, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 // Two query tiles per CTA; (d_k, d_v) in {(16,16), (32,32), (64,64), (128,128), (16,64), (32,64)}.
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int d_k, int d_v, cudaStream_t stream);
 // One 128-row query tile per CTA (d = 64, 128, 256, 512); K/V boxes of
@@ -101,6 +126,7 @@ struct GemmParams {
   GemmProblem prob[3];
   int num_problems;
   unsigned* status;
+  int pdl = 0;                // launched with a programmatic dependency on the previous kernel
 };
 constexpr int kGemmBlockM = 128;
 cudaError_t launch_gemm_tc(const GemmParams& p, int max_m, int max_n, cudaStream_t stream);

@@ -170,6 +170,10 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   const int bi = bh / p.h;
   const int hi = bh % p.h;
   const bool causal = (p.mask_kind & 1) != 0;
+  // Read before griddep_wait(): with a programmatic dependency the lengths
+  // must not come from the kernel this one depends on.  The one such caller,
+  // mha_forward, launches this kernel after its projection GEMM, which never
+  // writes them.
   int kv_len = p.n_k;
   if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
     kv_len = p.kv_lengths[bi];
@@ -224,6 +228,10 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every CTA holds its tensor memory now: the next kernel in the stream may
+  // launch; this grid's inputs may come from the previous one, so wait for it.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp >= 8) {
    regs_decrease<kRegsControl>();
@@ -573,8 +581,8 @@ cudaError_t launch_impl(const SdpaTcParams& p, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  sdpa_fwd_bf16_tc<DK, DV><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(sdpa_fwd_bf16_tc<DK, DV>, dim3(static_cast<unsigned>(blocks)),
+                       dim3(kThreads), smem, stream, p.pdl != 0, p);
 }
 
 }  // namespace
