@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   const int bi = bh / p.h;
   const int hi = bh % p.h;
   const bool causal = (p.mask_kind & 1) != 0;
+  // Read before griddep_wait(): the lengths are the caller's input, which the
+  // prep kernel this one may depend on never writes.
   int kv_len = p.n_k;
   if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
     kv_len = p.kv_lengths[bi];
@@ -252,6 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Every CTA holds its tensor memory now: the convert kernel may launch;
+  // the prep kernel's vectors and zeroed accumulator must be complete.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == kProducerWarp) {
     if (lane == 0 && n_it > 0) {
@@ -628,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 // DK / (DV / 8) of the row's fp32 dQ accumulator.
 template <int DK, int DV>
 __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
+  griddep_launch_dependents();   // the main kernel may start its set-up now
   constexpr int kLanes = DV / 8;
   constexpr int kRowsPerBlock = 256 / kLanes;
   constexpr int kZero = DK / kLanes;   // 2, 4 or 8 accumulator floats per lane
@@ -669,6 +676,7 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
 // dQ = scale * accumulator in bf16, 8 elements per thread.
 template <int D>
 __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const SdpaBwdPrepParams p) {
+  griddep_wait();   // the main kernel's reduces into the accumulator are complete
   const long long idx = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) * 8;
   const long long n = static_cast<long long>(p.b) * p.h * p.n_q * D;
   if (idx >= n) return;
@@ -686,7 +694,12 @@ template <int DK, int DV>
 cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
   const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
   cudaError_t err = cudaSuccess;
-  if (rows > 0) {
+  // The main kernel launches with a programmatic dependency on the prep
+  // kernel, and the convert kernel on the main one, whenever that kernel was
+  // launched: each starts while its predecessor's last CTAs finish and waits
+  // (griddep_wait) before reading what it wrote.
+  const bool prep = rows > 0;
+  if (prep) {
     constexpr long long kRowsPerBlock = 256 / (DV / 8);
     sdpa_bwd_prep<DK, DV><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256,
                             0, stream>>>(pp);
@@ -699,14 +712,15 @@ cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cud
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
   if (blocks > 0) {
-    n64::sdpa_bwd_tc_n64<DK, DV><<<static_cast<unsigned>(blocks), n64::kThreads, smem, stream>>>(bp);
-    err = cudaGetLastError();
+    err = launch_kernel(n64::sdpa_bwd_tc_n64<DK, DV>, dim3(static_cast<unsigned>(blocks)),
+                        dim3(n64::kThreads), smem, stream, prep, bp);
     if (err != cudaSuccess) return err;
   }
   const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * DK;
   if (n > 0)
-    sdpa_bwd_dq_convert<DK><<<static_cast<unsigned>((n / 8 + 255) / 256), 256, 0, stream>>>(pp);
-  return cudaGetLastError();
+    return launch_kernel(sdpa_bwd_dq_convert<DK>, dim3(static_cast<unsigned>((n / 8 + 255) / 256)),
+                         dim3(256), 0, stream, blocks > 0, pp);
+  return cudaSuccess;
 }
 
 }  // namespace
