@@ -92,6 +92,7 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
 
 template <int D, int MAXQ>
 __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const DecodeParams p) {
+  griddep_launch_dependents();   // the combine kernel may launch now
   constexpr int C = D / 32;
   __shared__ float sm_m[kDecWarps][MAXQ], sm_l[kDecWarps][MAXQ];
   __shared__ float sm_o[kDecWarps][MAXQ][D];
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const DecodePar
 
 template <int D>
 __global__ void __launch_bounds__(D) sdpa_decode_combine(const DecodeParams p) {
+  griddep_wait();   // every split's partial results are complete
   const long long row = blockIdx.x;
   const int col = threadIdx.x;
   const long long rows = static_cast<long long>(p.b) * p.h * p.n_q;
@@ -246,8 +248,9 @@ cudaError_t launch_d(const DecodeParams& p, cudaStream_t stream) {
   else if (p.n_q <= 4) err = launch_split<D, 4>(p, stream);
   else err = launch_split<D, 8>(p, stream);
   if (err != cudaSuccess || p.splits == 1) return err;
-  sdpa_decode_combine<D><<<static_cast<unsigned>(p.b * p.h * p.n_q), D, 0, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependency on the split kernel just launched
+  return launch_kernel(sdpa_decode_combine<D>, dim3(static_cast<unsigned>(p.b * p.h * p.n_q)),
+                       dim3(D), 0, stream, true, p);
 }
 
 }  // namespace
