@@ -214,14 +214,17 @@ Strides bhsd(int h, int n, int d) { return {d, 1ll * n * d, 1ll * h * n * d}; }
 Strides bshd(int h, int n, int d) { return {1ll * h * d, d, 1ll * n * h * d}; }
 
 // Launches the tensor-core attention over tensors with arbitrary (n, h, b)
-// element strides (BHSD for sdpa_forward, BSHD inside mha_forward).
+// element strides (BHSD for sdpa_forward, BSHD inside mha_forward).  The
+// launch carries a programmatic dependency on the previous kernel in the
+// stream: the CTAs may start and set up early, and read or write global
+// memory only after griddep_wait(), so any predecessor stays safe.
 sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, void* out, int b,
                                 int h, int n_q, int n_k, int d_k, int d_v, Strides sq, Strides sk,
                                 Strides sv, Strides so, int mask_kind, const int32_t* kv_lengths,
                                 float scale, unsigned* status, cudaStream_t stream,
                                 int win_left = sdpa::kWindowUnbounded,
                                 int win_right = sdpa::kWindowUnbounded, float* lse = nullptr,
-                                bool pdl = false) {
+                                bool pdl = true) {
   SdpaTcParams p;
   p.pdl = pdl ? 1 : 0;
   // The one-tile kernel (one 128-row query tile per CTA, 32- or 64-key tiles;
@@ -549,8 +552,9 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
 
   // Heads: strides of [b, n, h, d]; the output lands in Concat order.
   // The attention and the W^O product each launch with a programmatic
-  // dependency on the kernel before them: their CTAs start, allocate and set
-  // up while that kernel's last CTAs finish, then wait for its results.
+  // dependency on the kernel before them (as every attention launch does):
+  // their CTAs start, allocate and set up while that kernel's last CTAs
+  // finish, then wait for its results before reading anything.
   st = launch_attention_tc(qp, kp, vp, op, b, h, n_q, n_k, d_k, d_v, bshd(h, n_q, d_k),
                            bshd(h, n_k, d_k), bshd(h, n_k, d_v), bshd(h, n_q, d_v), mask_kind,
                            kv_lengths, scale, status, s, sdpa::kWindowUnbounded,

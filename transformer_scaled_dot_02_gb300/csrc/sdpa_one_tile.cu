@@ -149,29 +149,6 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   const int bi = bh / p.h;
   const int hi = bh % p.h;
   const bool causal = (p.mask_kind & 1) != 0;
-  // Read before griddep_wait(): with a programmatic dependency the lengths
-  // must not come from the kernel this one depends on.  The one such caller,
-  // mha_forward, launches this kernel after its projection GEMM, which never
-  // writes them.
-  int kv_len = p.n_k;
-  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
-    kv_len = p.kv_lengths[bi];
-    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
-  }
-  // key tiles [j_lo, j_hi) hold a key some row of the tile can see
-  const int qs = qb * kBlockM;
-  int j_lo = 0, j_hi = 0;
-  {
-    const int row_hi = min(qs + kBlockM, p.n_q) - 1;
-    const int key_lo = max(0, qs - p.win_left);
-    int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
-    if (causal) key_hi = min(key_hi, row_hi + 1);
-    if (key_hi > key_lo) {
-      j_lo = key_lo / BN;
-      j_hi = (key_hi + BN - 1) / BN;
-    }
-  }
-  const int n_kv = j_hi - j_lo;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -197,6 +174,27 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   // launch; this grid's inputs may come from the previous one, so wait for it.
   griddep_launch_dependents();
   griddep_wait();
+  // The key-padding lengths may come from the previous kernel in the
+  // stream: read them only after griddep_wait().
+  int kv_len = p.n_k;
+  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
+    kv_len = p.kv_lengths[bi];
+    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
+  }
+  // key tiles [j_lo, j_hi) hold a key some row of the tile can see
+  const int qs = qb * kBlockM;
+  int j_lo = 0, j_hi = 0;
+  {
+    const int row_hi = min(qs + kBlockM, p.n_q) - 1;
+    const int key_lo = max(0, qs - p.win_left);
+    int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
+    if (causal) key_hi = min(key_hi, row_hi + 1);
+    if (key_hi > key_lo) {
+      j_lo = key_lo / BN;
+      j_hi = (key_hi + BN - 1) / BN;
+    }
+  }
+  const int n_kv = j_hi - j_lo;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer

@@ -170,38 +170,6 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   const int bi = bh / p.h;
   const int hi = bh % p.h;
   const bool causal = (p.mask_kind & 1) != 0;
-  // Read before griddep_wait(): with a programmatic dependency the lengths
-  // must not come from the kernel this one depends on.  The one such caller,
-  // mha_forward, launches this kernel after its projection GEMM, which never
-  // writes them.
-  int kv_len = p.n_k;
-  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
-    kv_len = p.kv_lengths[bi];
-    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
-  }
-  // Query tile t covers rows [q0 + 128 t, q0 + 128 t + 128).  It needs the key
-  // tiles [lo_of(t), hi_of(t)): those holding at least one key that some
-  // row of the tile can see (causal, padding and restricted-window limits).
-  const int q0 = qb * 2 * kBlockM;
-  auto tile_range = [&](int t) -> int2 {
-    const int qs = q0 + t * kBlockM;
-    if (qs >= p.n_q) return make_int2(0, 0);
-    const int row_hi = min(qs + kBlockM, p.n_q) - 1;
-    int key_lo = max(0, qs - p.win_left);
-    int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
-    if (causal) key_hi = min(key_hi, row_hi + 1);
-    if (key_hi <= key_lo) return make_int2(0, 0);
-    return make_int2(key_lo / kBlockN, (key_hi + kBlockN - 1) / kBlockN);
-  };
-  const int2 range0 = tile_range(0), range1 = tile_range(1);
-  auto lo_of = [&](int t) { return t ? range1.x : range0.x; };
-  auto hi_of = [&](int t) { return t ? range1.y : range0.y; };
-  const bool has0 = range0.y > range0.x, has1 = range1.y > range1.x;
-  // the CTA walks key tiles [j_first, j_first + n_kv)
-  const int j_first = has0 ? (has1 ? min(range0.x, range1.x) : range0.x) : (has1 ? range1.x : 0);
-  const int j_end = has0 ? (has1 ? max(range0.y, range1.y) : range0.y) : (has1 ? range1.y : 0);
-  const int n_kv = j_end - j_first;
-  auto active = [&](int t, int j) { return j >= lo_of(t) && j < hi_of(t); };
 
   // ---- set-up: barriers (one thread), tensor memory (MMA warp)
   if (threadIdx.x == 0) {
@@ -232,6 +200,36 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   // launch; this grid's inputs may come from the previous one, so wait for it.
   griddep_launch_dependents();
   griddep_wait();
+  // The key-padding lengths may come from the previous kernel in the
+  // stream: read them only after griddep_wait().
+  int kv_len = p.n_k;
+  if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
+    kv_len = p.kv_lengths[bi];
+    kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
+  }
+  // Query tile t covers rows [q0 + 128 t, q0 + 128 t + 128).  It needs the key
+  // tiles [lo_of(t), hi_of(t)): those holding at least one key that some
+  // row of the tile can see (causal, padding and restricted-window limits).
+  const int q0 = qb * 2 * kBlockM;
+  auto tile_range = [&](int t) -> int2 {
+    const int qs = q0 + t * kBlockM;
+    if (qs >= p.n_q) return make_int2(0, 0);
+    const int row_hi = min(qs + kBlockM, p.n_q) - 1;
+    int key_lo = max(0, qs - p.win_left);
+    int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
+    if (causal) key_hi = min(key_hi, row_hi + 1);
+    if (key_hi <= key_lo) return make_int2(0, 0);
+    return make_int2(key_lo / kBlockN, (key_hi + kBlockN - 1) / kBlockN);
+  };
+  const int2 range0 = tile_range(0), range1 = tile_range(1);
+  auto lo_of = [&](int t) { return t ? range1.x : range0.x; };
+  auto hi_of = [&](int t) { return t ? range1.y : range0.y; };
+  const bool has0 = range0.y > range0.x, has1 = range1.y > range1.x;
+  // the CTA walks key tiles [j_first, j_first + n_kv)
+  const int j_first = has0 ? (has1 ? min(range0.x, range1.x) : range0.x) : (has1 ? range1.x : 0);
+  const int j_end = has0 ? (has1 ? max(range0.y, range1.y) : range0.y) : (has1 ? range1.y : 0);
+  const int n_kv = j_end - j_first;
+  auto active = [&](int t, int j) { return j >= lo_of(t) && j < hi_of(t); };
 
   if (warp >= 8) {
    regs_decrease<kRegsControl>();
