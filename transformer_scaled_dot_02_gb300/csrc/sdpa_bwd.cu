@@ -53,13 +53,17 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 //                write dK and dV.
 //   warp 8       TMA producer (K_j, V_j once; Q_i, dO_i, lse2, D in 3 stages).
 //   warp 9       MMA issuer (the whole warp; one elected lane issues each
-//                instruction), in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T(i).
-//   warps 10-13  dQ^T of each step out of tensor memory into the staging tile.
+//                instruction), in the order S(i+1), dP(i+1), dV(i), dK(i), dQ^T.
+//   warps 10-13  dQ^T out of tensor memory into the staging tile.
 // Tensor memory: buffer b = step & 1 holds S^T at 128 b (64 columns; P^T in
 // bf16 over columns 128 b + 32 h .. +16 of each half h) and dP^T at
-// 128 b + 64 (dS^T in bf16 the same way; then dQ^T = K^T dS^T, keyed by d),
-// dV at 256, dK at 256 + d_v.  dQ^T leaves through a 64 x d_k fp32 staging tile
-// and one bulk reduce-add into the fp32 dQ accumulator per step.
+// 128 b + 64 (dS^T in bf16 the same way), dV at 256, dK at 256 + d_v.
+// dQ^T = K^T dS^T (keyed by d):
+//   d_k + d_v > 128: one N = 64 product per step into the dP^T half of its
+//                buffer, drained through a 64 x d_k fp32 staging tile;
+//   d_k + d_v <= 128: one N = 128 product per pair of steps into columns
+//                384 .. 511, drained through a 128 x d_k staging tile.
+// Each 64 rows then go into the fp32 dQ accumulator by one bulk reduce-add.
 namespace n64 {
 
 constexpr int kBM = 128;                 // keys per CTA
