@@ -6,6 +6,7 @@ C ABI, for profiling a single kernel launch under a profiler.
     python -m transformer_scaled_dot_02_gb300.profile --decode --b 32 --h 16 --n 1 --nk 8192 --d 128
     python -m transformer_scaled_dot_02_gb300.profile --restricted 1024 --b 4 --h 16 --n 8192 --mask 1
     python -m transformer_scaled_dot_02_gb300.profile --backward --b 4 --h 16 --n 8192 --mask 1
+    python -m transformer_scaled_dot_02_gb300.profile --gemm 16384,4096,4096
 
 Inputs are seeded N(0,1) bf16 values made on the device; nothing is checked.
 Prints the mean call time measured with CUDA events after one warm-up call;
@@ -37,6 +38,7 @@ def main():
     ap.add_argument("--decode", action="store_true", help="one decoding step: --n new queries, --nk cache")
     ap.add_argument("--restricted", type=int, default=0, help="neighbourhood size r (restricted)")
     ap.add_argument("--backward", action="store_true", help="the gradients (after one forward)")
+    ap.add_argument("--gemm", default="", help="M,N,K: one projection Y = X W on its own")
     ap.add_argument("--d-model", type=int, default=512)
     ap.add_argument("--iters", type=int, default=3)
     a = ap.parse_args()
@@ -51,7 +53,16 @@ def main():
         lo = a.len_lo or n_k // 2
         lens = torch.randint(lo, n_k + 1, (a.b,), dtype=torch.int32, device=dev)
     sd.load_library()
-    if a.decode:
+    gemm_mnk = [int(x) for x in a.gemm.split(",")] if a.gemm else None
+    if gemm_mnk:
+        gm, gn, gk = gemm_mnk
+        x = (torch.randn(gm, gk, device=dev) * 0.1).to(torch.bfloat16)
+        w = (torch.randn(gk, gn, device=dev) * 0.1).to(torch.bfloat16)
+        y = torch.empty(gm, gn, dtype=torch.bfloat16, device=dev)
+
+        def run():
+            sd.linear_forward(x, w, y, gm, gn, gk)
+    elif a.decode:
         q = torch.randn(a.b, a.h, n_q, a.d, device=dev).to(torch.bfloat16)
         k = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
         v = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
@@ -107,7 +118,9 @@ def main():
     sd.sdpa_device_check()
     ms = s.elapsed_time(e) / a.iters
     line = "mean %.4f ms per call over %d calls" % (ms, a.iters)
-    if not (a.mha or a.decode or a.restricted):
+    if gemm_mnk:
+        line += ", %.1f TFLOP/s" % (2.0 * gm * gn * gk / (ms * 1e-3) / 1e12)
+    elif not (a.mha or a.decode or a.restricted):
         # 2 n_q n_k per unit of head size: S and O in the forward; S, dP, dV, dK, dQ in the backward
         units = 3 * a.d + 2 * d_v if a.backward else a.d + d_v
         flops = 2 * units * a.b * a.h * n_q * n_k * (0.5 if a.mask & 1 else 1)
