@@ -19,7 +19,11 @@
  *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream).  A successful return means the work was
  *     enqueued; errors detected on the host are returned before anything is
- *     enqueued.
+ *     enqueued.  The attention, projection, backward-convert and decode-
+ *     combine kernels launch with a programmatic dependency on the kernel
+ *     before them in the stream: they may start setting up while it
+ *     finishes, but read or write no global memory until it has completed,
+ *     so stream order is kept.
  *   - Masks (`mask_kind`, bit flags): SDPA_MASK_CAUSAL hides keys j > i (it
  *     requires n_q == n_k); SDPA_MASK_PADDING hides keys j >= kv_lengths[b]
  *     (`kv_lengths`: device int32 [b], values clamped into [0, n_k] on the
