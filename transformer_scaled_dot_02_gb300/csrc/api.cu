@@ -540,6 +540,7 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
   GemmParams gp;
   gp.status = status;
   gp.num_problems = 0;
+  gp.pdl = 1;   // the GEMM touches global memory only after griddep_wait()
   if (!fill_gemm_problem(&gp.prob[gp.num_problems++], xq, wq, qp, m_q, hd, d_model))
     return SDPA_ERR_CUDA;
   if (m_k > 0) {
@@ -583,6 +584,7 @@ sdpa_status linear_forward(const void* x, const void* w, void* y, int m, int n, 
   GemmParams gp;
   gp.status = status;
   gp.num_problems = 1;
+  gp.pdl = 1;
   if (!fill_gemm_problem(&gp.prob[0], x, w, y, m, n, k)) return SDPA_ERR_CUDA;
   return sdpa::launch_gemm_tc(gp, m, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SDPA_OK
