@@ -17,7 +17,9 @@
 //               past n).
 //   warp 9      MMA issuer (the whole warp; one elected lane issues each
 //               instruction): S_t = Q_t K_j^T into tensor memory,
-//               then O_t += P_t V_j with P_t read from tensor memory.
+//               then O_t += P_t V_j with P_t read from tensor memory, in
+//               parts of 64 keys: each starts as soon as the softmax has
+//               written that part of P_t.
 //   warps 10-11 idle (they complete the third warpgroup for the register split).
 //   warps 0-7   two softmax warpgroups, one per query tile, one thread per
 //               score row (TMEM lane = row): scale, mask, running max and
@@ -54,6 +56,10 @@ constexpr uint32_t kRegsSoftmax = 216;
 constexpr int kHeadGroup = 8;    // heads whose K/V share L2 at a time
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: a factor of 256
+// P_t is handed to the MMA warp in kPParts parts of kBlockN / kPParts keys;
+// O_t += P_t V_j starts on a part as soon as the softmax has written it.
+constexpr int kPParts = 2;
+constexpr int kPPartKeys = kBlockN / kPParts;
 
 // Layout of one operand whose rows hold D bf16 values (Q and K at d_k; V
 // and O at d_v).
@@ -90,7 +96,7 @@ struct Plan {
   static constexpr int kVEnd = kVOff + kVStages * CV::kTileBytes;
   static constexpr int kStageOff = kStageOverQ ? kQOff : kVEnd;
   static constexpr int kBarOff = kStageOverQ ? kVEnd : kVEnd + 2 * CV::kTileBytes;
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6 + 1;
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 6 + 2 * (kPParts - 1) + 1;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false, false);
   static constexpr uint32_t kIdescPV = idesc_bf16(kBlockM, DV, false, true);
@@ -104,6 +110,7 @@ struct Bars {
   uint64_t* v_full;
   uint64_t* v_empty;
   uint64_t* s_full;   // [2]
+  uint64_t* p_part;   // [2 * (kPParts - 1)]: parts of P_t written (the last part signals p_full)
   uint64_t* p_full;   // [2]
   uint64_t* o_full;   // [2]
   uint64_t* drain;
@@ -141,7 +148,8 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
   bars.v_full = bars.k_empty + C::kKStages;
   bars.v_empty = bars.v_full + C::kVStages;
   bars.s_full = bars.v_empty + C::kVStages;
-  bars.p_full = bars.s_full + 2;
+  bars.p_part = bars.s_full + 2;
+  bars.p_full = bars.p_part + 2 * (kPParts - 1);
   bars.o_full = bars.p_full + 2;
   bars.drain = bars.o_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars.drain + 1);
@@ -184,6 +192,7 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bars.s_full + t, 1);
+      for (int q = 0; q + 1 < kPParts; ++q) mbar_init(bars.p_part + t * (kPParts - 1) + q, kBlockM);
       mbar_init(bars.p_full + t, kBlockM);
       mbar_init(bars.o_full + t, 1);
     }
@@ -309,12 +318,13 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
           mma_bf16_ss_warp(d_tmem, a0 + off, qk_hi, b0 + off, qk_hi, C::kIdescS, k > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int stage, bool accumulate) {
+      // O_t += P_t V_j over keys [16 k_begin, 16 k_end) of the tile.
+      auto issue_pv = [&](int t, int stage, bool accumulate, int k_begin, int k_end) {
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(256 + t * DV);
         const uint32_t p_tmem = tmem + static_cast<uint32_t>(t * kBlockN);
         const uint32_t b0 = v_lo + static_cast<uint32_t>((stage * CV::kTileBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < kBlockN / 16; ++k) {
+        for (int k = k_begin; k < k_end; ++k) {
           mma_bf16_ts_warp(d_tmem, p_tmem + static_cast<uint32_t>(k * 8),
                            b0 + static_cast<uint32_t>((k * 16 * CV::kRowBytes) >> 4), v_hi, C::kIdescPV,
                            (accumulate || k > 0) ? 1u : 0u);
@@ -354,10 +364,18 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
         bool k_next_ready = false;
         for (int t = 0; t < 2 && ok; ++t) {
           if (active(t, j)) {
-            ok = mbar_wait_warp(bars.p_full + t, static_cast<uint32_t>(j - lo_of(t)) & 1u, ab);
+            // P_t V_j starts on the first parts of P_t while the softmax
+            // still computes the later ones.
+            const uint32_t pp = static_cast<uint32_t>(j - lo_of(t)) & 1u;
+            constexpr int kSteps = kPPartKeys / 16;
+#pragma unroll
+            for (int q = 0; q < kPParts && ok; ++q) {
+              ok = mbar_wait_warp(q + 1 < kPParts ? bars.p_part + t * (kPParts - 1) + q : bars.p_full + t, pp, ab);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, s, q > 0 || j > lo_of(t), q * kSteps, (q + 1) * kSteps);
+            }
             if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, s, j > lo_of(t));
             mma_commit_warp(bars.o_full + t);
             if (t == last_pv_t) mma_commit_warp(bars.v_empty + s);
           }
@@ -461,6 +479,23 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
           l *= alpha;
         }
       }
+      // O_t already holds P(j-1) V(j-1): the commit that signalled S_t(j)
+      // covers every MMA issued before it, PV_t(j-1) included.  The rescale
+      // comes before the first half of P is released, since P(j) V(j) then
+      // starts to accumulate into O_t.
+      // (16-column chunks: the 128 scores are live here.)
+      if (rescale_warp) {
+#pragma unroll
+        for (int c = 0; c < DV / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld_chunk(lane_base + o_col + c * 16, o);
+          tmem_ld_wait();
+          reg_fence(o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_chunk(lane_base + o_col + c * 16, o);
+        }
+      }
       const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
       // p = exp2(s * scale * log2(e) - m): one packed FMA per pair of scores,
       // four independent packed partial sums.
@@ -470,36 +505,27 @@ sdpa_fwd_bf16_tc(const __grid_constant__ SdpaTcParams p) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int q = 0; q < kPParts; ++q) {
+        uint32_t pk[kPPartKeys / 2];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int c = half * 64 + 2 * e;
+        for (int e = 0; e < kPPartKeys / 2; ++e) {
+          const int c = q * kPPartKeys + 2 * e;
           const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, neg2);
           const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[e & 3] = __fadd2_rn(acc[e & 3], pe);
           pk[e] = pack_bf16x2(pe.x, pe.y);
         }
-        tmem_st32(lane_base + s_col + half * 32, pk);
+        tmem_st_chunk(lane_base + s_col + q * (kPPartKeys / 2), pk);
+        if (q + 1 < kPParts) {
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bars.p_part + t * (kPParts - 1) + q);
+        }
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]);
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 a = __fadd2_rn(a01, a23);
       const float rowsum = a.x + a.y;
-      // O_t already holds P(j-1) V(j-1): the commit that signalled S_t(j)
-      // covers every MMA issued before it, PV_t(j-1) included.
-      if (rescale_warp) {
-#pragma unroll
-        for (int c = 0; c < DV / CV::kOChunk; ++c) {
-          uint32_t o[CV::kOChunk];
-          tmem_ld_chunk(lane_base + o_col + c * CV::kOChunk, o);
-          tmem_ld_wait();
-          reg_fence(o);
-#pragma unroll
-          for (int e = 0; e < CV::kOChunk; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_chunk(lane_base + o_col + c * CV::kOChunk, o);
-        }
-      }
       l += rowsum;
       tmem_st_wait();
       tc_fence_before();
