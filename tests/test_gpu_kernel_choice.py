@@ -57,3 +57,18 @@ def test_kernels_agree_on_long_causal(d, monkeypatch):
         outs.append(host(sd.attention(q, k, v, sd.SDPA_MASK_CAUSAL)))
         sd.sdpa_device_check()
     assert rel_err(outs[1], outs[0]) <= 1e-2
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("n", [3072, 3200])
+def test_default_choice_either_side_of_the_crossover(d, n, monkeypatch):
+    """Unpinned: a 3072-key walk runs on the one-tile kernel and a 3200-key
+    walk on the two-tile kernel; both against the oracle, causal with padding."""
+    monkeypatch.delenv("LIBSDPA_ATTENTION_KERNEL", raising=False)
+    rng = np.random.default_rng(13200 + d + n)
+    b, h = 2, 1
+    q, k, v = (_rand(rng, (b, h, n, d), 0.5) for _ in range(3))
+    lens = np.array([n, n - 77], np.int32)
+    got = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL | sd.SDPA_MASK_PADDING, dev_int(lens)))
+    sd.sdpa_device_check()
+    assert rel_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL | sd.SDPA_MASK_PADDING, lens)) <= TOL_BF16

@@ -83,8 +83,14 @@ sdpa_status current_device(unsigned** status) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Key spans up to this length use the one-tile kernel at d = 128.
-constexpr long long kOneTileMaxKeys = 2048;
+// Key spans up to these lengths use the one-tile kernel (d <= 128); longer
+// walks use the two-tile kernel.  Measured on GB300 (b = 4, 16 * 8192 / n
+// heads, d = 16 to 128): the kernels are within 1-3 % at 3072 keys; at 512
+// keys the one-tile kernel leads by up to 40 %, at 8192 keys the two-tile
+// kernel by up to 13 % (d = 16 and 32, causal).  A restricted window keeps
+// every query tile's walk short, and the one-tile kernel leads up to r = 4096
+// (within 2 % there).
+constexpr long long kOneTileMaxKeys = 3072;
 constexpr long long kOneTileMaxKeysWindowed = 4352;   // r up to 4096
 
 // 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
@@ -200,7 +206,6 @@ bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
   const char* e = std::getenv("LIBSDPA_ATTENTION_KERNEL");
   if (e != nullptr && std::strcmp(e, "one_tile") == 0) return true;
   if (e != nullptr && std::strcmp(e, "two_tile") == 0) return false;
-  if (d <= 64) return true;
   const long long span = std::min<long long>(n_k, 1ll * win_left + win_right + 128);
   const bool windowed = win_left != sdpa::kWindowUnbounded || win_right != sdpa::kWindowUnbounded;
   return span <= (windowed ? kOneTileMaxKeysWindowed : kOneTileMaxKeys);
@@ -228,9 +233,9 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   SdpaTcParams p;
   p.pdl = pdl ? 1 : 0;
   // The one-tile kernel (one 128-row query tile per CTA, 32- or 64-key tiles;
-  // two or four CTAs per SM at d <= 128) takes wide heads, small heads, and
-  // the short key walks where the two-tile kernel's longer per-CTA chain
-  // would leave SMs idle.  Unequal key and value sizes take the two-tile one.
+  // two or four CTAs per SM at d <= 128) takes wide heads and the short key
+  // walks where the two-tile kernel's longer per-CTA chain would leave SMs
+  // idle.  Unequal key and value sizes take the two-tile one.
   const bool one_tile = d_k == d_v && use_one_tile_kernel(d_k, n_k, win_left, win_right);
   const int kv_rows = one_tile ? sdpa::one_tile_key_tile(d_k) : 128;
   if (!make_map_4d(&p.tm_q, q, d_k, n_q, h, b, sq.n, sq.h, sq.b) ||
