@@ -2,7 +2,8 @@
 with LIBSDPA_ATTENTION_KERNEL, against the oracle (2e-2 of the output scale):
 the two-tile kernel (two 128-row query tiles per CTA, 128-key tiles) and the
 one-tile kernel (one query tile per CTA; 64-key tiles and two CTAs per SM at
-d = 64, 128; 32-key tiles and four CTAs per SM at d = 16, 32).
+d = 64, 128; 32-key tiles and four CTAs per SM at d = 16, 32, and at d = 64
+for short walks over many CTAs).
 The library picks between them by shape; these tests keep both covered on
 the same shapes, masks, windows and ragged tails."""
 import numpy as np
@@ -30,6 +31,33 @@ def test_kernel_parity(kernel, d, mask, r, monkeypatch):
     n_k = n if (mask & 1) or r else 650
     q, k, v = _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
     lens = np.array([n_k, 201], np.int32) if mask & 2 else None
+    lens_d = None if lens is None else dev_int(lens)
+    t = __import__("torch")
+    out = t.full((b, h, n, d), 9.0, dtype=t.bfloat16, device="cuda")
+    lse = t.zeros((b, h, n), dtype=t.float32, device="cuda")
+    sd.sdpa_forward_lse(dev(q), dev(k), dev(v), out, lse, b, h, n, n_k, d, d, mask, lens_d, r)
+    sd.sdpa_device_check()
+    window = r or None
+    assert rel_err(host(out), oracle.sdpa(q, k, v, mask, lens, window=window)) <= TOL_BF16
+    ref_lse = oracle.lse(q, k, mask, lens, window=window)
+    got_lse = lse.double().cpu().numpy()
+    assert np.array_equal(np.isneginf(got_lse), np.isneginf(ref_lse))
+    fin = ~np.isneginf(ref_lse)
+    assert np.abs(got_lse[fin] - ref_lse[fin]).max() <= 1e-3
+
+
+@pytest.mark.parametrize("keys", [32, 64])
+@pytest.mark.parametrize("mask,r", [(0, 0), (1, 0), (2, 0), (3, 0), (1, 100), (0, 257), (3, 64)])
+def test_one_tile_d64_key_tiles(keys, mask, r, monkeypatch):
+    """The one-tile kernel at d = 64 with each key tile (32: four CTAs per SM;
+    64: two), pinned with LIBSDPA_ONE_TILE_KEYS, against the oracle."""
+    monkeypatch.setenv("LIBSDPA_ATTENTION_KERNEL", "one_tile")
+    monkeypatch.setenv("LIBSDPA_ONE_TILE_KEYS", str(keys))
+    rng = np.random.default_rng(13300 + keys + 7 * mask + r)
+    b, h, n, d = 2, 3, 333, 64
+    n_k = n if (mask & 1) or r else 650
+    q, k, v = _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+    lens = np.array([n_k, 95], np.int32) if mask & 2 else None
     lens_d = None if lens is None else dev_int(lens)
     t = __import__("torch")
     out = t.full((b, h, n, d), 9.0, dtype=t.bfloat16, device="cuda")

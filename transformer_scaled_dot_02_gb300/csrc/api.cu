@@ -91,6 +91,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // every query tile's walk short, and the one-tile kernel leads up to r = 4096
 // (within 2 % there).
 constexpr long long kOneTileMaxKeys = 3072;
+constexpr long long kOneTileShortKeys = 2048;   // d = 64: 32-key tiles up to this span
 constexpr long long kOneTileMaxKeysWindowed = 4352;   // r up to 4096
 
 // 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
@@ -201,14 +202,36 @@ float effective_scale(float scale, int d_k) {
 // 4096 to 16384, causal or not).  A restricted window gives every query tile
 // the same short walk, and there the one-tile kernel leads up to r = 4096
 // (0.375 against 0.396 ms at b4 h16 n8192, causal).
+// Keys one 128-row query tile can see at most.
+long long key_span(int n_k, int win_left, int win_right) {
+  return std::min<long long>(n_k, 1ll * win_left + win_right + 128);
+}
+
 bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
   if (d > 128) return true;
   const char* e = std::getenv("LIBSDPA_ATTENTION_KERNEL");
   if (e != nullptr && std::strcmp(e, "one_tile") == 0) return true;
   if (e != nullptr && std::strcmp(e, "two_tile") == 0) return false;
-  const long long span = std::min<long long>(n_k, 1ll * win_left + win_right + 128);
+  const long long span = key_span(n_k, win_left, win_right);
   const bool windowed = win_left != sdpa::kWindowUnbounded || win_right != sdpa::kWindowUnbounded;
   return span <= (windowed ? kOneTileMaxKeysWindowed : kOneTileMaxKeys);
+}
+
+// Key tile of the one-tile kernel: 32 below d = 64, 64 above.  At d = 64,
+// 32-key tiles need 128 tensor-memory columns, so four CTAs share an SM
+// instead of two; that pays when the walk is short and the grid holds at
+// least two waves of two-CTA slots (measured on GB300: 6-17 % faster on
+// 1024-key walks and restricted windows, 15 % on b32 h16 256 x 384; 22 %
+// slower on b32 h8 n128, 2 % on 3072-key walks).  LIBSDPA_ONE_TILE_KEYS =
+// 32 | 64 pins it at d = 64.
+int one_tile_key_tile(int d, long long span, long long ctas) {
+  if (d < 64) return 32;
+  if (d > 64) return 64;
+  if (const char* e = std::getenv("LIBSDPA_ONE_TILE_KEYS")) {
+    const int v = std::atoi(e);
+    if (v == 32 || v == 64) return v;
+  }
+  return (span <= kOneTileShortKeys && ctas >= 4ll * sdpa::device_sm_count()) ? 32 : 64;
 }
 
 // Element strides of a 4-D (d, n, h, b) tensor along n, h and b.
@@ -237,7 +260,11 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   // walks where the two-tile kernel's longer per-CTA chain would leave SMs
   // idle.  Unequal key and value sizes take the two-tile one.
   const bool one_tile = d_k == d_v && use_one_tile_kernel(d_k, n_k, win_left, win_right);
-  const int kv_rows = one_tile ? sdpa::one_tile_key_tile(d_k) : 128;
+  const int kv_rows =
+      one_tile ? one_tile_key_tile(d_k, key_span(n_k, win_left, win_right),
+                                   1ll * ((n_q + 127) / 128) * b * h)
+               : 128;
+  if (one_tile && !sdpa::one_tile_supports(d_k, kv_rows)) return SDPA_ERR_UNSUPPORTED;
   if (!make_map_4d(&p.tm_q, q, d_k, n_q, h, b, sq.n, sq.h, sq.b) ||
       !make_map_4d(&p.tm_k, k, d_k, n_k, h, b, sk.n, sk.h, sk.b, kv_rows) ||
       !make_map_4d(&p.tm_v, v, d_v, n_k, h, b, sv.n, sv.h, sv.b, kv_rows) ||
@@ -255,7 +282,7 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.win_left = win_left;
   p.win_right = win_right;
   p.lse = lse;
-  const cudaError_t err = one_tile ? sdpa::launch_sdpa_one_tile(p, d_k, stream)
+  const cudaError_t err = one_tile ? sdpa::launch_sdpa_one_tile(p, d_k, kv_rows, stream)
                                    : sdpa::launch_sdpa_tc(p, d_k, d_v, stream);
   return err == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }

@@ -220,8 +220,24 @@ cudaError_t launch_bn(const GemmParams& p, int max_m, int max_n, cudaStream_t st
                        p.pdl != 0, p);
 }
 
+// Tile width: 256 columns, or 128 when 256-column tiles would not reach
+// half the SMs.  LIBSDPA_GEMM_BN = 256 | 128 pins it.
+int gemm_tile_n(const GemmParams& p) {
+  if (const char* e = std::getenv("LIBSDPA_GEMM_BN")) {
+    const int v = std::atoi(e);
+    if (v == 256 || v == 128) return v;
+  }
+  const int sms = device_sm_count();
+  long long tiles = 0;
+  for (int i = 0; i < p.num_problems; ++i)
+    tiles += 1ll * ((p.prob[i].m + BM - 1) / BM) * ((p.prob[i].n + 255) / 256);
+  return 2 * tiles >= sms ? 256 : 128;
+}
+
+}  // namespace
+
 // SMs of the current device, read once per device.
-int sm_count() {
+int device_sm_count() {
   constexpr int kMaxDevices = 64;
   static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
@@ -239,22 +255,6 @@ int sm_count() {
   }
   return v;
 }
-
-// Tile width: 256 columns, or 128 when 256-column tiles would not reach
-// half the SMs.  LIBSDPA_GEMM_BN = 256 | 128 pins it.
-int gemm_tile_n(const GemmParams& p) {
-  if (const char* e = std::getenv("LIBSDPA_GEMM_BN")) {
-    const int v = std::atoi(e);
-    if (v == 256 || v == 128) return v;
-  }
-  const int sms = sm_count();
-  long long tiles = 0;
-  for (int i = 0; i < p.num_problems; ++i)
-    tiles += 1ll * ((p.prob[i].m + BM - 1) / BM) * ((p.prob[i].n + 255) / 256);
-  return 2 * tiles >= sms ? 256 : 128;
-}
-
-}  // namespace
 
 cudaError_t launch_gemm_tc(const GemmParams& p, int max_m, int max_n, cudaStream_t stream) {
   if (max_m <= 0 || max_n <= 0 || p.num_problems <= 0) return cudaSuccess;

@@ -55,10 +55,15 @@ inline cudaError_t launch_kernel(void (*kernel)(Params), dim3 grid, dim3 block, 
 }
 // Two query tiles per CTA; (d_k, d_v) in {(16,16), (32,32), (64,64), (128,128), (16,64), (32,64)}.
 cudaError_t launch_sdpa_tc(const SdpaTcParams& p, int d_k, int d_v, cudaStream_t stream);
-// One 128-row query tile per CTA (d = 64, 128, 256, 512); K/V boxes of
-// one_tile_key_tile(d) rows; num_q_blocks = ceil(n_q / 128).
-int one_tile_key_tile(int head_dim);
-cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, cudaStream_t stream);
+// One 128-row query tile per CTA (d = 16 .. 512) with key tiles of key_tile
+// rows (32 for d = 16, 32; 32 or 64 for d = 64; 64 from d = 128); the K/V
+// maps' boxes must have key_tile rows; num_q_blocks = ceil(n_q / 128).
+bool one_tile_supports(int head_dim, int key_tile);
+cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, int key_tile,
+                                 cudaStream_t stream);
+
+// SMs of the current device (read once per device and cached).
+int device_sm_count();
 
 // One decoding step over a K/V cache on the CUDA cores, split across CTAs.
 struct DecodeParams {

@@ -43,9 +43,11 @@ constexpr int kMmaWarp = 5;
 constexpr int kHeadGroup = 8;              // (head, d_v slice) units sharing L2
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the 64/128 kernel
 
-template <int DK>
+// KT: keys per tile, 32 or 64 (64 for d >= 128).
+template <int DK, int KT>
 struct OCfg {
-  static constexpr int BN = DK < 64 ? 32 : 64;             // keys per tile
+  static constexpr int BN = KT;                             // keys per tile
+  static_assert(KT == 32 || (KT == 64 && DK >= 64), "key tile");
   // d = 512: one K stage and one V stage (Q alone takes 128 KB), K loaded
   // and released in two halves so that the next tile's first half lands
   // while the scores still run over the second.
@@ -60,7 +62,8 @@ struct OCfg {
   static constexpr uint32_t kLayout = kRowBytes == 128 ? 2u : (kRowBytes == 64 ? 4u : 6u);
   static constexpr uint32_t kSBO = 8 * kRowBytes;           // 8-row group stride
   static constexpr int kStepsPerRow = kRowBytes / 32;       // K=16 steps per swizzled row
-  static constexpr int kOChunk = kDvc < 32 ? kDvc : 32;     // O columns per TMEM load
+  // O columns per TMEM load (16 when four CTAs share an SM at d = 64, to fit 80 registers)
+  static constexpr int kOChunk = kDvc < 32 ? kDvc : (DK == 64 && KT == 32 ? 16 : 32);
   static constexpr int kQBox = 128 * kRowBytes;             // kBoxCols columns x 128 rows
   static constexpr int kKVBox = BN * kRowBytes;             // kBoxCols columns x BN rows
   static constexpr int kQBytes = (DK / kBoxCols) * kQBox;
@@ -100,10 +103,10 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-template <int DK>
-__global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
+template <int DK, int KT>
+__global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
     sdpa_fwd_one_tile(const __grid_constant__ SdpaTcParams p) {
-  using C = OCfg<DK>;
+  using C = OCfg<DK, KT>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -522,33 +525,45 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK>::kMinBlocks)
   }
 }
 
-template <int DK>
+template <int DK, int KT>
 cudaError_t launch_one_tile_impl(const SdpaTcParams& p, cudaStream_t stream) {
-  const int smem = OCfg<DK>::kSmemBytes;
-  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_one_tile<DK>,
+  const int smem = OCfg<DK, KT>::kSmemBytes;
+  cudaError_t err = cudaFuncSetAttribute(sdpa_fwd_one_tile<DK, KT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h * OCfg<DK>::kChunks;
+  const long long blocks = static_cast<long long>(p.num_q_blocks) * p.b * p.h * OCfg<DK, KT>::kChunks;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-  return launch_kernel(sdpa_fwd_one_tile<DK>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
+  return launch_kernel(sdpa_fwd_one_tile<DK, KT>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
                        smem, stream, p.pdl != 0, p);
 }
 
 }  // namespace
 
-int one_tile_key_tile(int head_dim) {
-  return head_dim < 64 ? OCfg<32>::BN : OCfg<256>::BN;
+bool one_tile_supports(int head_dim, int key_tile) {
+  switch (head_dim) {
+    case 16:
+    case 32: return key_tile == 32;
+    case 64: return key_tile == 32 || key_tile == 64;
+    case 128:
+    case 256:
+    case 512: return key_tile == 64;
+    default: return false;
+  }
 }
 
-cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, cudaStream_t stream) {
-  if (head_dim == 16) return launch_one_tile_impl<16>(p, stream);
-  if (head_dim == 32) return launch_one_tile_impl<32>(p, stream);
-  if (head_dim == 64) return launch_one_tile_impl<64>(p, stream);
-  if (head_dim == 128) return launch_one_tile_impl<128>(p, stream);
-  if (head_dim == 256) return launch_one_tile_impl<256>(p, stream);
-  if (head_dim == 512) return launch_one_tile_impl<512>(p, stream);
-  return cudaErrorInvalidValue;
+cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, int key_tile,
+                                 cudaStream_t stream) {
+  if (!one_tile_supports(head_dim, key_tile)) return cudaErrorInvalidValue;
+  switch (head_dim) {
+    case 16: return launch_one_tile_impl<16, 32>(p, stream);
+    case 32: return launch_one_tile_impl<32, 32>(p, stream);
+    case 64: return key_tile == 32 ? launch_one_tile_impl<64, 32>(p, stream)
+                                   : launch_one_tile_impl<64, 64>(p, stream);
+    case 128: return launch_one_tile_impl<128, 64>(p, stream);
+    case 256: return launch_one_tile_impl<256, 64>(p, stream);
+    default: return launch_one_tile_impl<512, 64>(p, stream);
+  }
 }
 
 }  // namespace sdpa
