@@ -15,10 +15,13 @@
 //                that product never waits for a K load.
 //   - d = 64 and 128 where the key walk is short: key tiles of 64, 256
 //     tensor-memory columns, two CTAs per SM, so short sequences get twice
-//     the CTAs in flight and half the serial chain per CTA.
-//   - small heads, d = 16 and 32: key tiles of 32, 128 tensor-memory
-//     columns, four CTAs per SM; rows of 32 or 64 bytes, swizzled at that
-//     width.
+//     the CTAs in flight and half the serial chain per CTA.  At d = 64 the
+//     library may instead pick key tiles of 32 (128 columns, four CTAs per
+//     SM) for short walks over many CTAs; the key tile is a template
+//     parameter and the K/V boxes must match it.
+//   - small heads, d = 16 and 32 on short walks: key tiles of 32, 128
+//     tensor-memory columns, four CTAs per SM; rows of 32 or 64 bytes,
+//     swizzled at that width.
 // Roles:
 //   warp 4      TMA producer: Q once, K_j and V_j (this CTA's d_v slice) in
 //               two stages each.
