@@ -55,6 +55,21 @@ typedef enum {
 enum { SDPA_MASK_NONE = 0, SDPA_MASK_CAUSAL = 1, SDPA_MASK_PADDING = 2 };
 
 /*
+ * Kernel choice.  The library picks each launch's kernel and tile sizes from
+ * the shapes; the results agree to bf16 rounding whichever is picked.  Three
+ * environment variables, read at every call, pin a choice (for tests and
+ * tuning; anything else is ignored):
+ *   LIBSDPA_ATTENTION_KERNEL = one_tile | two_tile   forward attention kernel
+ *       (d_k == d_v <= 128): one 128-row query tile per CTA, or two.  The
+ *       default takes one_tile while a query tile sees at most 3072 keys
+ *       (4352 with a restricted window), two_tile beyond.
+ *   LIBSDPA_ONE_TILE_KEYS = 32 | 64   key tile of the one-tile kernel at
+ *       d = 64.  The default takes 32 for walks of at most 2048 keys when
+ *       the grid has at least four CTAs per SM, 64 otherwise.
+ *   LIBSDPA_GEMM_BN = 256 | 128   column tile of the projection GEMMs.
+ */
+
+/*
  * Scaled dot-product attention, bf16 (Eq. (1) with the masks above).
  *   q   [b, h, n_q, d_k]  bf16, device
  *   k   [b, h, n_k, d_k]  bf16, device
