@@ -187,20 +187,23 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
     kv_len = p.kv_lengths[bi];
     kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
   }
-  // key tiles [j_lo, j_hi) hold a key some row of the tile can see
+  // Key tile u covers keys [key_base + u BN, key_base + (u + 1) BN), from
+  // the first key some row of the tile can see (0 without a restricted
+  // window; with one, starting there instead of at a multiple of BN saves
+  // the mostly masked tile an aligned grid adds).  Keys past n_k load as
+  // zeros and are masked.
   const int qs = qb * kBlockM;
-  int j_lo = 0, j_hi = 0;
+  int key_base = 0, n_kv = 0;
   {
     const int row_hi = min(qs + kBlockM, p.n_q) - 1;
     const int key_lo = max(0, qs - p.win_left);
     int key_hi = min(kv_len, row_hi + 1 + min(p.win_right, p.n_k));
     if (causal) key_hi = min(key_hi, row_hi + 1);
     if (key_hi > key_lo) {
-      j_lo = key_lo / BN;
-      j_hi = (key_hi + BN - 1) / BN;
+      key_base = key_lo;
+      n_kv = (key_hi - key_lo + BN - 1) / BN;
     }
   }
-  const int n_kv = j_hi - j_lo;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -218,14 +221,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
         constexpr int kHalfBoxes = DK / C::kBoxCols / 2;
         int k0_issued = 0;
         for (int u = 0; u < n_kv; ++u) {
-          const int j = j_lo + u;
+          const int j0 = key_base + u * BN;   // first key of the tile
           const uint32_t prev = static_cast<uint32_t>(u - 1);
           // S(u-1)'s first half read this half last; kh_free cannot be a
           // phase ahead of it, since S(u) needs the half loaded here.
           if (u >= 1 && !mbar_wait(kh_free, prev & 1u, ab)) break;
           mbar_arrive_expect_tx(k_full, C::kKBytes / 2);
           for (int c = 0; c < kHalfBoxes; ++c)
-            tma_load_4d(&p.tm_k, k_full, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols, j * BN,
+            tma_load_4d(&p.tm_k, k_full, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols, j0,
                         hi, bi);
           k0_issued = u + 1;
           // all of S(u-1) read the second half (s_full of its buffer)
@@ -233,14 +236,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           mbar_arrive_expect_tx(k_full + 1, C::kKBytes / 2);
           for (int c = kHalfBoxes; c < 2 * kHalfBoxes; ++c)
             tma_load_4d(&p.tm_k, k_full + 1, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols,
-                        j * BN, hi, bi);
+                        j0, hi, bi);
           k_issued = u + 1;
           // O += P(u-1) V(u-1) read V last (o_full of its parity)
           if (u >= 1 && !mbar_wait(o_full + (prev & 1u), (prev >> 1) & 1u, ab)) break;
           mbar_arrive_expect_tx(v_full, C::kVBytes);
           for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
             tma_load_4d(&p.tm_v, v_full, smem + C::kVOff + c * C::kKVBox,
-                        chunk * C::kDvc + c * C::kBoxCols, j * BN, hi, bi);
+                        chunk * C::kDvc + c * C::kBoxCols, j0, hi, bi);
           v_issued = u + 1;
         }
         mbar_wait_drain(q_full, 0);
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
         if (v_issued > 0) mbar_wait_drain(v_full, static_cast<uint32_t>(v_issued - 1) & 1u);
       } else {
         for (int u = 0; u < n_kv; ++u) {
-          const int j = j_lo + u;
+          const int j0 = key_base + u * BN;   // first key of the tile
           const int s = u & 1;
           const uint32_t use = static_cast<uint32_t>(u >> 1);
           // S(u-2) read this stage last.  s_full[s] cannot be two phases
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           mbar_arrive_expect_tx(k_full + s, C::kKBytes);
           for (int c = 0; c < DK / C::kBoxCols; ++c)
             tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox,
-                        c * C::kBoxCols, j * BN, hi, bi);
+                        c * C::kBoxCols, j0, hi, bi);
           k_issued = u + 1;
           // O += P(u-2) V(u-2) read this stage last; o_full[s] cannot be two
           // phases ahead either (O += P(u) V_u needs V_u).
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           mbar_arrive_expect_tx(v_full + s, C::kVBytes);
           for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
             tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
-                        chunk * C::kDvc + c * C::kBoxCols, j * BN, hi, bi);
+                        chunk * C::kDvc + c * C::kBoxCols, j0, hi, bi);
           v_issued = u + 1;
         }
         mbar_wait_drain(q_full, 0);
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(sr[e]);
         }
       }
-      const int key0 = (j_lo + u) * BN;
+      const int key0 = key_base + u * BN;
       const bool tile_masked = (key0 + BN > kv_len) || (causal && key0 + BN - 1 > qs) ||
                                (key0 + BN - 1 > qs + p.win_right) ||
                                (key0 < qs + kBlockM - 1 - p.win_left);
