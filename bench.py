@@ -580,6 +580,7 @@ def run_row(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         val, threads, sample = oracle_sample()
         line["cpu_baseline"] = {"value": val, "unit": unit, "cores": threads, "kind": "oracle",
+                                "cpu": cpu_model(),
                                 "sample": sample}
     if pg:
         pg.barrier()
@@ -600,6 +601,27 @@ def _rows_flops(w, rows):
     return float(np.sum(4.0 * visible * w.d_k))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (x86 "model name"; on Arm, implementer/part
+    codes when no name is given), for the oracle baseline's record."""
+    import platform
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.machine()
+    fields = {}
+    for l in info:
+        if ":" in l:
+            key, val = (x.strip() for x in l.split(":", 1))
+            fields.setdefault(key, val)
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "%s (implementer %s, part %s)" % (platform.machine(), fields.get("CPU implementer", "?"),
+                                                 fields["CPU part"])
+    return platform.machine()
+
+
 def oracle_baseline(w, q, k, v, n_rows):
     import oracle
     threads = oracle.default_threads()
@@ -610,7 +632,8 @@ def oracle_baseline(w, q, k, v, n_rows):
     value = _rows_flops(w, rows) / dt / 1e12
     return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": "%d query rows drawn uniformly from the %d rows of the workload "
-                      "(fp64 C oracle, %.1f s)" % (len(rows), w.b * w.h * w.n_q, dt)}
+                      "(fp64 C oracle, %.1f s)" % (len(rows), w.b * w.h * w.n_q, dt),
+            "cpu": cpu_model()}
 
 
 def run_reference(args, world, rank, local):
@@ -644,6 +667,7 @@ def run_reference(args, world, rank, local):
                    "b": w.b, "h": w.h, "n_q": w.n_q, "n_k": w.n_k, "d_k": w.d_k, "d_v": w.d_v,
                    "mask": "causal"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -35,6 +35,7 @@ def test_reference_arm_prints_the_contract_line():
     base = line["cpu_baseline"]
     assert base["kind"] == "oracle" and base["cores"] >= 1 and base["value"] == line["value"]
     assert "64 query rows" in base["sample"]
+    assert isinstance(base["cpu"], str) and base["cpu"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == "TFLOP/s"
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
