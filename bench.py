@@ -617,8 +617,12 @@ def cpu_model() -> str:
     if "model name" in fields:
         return fields["model name"]
     if "CPU part" in fields:
-        return "%s (implementer %s, part %s)" % (platform.machine(), fields.get("CPU implementer", "?"),
-                                                 fields["CPU part"])
+        # Arm Ltd (implementer 0x41) core part numbers
+        arm_parts = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2",
+                     "0xd4f": "Neoverse-V2", "0xd84": "Neoverse-V3"}
+        impl, part = fields.get("CPU implementer", "?"), fields["CPU part"]
+        name = arm_parts.get(part) if impl == "0x41" else None
+        return "%s %s (implementer %s, part %s)" % (platform.machine(), name or "core", impl, part)
     return platform.machine()
 
 
