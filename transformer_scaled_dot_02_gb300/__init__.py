@@ -9,6 +9,11 @@ to PyTorch's current CUDA stream.
 
 There is no fallback: if libsdpa.so is missing or fails to load, importing the
 functions raises, and every call returns the library's status as an exception.
+
+The library picks kernels and tile sizes from the shapes; the environment
+variables LIBSDPA_ATTENTION_KERNEL (one_tile | two_tile), LIBSDPA_ONE_TILE_KEYS
+(32 | 64, at d = 64) and LIBSDPA_GEMM_BN (256 | 128) pin them, read at every
+call (include/sdpa.h gives the defaults).
 """
 from __future__ import annotations
 
