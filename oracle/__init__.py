@@ -53,7 +53,7 @@ class Oracle:
         lib.oracle_sdpa_restricted.restype = I
         lib.oracle_sdpa_decode.argtypes = [P, P, P, P, I, I, I, I, I, I, P, D, P, I64, I]
         lib.oracle_sdpa_decode.restype = I
-        lib.oracle_sdpa_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, D, I, I]
+        lib.oracle_sdpa_backward.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, D, I, I]
         lib.oracle_sdpa_backward.restype = I
         lib.oracle_sdpa_lse.argtypes = [P, P, P, I, I, I, I, I, I, P, I, D, I]
         lib.oracle_sdpa_lse.restype = I
@@ -138,16 +138,24 @@ def _lse(lib, q, k, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, window=None
 
 
 def _backward(lib, q, k, v, dout, mask_kind=MASK_NONE, kv_lengths=None, scale=0.0, window=None,
-              threads=None):
-    """dq, dk, dv (float64, shapes of q, k, v) of sum(dout * attention(q, k, v))."""
+              threads=None, out=None):
+    """dq, dk, dv (float64, shapes of q, k, v) of sum(dout * attention(q, k, v)).
+
+    ``out`` [b,h,n_q,d_v] is the forward output handed to the backward (None:
+    the exact output).  It enters only through D_i = dO_i . O_i in
+    dS = P o (dP - D), as it does for a backward routine that takes O as an input.
+    """
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
     b, h, n_q, d_k = q.shape
     n_k, d_v = k.shape[2], v.shape[3]
+    if out is not None:
+        out = _f32(out)
+        assert out.shape == (b, h, n_q, d_v)
     lens = None if kv_lengths is None else np.ascontiguousarray(kv_lengths, dtype=np.int32)
     dq = np.zeros(q.shape, dtype=np.float64)
     dk = np.zeros(k.shape, dtype=np.float64)
     dv = np.zeros(v.shape, dtype=np.float64)
-    rc = lib.oracle_sdpa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk),
+    rc = lib.oracle_sdpa_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out), _ptr(dq), _ptr(dk),
                                   _ptr(dv), b, h, n_q, n_k, d_k, d_v, int(mask_kind), _ptr(lens),
                                   float(scale), int(window or 0), threads or default_threads())
     if rc != 0:

@@ -37,6 +37,8 @@
  *       dV = P^T dO,   dP = dO V^T,   D_i = sum_j P_ij dP_ij (= dO_i . O_i),
  *       dS = P o (dP - D),   dQ = scale * dS K,   dK = scale * dS^T Q,
  *   the softmax Jacobian written out row by row; masked entries have P = 0.
+ *   A backward routine is handed the forward output O and forms D_i from it;
+ *   the oracle takes that O as an optional input for the same term.
  *
  *   Section 3.2.2, multi-head attention:
  *       MultiHead(Q, K, V) = Concat(head_1, ..., head_h) W^O,
@@ -285,7 +287,7 @@ int oracle_sdpa_lse(const float* q, const float* k, double* lse, int b, int h, i
 /* ------------------------------------------------------------------------ */
 /* Gradients of Eq. (1) for one (batch, head): plain loops over rows.         */
 typedef struct {
-  const float *q, *k, *v, *dout;
+  const float *q, *k, *v, *dout, *out;
   double *dq, *dk, *dv;
   int h, n_q, n_k, d_k, d_v, mask_kind;
   const int32_t* kv_lengths;
@@ -345,6 +347,14 @@ static void bwd_range(void* p, int64_t begin, int64_t end) {
         dprow[j] = dot;
         Di += prow[j] * dot;
       }
+      /* With a forward output O handed in, D_i is dO_i . O_i of that O (what
+         the backward routine is given); without one, sum_j P_ij dP_ij above is
+         dO_i . O_i of the exact O. */
+      if (c->out != NULL) {
+        const float* oi = c->out + bh * (int64_t)c->n_q * c->d_v + (int64_t)i * c->d_v;
+        Di = 0.0;
+        for (int x = 0; x < c->d_v; ++x) Di += (double)doi[x] * (double)oi[x];
+      }
       for (int j = 0; j < c->n_k; ++j) {
         if (prow[j] == 0.0) continue;
         double ds = prow[j] * (dprow[j] - Di);
@@ -366,16 +376,20 @@ static void bwd_range(void* p, int64_t begin, int64_t end) {
 /*
  * Gradients of Eq. (1) with masks: given q, k, v (BHSD float32) and dout
  * [b,h,n_q,d_v], writes dq [b,h,n_q,d_k], dk [b,h,n_k,d_k], dv [b,h,n_k,d_v]
- * (fp64).  Parallel over (batch, head).  Returns 0, or -1 on bad arguments.
+ * (fp64).  out [b,h,n_q,d_v] is the forward output the backward is handed, or
+ * NULL for the exact one: it enters only through D_i = dO_i . O_i, the row
+ * term of dS = P o (dP - D).  Parallel over (batch, head).  Returns 0, or -1
+ * on bad arguments.
  */
 int oracle_sdpa_backward(const float* q, const float* k, const float* v, const float* dout,
+                         const float* out,
                          double* dq, double* dk, double* dv, int b, int h, int n_q, int n_k,
                          int d_k, int d_v, int mask_kind, const int32_t* kv_lengths,
                          double scale, int r, int n_threads) {
   if (b < 0 || h < 0 || n_q < 0 || n_k < 0 || d_k < 1 || d_v < 1) return -1;
   if ((mask_kind & ORACLE_MASK_CAUSAL) && n_q != n_k) return -1;
   if ((mask_kind & ORACLE_MASK_PADDING) && kv_lengths == NULL) return -1;
-  bwd_ctx c = {q, k, v, dout, dq, dk, dv, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths,
+  bwd_ctx c = {q, k, v, dout, out, dq, dk, dv, h, n_q, n_k, d_k, d_v, mask_kind, kv_lengths,
                scale > 0.0 ? scale : 1.0 / sqrt((double)d_k),
                r > 0 ? (int64_t)((r - 1) / 2) : INT64_MAX / 4,
                r > 0 ? (int64_t)(r / 2) : INT64_MAX / 4};

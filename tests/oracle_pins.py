@@ -522,6 +522,41 @@ def pin_backward_closed_forms(o):
     assert np.allclose(dv.sum(2), do.astype(np.float64).sum(2), atol=1e-12)
 
 
+def pin_backward_given_output(o):
+    """The forward output handed to the backward enters only through
+    D_i = dO_i . O_i.  Handing in the exact output (rounded to float32)
+    changes the gradients by that rounding alone.  Moving row i of it so that
+    D_i moves by c_i leaves dV unchanged, moves dQ_i by -scale c_i sum_j P_ij k_j
+    (the attention output of row i with the keys as values), and moves the sum
+    of dK over keys by -scale sum_i c_i q_i over the rows that see a key."""
+    rng = np.random.default_rng(53)
+    b, h, n, d_k, d_v = 2, 2, 7, 3, 4
+    q = rng.standard_normal((b, h, n, d_k)).astype(np.float32)
+    k = rng.standard_normal((b, h, n, d_k)).astype(np.float32)
+    v = rng.standard_normal((b, h, n, d_v)).astype(np.float32)
+    do = rng.standard_normal((b, h, n, d_v)).astype(np.float32)
+    lens = np.array([n, 4], np.int32)
+    scale = 1.0 / np.sqrt(d_k)
+    for mask, r in ((MASK_NONE, None), (MASK_CAUSAL | MASK_PADDING, None), (MASK_PADDING, 3)):
+        exact = o.backward(q, k, v, do, mask, lens, window=r)
+        out32 = o.sdpa(q, k, v, mask, lens, window=r).astype(np.float32)
+        given = o.backward(q, k, v, do, mask, lens, window=r, out=out32)
+        assert np.array_equal(given[2], exact[2])
+        for g, e in zip(given[:2], exact[:2]):
+            assert np.allclose(g, e, rtol=0, atol=1e-6), mask
+        moved = (out32 + rng.standard_normal(out32.shape).astype(np.float32)).astype(np.float32)
+        c = (np.einsum("bhic,bhic->bhi", do.astype(np.float64), moved.astype(np.float64))
+             - np.einsum("bhic,bhic->bhi", do.astype(np.float64), out32.astype(np.float64)))
+        dq, dk, dv = o.backward(q, k, v, do, mask, lens, window=r, out=moved)
+        assert np.array_equal(dv, given[2])
+        kbar = o.sdpa(q, k, k, mask, lens, window=r)
+        assert np.allclose(dq, given[0] - scale * c[..., None] * kbar, rtol=0, atol=1e-10), mask
+        seen = np.isfinite(o.lse(q, k, mask, lens, window=r))
+        want = given[1].sum(2) - scale * np.einsum("bhi,bhic->bhc", np.where(seen, c, 0.0),
+                                                   q.astype(np.float64))
+        assert np.allclose(dk.sum(2), want, rtol=0, atol=1e-10), mask
+
+
 def pin_lse_closed_forms(o):
     """The per-row log-sum-exp: zero keys give ln(number of visible keys)
     under every mask; a row that sees nothing gives -inf; one query 1 against
@@ -570,5 +605,5 @@ PINS = [pin_worked_example, pin_worked_example_causal, pin_toy_rows, pin_scale_i
         pin_mha_single_head_identity, pin_mha_matches_matrix_form, pin_mha_concat_not_average,
         pin_mha_rows_selection, pin_restricted_worked_example, pin_restricted_extremes,
         pin_restricted_brute_force, pin_decode_matches_causal_rows, pin_decode_cache_lengths,
-        pin_backward_finite_differences, pin_backward_closed_forms, pin_lse_closed_forms,
-        pin_lse_rebuilds_softmax]
+        pin_backward_finite_differences, pin_backward_closed_forms, pin_backward_given_output,
+        pin_lse_closed_forms, pin_lse_rebuilds_softmax]

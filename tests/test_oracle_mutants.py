@@ -43,6 +43,13 @@ MUTANTS = {
     "backward_ds_sign": ("double ds = prow[j] * (dprow[j] - Di);", "double ds = prow[j] * (dprow[j] + Di);"),
     "backward_dk_unscaled": ("dkj[x] += c->scale * ds * (double)qi[x];", "dkj[x] += ds * (double)qi[x];"),
     "backward_dv_uses_dp": ("dvj[x] += prow[j] * (double)doi[x];", "dvj[x] += dprow[j] * (double)doi[x];"),
+    "backward_given_output_no_head_offset": (
+        "const float* oi = c->out + bh * (int64_t)c->n_q * c->d_v + (int64_t)i * c->d_v;",
+        "const float* oi = c->out + (int64_t)i * c->d_v;"),
+    "backward_given_output_not_reset": ("        Di = 0.0;\n        for (int x = 0; x < c->d_v; ++x) Di +=",
+                                        "        for (int x = 0; x < c->d_v; ++x) Di +="),
+    "backward_given_output_squared": ("Di += (double)doi[x] * (double)oi[x];",
+                                      "Di += (double)oi[x] * (double)oi[x];"),
     "lse_drops_max": ("c->lse[r] = m + log(l);", "c->lse[r] = log(l);"),
     "lse_log2": ("c->lse[r] = m + log(l);", "c->lse[r] = m + log2(l);"),
     "lse_unscaled": ("s[j] = c->scale * dot;", "s[j] = dot;"),
