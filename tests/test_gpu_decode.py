@@ -6,7 +6,7 @@ import pytest
 import oracle
 import synthetic
 import transformer_scaled_dot_02_gb300 as sd
-from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+from gpu_util import TOL_BF16, dev, dev_int, host, parity_err
 
 pytestmark = pytest.mark.gpu
 
@@ -31,9 +31,9 @@ def test_decode_shapes(d, n_q, b, h, n_k):
     lens[0] = n_k
     got = _gpu(q, k, v, lens)
     ref = oracle.decode(q, k, v, lens)
-    assert rel_err(got, ref) <= TOL_BF16
+    assert parity_err(got, ref) <= TOL_BF16
     got_full = _gpu(q, k, v, None)
-    assert rel_err(got_full, oracle.decode(q, k, v)) <= TOL_BF16
+    assert parity_err(got_full, oracle.decode(q, k, v)) <= TOL_BF16
 
 
 def test_decode_edge_lengths():
@@ -47,7 +47,7 @@ def test_decode_edge_lengths():
     ref = oracle.decode(q, k, v, lens)
     assert np.array_equal(got[0], np.zeros_like(got[0]))
     assert np.array_equal(got[1, :, :2], np.zeros_like(got[1, :, :2]))
-    assert rel_err(got, ref) <= TOL_BF16
+    assert parity_err(got, ref) <= TOL_BF16
 
 
 def test_decode_matches_causal_attention_rows():
@@ -57,7 +57,7 @@ def test_decode_matches_causal_attention_rows():
     q, k, v = _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n, d)), _rand(rng, (b, h, n, d))
     full = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL))
     step = _gpu(q[:, :, n - n_q:], k, v)
-    assert rel_err(step, full[:, :, n - n_q:]) <= TOL_BF16
+    assert parity_err(step, full[:, :, n - n_q:]) <= TOL_BF16
 
 
 @pytest.mark.parametrize("n_q", [1, 4])
@@ -70,4 +70,4 @@ def test_decode_workload(n_q):
     lens = rng.integers(4096, n_k + 1, size=b).astype(np.int32)
     got = _gpu(q, k, v, lens)
     ref = oracle.decode(q, k, v, lens)
-    assert rel_err(got, ref) <= TOL_BF16
+    assert parity_err(got, ref) <= TOL_BF16

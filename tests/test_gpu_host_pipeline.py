@@ -8,7 +8,7 @@ import pytest
 import oracle
 import synthetic
 import transformer_scaled_dot_02_gb300 as sd
-from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+from gpu_util import TOL_BF16, dev, dev_int, host, parity_err
 
 pytestmark = pytest.mark.gpu
 
@@ -33,4 +33,4 @@ def test_attention_from_host(d, mask, hc):
     sd.sdpa_device_check()
     got = oh.float().numpy().astype(np.float64)
     assert np.array_equal(got, host(whole))
-    assert rel_err(got, oracle.sdpa(q, k, v, mask, lens)) <= TOL_BF16
+    assert parity_err(got, oracle.sdpa(q, k, v, mask, lens)) <= TOL_BF16

@@ -13,16 +13,16 @@ import pytest
 import oracle
 import synthetic
 import transformer_scaled_dot_02_gb300 as sd
-from gpu_util import TOL_BF16, dev, host, rel_err
+from gpu_util import TOL_BF16, dev, host, parity_err
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("kernel,d,n", [("one_tile", 64, 384), ("two_tile", 64, 384), ("two_tile", 128, 640),
                                         ("one_tile", 512, 200)])
-def test_inputs_written_just_before_the_call(kernel, d, n, monkeypatch):
+def test_inputs_written_just_before_the_call(kernel, d, n, pin_kernels):
     import torch
-    monkeypatch.setenv("LIBSDPA_ATTENTION_KERNEL", kernel)
+    pin_kernels(attention=kernel)
     rng = np.random.default_rng(40 + d)
     b, h = 3, 2
     q0 = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
@@ -43,7 +43,7 @@ def test_inputs_written_just_before_the_call(kernel, d, n, monkeypatch):
         got = host(out)
         sd.sdpa_device_check()
         ref = oracle.sdpa(q0 * np.float32(sign), k, v, sd.SDPA_MASK_PADDING, lens)
-        assert rel_err(got, ref) <= TOL_BF16, (r, kernel)
+        assert parity_err(got, ref) <= TOL_BF16, (r, kernel)
 
 
 def test_backward_inputs_written_just_before_the_call():
@@ -61,4 +61,4 @@ def test_backward_inputs_written_just_before_the_call():
         sd.sdpa_device_check()
         rq, rk, rv = oracle.backward(q, k, v, do0 * np.float32(sign), sd.SDPA_MASK_CAUSAL)
         for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-            assert rel_err(host(got), ref) <= TOL_BF16, r
+            assert parity_err(host(got), ref) <= TOL_BF16, r

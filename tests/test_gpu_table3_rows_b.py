@@ -7,7 +7,7 @@ import pytest
 import oracle
 import synthetic
 import transformer_scaled_dot_02_gb300 as sd
-from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+from gpu_util import TOL_BF16, dev, dev_int, host, parity_err
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def test_rows_b_attention(d_k, mask, r):
     sd.sdpa_device_check()
     assert tuple(out.shape) == (b, h, n, d_v)
     window = r or None
-    assert rel_err(host(out), oracle.sdpa(q, k, v, mask, lens, window=window)) <= TOL_BF16
+    assert parity_err(host(out), oracle.sdpa(q, k, v, mask, lens, window=window)) <= TOL_BF16
     ref_lse = oracle.lse(q, k, mask, lens, window=window)
     got = lse.double().cpu().numpy()
     fin = ~np.isneginf(ref_lse)
@@ -44,7 +44,7 @@ def test_rows_b_long_causal(d_k):
     v = _rand(rng, (1, 2, 2048, 64))
     got = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL))
     sd.sdpa_device_check()
-    assert rel_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
+    assert parity_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
 
 
 @pytest.mark.parametrize("d_k", [16, 32])
@@ -62,4 +62,4 @@ def test_rows_b_mha(d_k):
                                 sd.SDPA_MASK_PADDING, dev_int(lens))
     sd.sdpa_device_check()
     ref = oracle.mha(x, x, wq, wk, wv, wo, h, d_k, d_v, sd.SDPA_MASK_PADDING, lens)
-    assert rel_err(host(y), ref) <= TOL_BF16
+    assert parity_err(host(y), ref) <= TOL_BF16

@@ -21,7 +21,7 @@ import oracle
 import synthetic
 import transformer_scaled_dot_02_gb300 as sd
 from transformer_scaled_dot_02_gb300 import build as sd_build
-from gpu_util import TOL_BF16, dev, host, rel_err
+from gpu_util import TOL_BF16, dev, host, parity_err
 
 pytestmark = pytest.mark.gpu
 
@@ -47,12 +47,12 @@ def faulty_lib():
 
 
 @pytest.mark.parametrize("kernel,d", [("two_tile", 64), ("one_tile", 64), ("one_tile", 512)])
-def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, d, monkeypatch):
+def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, d, pin_kernels):
     """d = 512 runs the one-tile kernel's single-stage path (K in two
     halves): its producer also waits on the withheld commit and must drain
     its own copies before the CTA leaves."""
     import torch
-    monkeypatch.setenv("LIBSDPA_ATTENTION_KERNEL", kernel)
+    pin_kernels(attention=kernel, lib=faulty_lib)
     rng = np.random.default_rng(1)
     b, h, n = 1, 1, 128   # one query tile (two CTAs at d = 512, one per half of d_v)
     q = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
@@ -74,7 +74,7 @@ def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, d, monkeypatch):
     v = synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
     got = host(sd.attention(dev(q), dev(k), dev(v), sd.SDPA_MASK_CAUSAL))
     sd.sdpa_device_check()
-    assert rel_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
+    assert parity_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
 
 
 def test_backward_bounded_wait_times_out_and_reports(faulty_lib):
@@ -105,4 +105,4 @@ def test_backward_bounded_wait_times_out_and_reports(faulty_lib):
     sd.sdpa_device_check()
     rq, rk, rv = oracle.backward(q, k, v, do, sd.SDPA_MASK_CAUSAL)
     for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-        assert rel_err(host(got), ref) <= TOL_BF16
+        assert parity_err(host(got), ref) <= TOL_BF16

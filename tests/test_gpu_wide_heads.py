@@ -8,7 +8,7 @@ import pytest
 import oracle
 import synthetic
 import transformer_scaled_dot_02_gb300 as sd
-from gpu_util import TOL_BF16, dev, dev_int, host, rel_err
+from gpu_util import TOL_BF16, dev, dev_int, host, parity_err
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def _check(q, k, v, mask, lens, r=0, scale=0.0):
     got, lse = _gpu(q, k, v, mask, lens, r, scale)
     window = r or None
     ref = oracle.sdpa(q, k, v, mask, lens, scale=scale, window=window)
-    assert rel_err(got, ref) <= TOL_BF16
+    assert parity_err(got, ref) <= TOL_BF16
     ref_lse = oracle.lse(q, k, mask, lens, scale=scale, window=window)
     hidden = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(lse), hidden)
@@ -123,4 +123,4 @@ def test_table3_row_a_mha(h, d):
                                 dev_int(lens))
     sd.sdpa_device_check()
     ref = oracle.mha(xq, xq, wq, wk, wv, wo, h, d, d, 2, lens)
-    assert rel_err(host(y), ref.reshape(b, n, dm)) <= TOL_BF16
+    assert parity_err(host(y), ref.reshape(b, n, dm)) <= TOL_BF16
