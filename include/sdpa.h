@@ -31,6 +31,11 @@
  *   - `scale` multiplies Q K^T; 0.0f selects 1/sqrt(d_k) (Eq. (1)); 1.0f gives
  *     the unscaled dot-product attention of section 3.2.1.  It must be >= 0
  *     and finite.
+ *   - Per-device state (the device check, the address of the kernels' error
+ *     word, the static array of mha_forward_noalloc) is set up by the first
+ *     call on each device and cached.  It belongs to the device's primary
+ *     context: after cudaDeviceReset, or anything else that destroys that
+ *     context, the process must not call the library again.
  */
 #ifndef LIBSDPA_SDPA_H
 #define LIBSDPA_SDPA_H
@@ -56,18 +61,23 @@ enum { SDPA_MASK_NONE = 0, SDPA_MASK_CAUSAL = 1, SDPA_MASK_PADDING = 2 };
 
 /*
  * Kernel choice.  The library picks each launch's kernel and tile sizes from
- * the shapes; the results agree to bf16 rounding whichever is picked.  Three
- * environment variables, read at every call, pin a choice (for tests and
- * tuning; anything else is ignored):
- *   LIBSDPA_ATTENTION_KERNEL = one_tile | two_tile   forward attention kernel
- *       (d_k == d_v <= 128): one 128-row query tile per CTA, or two.  The
- *       default takes one_tile while a query tile sees at most 3072 keys
- *       (4352 with a restricted window), two_tile beyond.
- *   LIBSDPA_ONE_TILE_KEYS = 32 | 64   key tile of the one-tile kernel at
- *       d = 64.  The default takes 32 for walks of at most 2048 keys when
- *       the grid has at least four CTAs per SM, 64 otherwise.
- *   LIBSDPA_GEMM_BN = 256 | 128   column tile of the projection GEMMs.
+ * the shapes; the results agree to bf16 rounding whichever is picked, and the
+ * library reads no environment variable.  For tests and tuning, this call
+ * pins a choice for every later call in the process (all threads, all
+ * devices) until it is called again; 0 leaves that choice to the shapes:
+ *   attention_kernel  forward attention kernel for d_k == d_v <= 128:
+ *       1 = one 128-row query tile per CTA, 2 = two.  By shape: one tile
+ *       while a query tile sees at most 3072 keys (4352 with a restricted
+ *       window), two beyond.
+ *   one_tile_keys  32 | 64: key tile of the one-tile kernel at d = 64.  By
+ *       shape: 32 for walks of at most 2048 keys when the grid has at least
+ *       four CTAs per SM, 64 otherwise.
+ *   gemm_bn  256 | 128: column tile of the projection GEMMs.  By shape: 256,
+ *       or 128 when 256-column tiles would not reach half the SMs.
+ * Returns SDPA_ERR_INVALID_ARG (and changes nothing) for any other value.
+ * Launches already enqueued are not affected.
  */
+sdpa_status sdpa_set_kernel_choice(int attention_kernel, int one_tile_keys, int gemm_bn);
 
 /*
  * Scaled dot-product attention, bf16 (Eq. (1) with the masks above).
@@ -225,7 +235,9 @@ sdpa_status mha_forward(const void* xq, const void* xkv, const void* wq, const v
  * meaning, layouts and rules as mha_forward.
  *   - Returns SDPA_ERR_WORKSPACE, before enqueuing anything, when
  *     mha_workspace_size(b, n_q, n_k, h, d_k, d_v) exceeds
- *     SDPA_MHA_NOALLOC_MAX_WORKSPACE.
+ *     SDPA_MHA_NOALLOC_MAX_WORKSPACE.  The argument checks of mha_forward
+ *     come first, so an invalid or unsupported argument returns the same
+ *     status as there.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *   - The first call on each device looks up the array's device address and
  *     caches it; make that first call before any stream capture.

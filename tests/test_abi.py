@@ -193,3 +193,24 @@ def test_valid_arguments_without_gpu_report_no_device(lib):
     assert lib.sdpa_decode(A, A, A, A, A, 1 << 30, 2, 2, 1, 4096, 128, 128, None,
                            ctypes.c_float(0.0), None) == NODEV
     assert lib.sdpa_device_check() == NODEV
+
+
+def test_kernel_choice_accepts_only_documented_values(lib):
+    """sdpa_set_kernel_choice is host-only: valid pins are taken, others
+    rejected with SDPA_ERR_INVALID_ARG; the test leaves every choice to the
+    shapes again."""
+    try:
+        for args in [(0, 0, 0), (1, 0, 0), (2, 32, 0), (1, 64, 256), (0, 0, 128)]:
+            assert lib.sdpa_set_kernel_choice(*args) == OK, args
+        for args in [(3, 0, 0), (-1, 0, 0), (0, 16, 0), (0, 128, 0), (0, 0, 64), (0, 0, 512)]:
+            assert lib.sdpa_set_kernel_choice(*args) == INVALID, args
+    finally:
+        assert lib.sdpa_set_kernel_choice(0, 0, 0) == OK
+
+
+def test_noalloc_limit_matches_the_header():
+    """The binding's copy of the static workspace size is the header's value."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+SDPA_MHA_NOALLOC_MAX_WORKSPACE\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "SDPA_MHA_NOALLOC_MAX_WORKSPACE not found"
+    assert int(m.group(1)) << int(m.group(2)) == sd.MHA_NOALLOC_MAX_WORKSPACE

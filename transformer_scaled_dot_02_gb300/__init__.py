@@ -10,10 +10,9 @@ to PyTorch's current CUDA stream.
 There is no fallback: if libsdpa.so is missing or fails to load, importing the
 functions raises, and every call returns the library's status as an exception.
 
-The library picks kernels and tile sizes from the shapes; the environment
-variables LIBSDPA_ATTENTION_KERNEL (one_tile | two_tile), LIBSDPA_ONE_TILE_KEYS
-(32 | 64, at d = 64) and LIBSDPA_GEMM_BN (256 | 128) pin them, read at every
-call (include/sdpa.h gives the defaults).
+The library picks kernels and tile sizes from the shapes;
+``sdpa_set_kernel_choice`` (or the ``kernel_choice`` context manager) pins
+them for tests and tuning (include/sdpa.h gives the defaults).
 """
 from __future__ import annotations
 
@@ -36,7 +35,8 @@ EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_lse",
            "sdpa_backward_workspace_size", "sdpa_backward", "sdpa_forward_f32",
            "sdpa_decode_workspace_size", "sdpa_decode", "mha_workspace_size",
            "mha_forward",
-           "mha_forward_noalloc", "linear_forward", "sdpa_device_check", "sdpa_status_string")
+           "mha_forward_noalloc", "linear_forward", "sdpa_set_kernel_choice", "sdpa_device_check",
+           "sdpa_status_string")
 
 # Size of the static workspace behind mha_forward_noalloc (SDPA_MHA_NOALLOC_MAX_WORKSPACE).
 MHA_NOALLOC_MAX_WORKSPACE = 32 << 20
@@ -87,6 +87,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.mha_forward_noalloc.restype = I
     lib.linear_forward.argtypes = [P, P, P, I, I, I, P]
     lib.linear_forward.restype = I
+    lib.sdpa_set_kernel_choice.argtypes = [I, I, I]
+    lib.sdpa_set_kernel_choice.restype = I
     lib.sdpa_device_check.argtypes = []
     lib.sdpa_device_check.restype = I
     lib.sdpa_status_string.argtypes = [I]
@@ -226,6 +228,32 @@ def linear_forward(x, w, y, m, n, k, stream=None) -> None:
     """y = x w for row-major bf16 matrices (see include/sdpa.h)."""
     _check(load_library().linear_forward(_addr(x), _addr(w), _addr(y), m, n, k, _stream(stream)),
            "linear_forward")
+
+
+ATTENTION_KERNELS = {None: 0, "one_tile": 1, "two_tile": 2}
+
+
+def sdpa_set_kernel_choice(attention_kernel=0, one_tile_keys=0, gemm_bn=0, lib=None) -> None:
+    """Pins kernel choices for every later call (0: choose by shape)."""
+    _check((lib or load_library()).sdpa_set_kernel_choice(attention_kernel, one_tile_keys, gemm_bn),
+           "sdpa_set_kernel_choice")
+
+
+class kernel_choice:
+    """Context manager: ``with kernel_choice(attention="one_tile", one_tile_keys=32): ...``
+    pins the choices inside the block and returns them to the shapes after it."""
+
+    def __init__(self, attention=None, one_tile_keys=0, gemm_bn=0, lib=None):
+        self.args = (ATTENTION_KERNELS[attention], int(one_tile_keys), int(gemm_bn))
+        self.lib = lib
+
+    def __enter__(self):
+        sdpa_set_kernel_choice(*self.args, lib=self.lib)
+        return self
+
+    def __exit__(self, *exc):
+        sdpa_set_kernel_choice(0, 0, 0, lib=self.lib)
+        return False
 
 
 def sdpa_device_check() -> None:

@@ -3,9 +3,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
-#include <cstdlib>
-#include <cstring>
 #include <cstdint>
 #include <mutex>
 
@@ -32,6 +31,11 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
+
+// Kernel pins set by sdpa_set_kernel_choice; 0 = choose by shape.
+std::atomic<int> g_pin_attention{0};       // 1 = one-tile kernel, 2 = two-tile kernel
+std::atomic<int> g_pin_one_tile_keys{0};   // 32 | 64
+std::atomic<int> g_pin_gemm_bn{0};         // 128 | 256
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -193,15 +197,10 @@ float effective_scale(float scale, int d_k) {
   return scale > 0.f ? scale : static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
 }
 
-// Kernel choice for tensor-core attention.  LIBSDPA_ATTENTION_KERNEL =
-// "one_tile" / "two_tile" pins it (tests use this to cover both kernels on
-// the same shapes); anything else, or unset, picks by shape.
-// Measured on GB300: the one-tile kernel is as fast or faster at d = 16, 32
-// and 64 for every shape tried, and at d = 128 while a query tile sees at
-// most 2048 keys; beyond that the two-tile kernel keeps a 1-3 % lead (n =
-// 4096 to 16384, causal or not).  A restricted window gives every query tile
-// the same short walk, and there the one-tile kernel leads up to r = 4096
-// (0.375 against 0.396 ms at b4 h16 n8192, causal).
+// Kernel choice for tensor-core attention.  sdpa_set_kernel_choice pins it
+// (tests use this to cover both kernels on the same shapes); otherwise it is
+// picked by shape, from the measurements on GB300 given with the thresholds
+// above.
 // Keys one 128-row query tile can see at most.
 long long key_span(int n_k, int win_left, int win_right) {
   return std::min<long long>(n_k, 1ll * win_left + win_right + 128);
@@ -209,9 +208,9 @@ long long key_span(int n_k, int win_left, int win_right) {
 
 bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
   if (d > 128) return true;
-  const char* e = std::getenv("LIBSDPA_ATTENTION_KERNEL");
-  if (e != nullptr && std::strcmp(e, "one_tile") == 0) return true;
-  if (e != nullptr && std::strcmp(e, "two_tile") == 0) return false;
+  const int pin = g_pin_attention.load(std::memory_order_relaxed);
+  if (pin == 1) return true;
+  if (pin == 2) return false;
   const long long span = key_span(n_k, win_left, win_right);
   const bool windowed = win_left != sdpa::kWindowUnbounded || win_right != sdpa::kWindowUnbounded;
   return span <= (windowed ? kOneTileMaxKeysWindowed : kOneTileMaxKeys);
@@ -222,15 +221,13 @@ bool use_one_tile_kernel(int d, int n_k, int win_left, int win_right) {
 // instead of two; that pays when the walk is short and the grid holds at
 // least two waves of two-CTA slots (measured on GB300: 6-17 % faster on
 // 1024-key walks and restricted windows, 15 % on b32 h16 256 x 384; 22 %
-// slower on b32 h8 n128, 2 % on 3072-key walks).  LIBSDPA_ONE_TILE_KEYS =
-// 32 | 64 pins it at d = 64.
+// slower on b32 h8 n128, 2 % on 3072-key walks).  sdpa_set_kernel_choice
+// pins it at d = 64.
 int one_tile_key_tile(int d, long long span, long long ctas) {
   if (d < 64) return 32;
   if (d > 64) return 64;
-  if (const char* e = std::getenv("LIBSDPA_ONE_TILE_KEYS")) {
-    const int v = std::atoi(e);
-    if (v == 32 || v == 64) return v;
-  }
+  const int pin = g_pin_one_tile_keys.load(std::memory_order_relaxed);
+  if (pin == 32 || pin == 64) return pin;
   return (span <= kOneTileShortKeys && ctas >= 4ll * sdpa::device_sm_count()) ? 32 : 64;
 }
 
@@ -300,7 +297,22 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
 
+namespace sdpa {
+int gemm_bn_pin() { return g_pin_gemm_bn.load(std::memory_order_relaxed); }
+}  // namespace sdpa
+
 extern "C" {
+
+sdpa_status sdpa_set_kernel_choice(int attention_kernel, int one_tile_keys, int gemm_bn) {
+  if (attention_kernel < 0 || attention_kernel > 2) return SDPA_ERR_INVALID_ARG;
+  if (one_tile_keys != 0 && one_tile_keys != 32 && one_tile_keys != 64)
+    return SDPA_ERR_INVALID_ARG;
+  if (gemm_bn != 0 && gemm_bn != 128 && gemm_bn != 256) return SDPA_ERR_INVALID_ARG;
+  g_pin_attention.store(attention_kernel, std::memory_order_relaxed);
+  g_pin_one_tile_keys.store(one_tile_keys, std::memory_order_relaxed);
+  g_pin_gemm_bn.store(gemm_bn, std::memory_order_relaxed);
+  return SDPA_OK;
+}
 
 sdpa_status sdpa_forward(const void* q, const void* k, const void* v, void* out, int b, int h,
                          int n_q, int n_k, int d_k, int d_v, int mask_kind,

@@ -18,7 +18,6 @@
 // when 256-column ones would leave half the SMs idle (the base model's
 // W^O, 4096 x 512 x 512).
 #include <atomic>
-#include <cstdlib>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -221,12 +220,10 @@ cudaError_t launch_bn(const GemmParams& p, int max_m, int max_n, cudaStream_t st
 }
 
 // Tile width: 256 columns, or 128 when 256-column tiles would not reach
-// half the SMs.  LIBSDPA_GEMM_BN = 256 | 128 pins it.
+// half the SMs.  sdpa_set_kernel_choice can pin it to 256 or 128.
 int gemm_tile_n(const GemmParams& p) {
-  if (const char* e = std::getenv("LIBSDPA_GEMM_BN")) {
-    const int v = std::atoi(e);
-    if (v == 256 || v == 128) return v;
-  }
+  const int pin = gemm_bn_pin();
+  if (pin == 256 || pin == 128) return pin;
   const int sms = device_sm_count();
   long long tiles = 0;
   for (int i = 0; i < p.num_problems; ++i)

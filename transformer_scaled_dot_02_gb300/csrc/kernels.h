@@ -65,6 +65,9 @@ cudaError_t launch_sdpa_one_tile(const SdpaTcParams& p, int head_dim, int key_ti
 // SMs of the current device (read once per device and cached).
 int device_sm_count();
 
+// Column tile of the projection GEMM pinned by sdpa_set_kernel_choice (0: by shape).
+int gemm_bn_pin();
+
 // One decoding step over a K/V cache on the CUDA cores, split across CTAs.
 struct DecodeParams {
   const uint16_t *q, *k, *v;  // bf16 BHSD: q [b,h,n_q,d], k/v [b,h,n_k,d]
