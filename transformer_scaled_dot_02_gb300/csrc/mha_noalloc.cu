@@ -14,6 +14,10 @@
 // first call should come before any stream capture.  The host-side name of
 // the array is only a stand-in for the symbol and is never passed to a kernel.
 //
+// The cached address belongs to the device's primary context: after
+// cudaDeviceReset (or anything else that destroys that context) the process
+// must not call the library again, as for the library's other per-device state.
+//
 // Every call shares the one array and it keeps the last call's contents.
 // Nothing in it needs to start at zero: each call writes the projected Q, K, V
 // and the heads completely before they are read.  Calls that overlap on the
@@ -72,12 +76,12 @@ extern "C" sdpa_status mha_forward_noalloc(const void* xq, const void* xkv, cons
                                            int d_k, int d_v, int mask_kind,
                                            const int32_t* kv_lengths, float scale,
                                            void* stream) {
-  if (b < 0 || n_q < 0 || n_k < 0 || h < 0 || d_k < 0 || d_v < 0) return SDPA_ERR_INVALID_ARG;
-  if (mha_workspace_size(b, n_q, n_k, h, d_k, d_v) > kNoAllocScratchBytes)
-    return SDPA_ERR_WORKSPACE;
   void* scratch = nullptr;
   const sdpa_status st = scratch_for_current_device(&scratch);
   if (st != SDPA_OK) return st;
+  // mha_forward checks every argument first, then returns SDPA_ERR_WORKSPACE
+  // (with nothing enqueued) when the problem needs more than the array holds,
+  // so a bad or unsupported argument gets the same status as from mha_forward.
   return mha_forward(xq, xkv, wq, wk, wv, wo, y, scratch, kNoAllocScratchBytes, b, n_q, n_k,
                      d_model, h, d_k, d_v, mask_kind, kv_lengths, scale, stream);
 }
