@@ -8,7 +8,9 @@ attention forward TFLOP/s with 4 b h n_q n_k d_k FLOP per pass, halved for the
 causal mask, whole job (all ranks).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload long_causal|restricted|decode|wide512|backward]
+                       [--workload long_causal|restricted|decode|wide512|backward|
+                                   tiny_f32|enc_base|enc_mha_base|dec_causal_base|
+                                   cross_big|cross_mha_big]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (no data-path collective); the timed region is bracketed by a barrier and the
 maximum over ranks is reported.  `--impl reference` times the CPU oracle on a
@@ -17,7 +19,13 @@ bounded sample of the same workload on the host cores (rank 0 only).
 `--workload` other than the default measures one of the widened rows with the
 same JSON line (value, roofline, e2e, clocks, an oracle baseline on a bounded
 sample): restricted self-attention (r = 1024), one decoding step against
-8192-token caches, Table 3's single 512-wide head, and the backward pass.
+8192-token caches, Table 3's single 512-wide head, and the backward pass; or
+one of the smaller configurations of the base and big models: the fp32 tiny
+case, the encoder's attention (core, and with its projections), the
+decoder's causal self-attention, and the big model's cross-attention (core,
+and with its projections).  These rotate over enough input sets that the
+inputs exceed L2, and report their roofline in GB/s against the algorithmic
+bytes (the multi-head lines: TFLOP/s of the whole call).
 """
 from __future__ import annotations
 
@@ -62,11 +70,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_sha() -> str:
-    """Hash of the kernel's code: comments and blank space are left out, so a
+def kernel_sha(source: str = KERNEL_SOURCE) -> str:
+    """Hash of a kernel's code: comments and blank space are left out, so a
     comment edit keeps the recorded DRAM traffic valid; any code change voids it."""
     import re
-    with open(KERNEL_SOURCE, encoding="utf-8") as f:
+    with open(source, encoding="utf-8") as f:
         src = f.read()
     src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
     src = re.sub(r"//[^\n]*", " ", src)
@@ -83,7 +91,11 @@ def recorded_traffic(workload: str):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("kernel_sha") != kernel_sha():
+    if not e:
+        return None
+    source = os.path.join(ROOT, "transformer_scaled_dot_02_gb300", "csrc",
+                          e.get("source_file", "sdpa_tc.cu"))
+    if e.get("kernel_sha") != kernel_sha(source):
         return None
     return e.get("bytes_per_launch")
 
@@ -374,6 +386,49 @@ def _time_steps(step, args, stream, pg, dev, local):
     return total, [a.elapsed_time(b) for a, b in zip(starts, ends)], sampler.summary()
 
 
+def _time_graph(step, args, pg, dev, local, cur):
+    """The K steps captured into one CUDA graph (after a warm-up), then one
+    replay timed between events on the replay stream, bracketed by a barrier
+    and a synchronize.  `cur[0]` is the stream the steps launch on: the
+    capture stream while capturing."""
+    import torch
+    import transformer_scaled_dot_02_gb300 as sd
+    side = torch.cuda.Stream(dev)
+    graph = torch.cuda.CUDAGraph()
+    saved = cur[0]
+    cur[0] = side.cuda_stream
+    try:
+        with torch.cuda.stream(side):
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(args.steps):
+                    step()
+    finally:
+        cur[0] = saved
+    torch.cuda.synchronize(dev)
+    sd.sdpa_device_check()
+    replay = torch.cuda.current_stream(dev)
+    graph.replay()      # one untimed replay
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    with sampler:
+        t0.record(replay)
+        graph.replay()
+        t1.record(replay)
+        torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    sd.sdpa_device_check()
+    return max_over_ranks(t0.elapsed_time(t1), pg, dev), sampler.summary()
+
+
 def _time_e2e(e2e_step, args, stream, pg, dev):
     import torch
     import transformer_scaled_dot_02_gb300 as sd
@@ -589,6 +644,247 @@ def run_row(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------ the smaller configurations (--workload)
+# The base and big models' shapes ("Attention Is All You Need", section 3.2.2
+# and Table 3): the fp32 tiny case, the encoder's attention (core and with its
+# projections), the decoder's causal self-attention and the big model's
+# cross-attention (core and with projections).
+CONFIG_WORKLOADS = {
+    "tiny_f32": "tiny_f32",
+    "enc_base": "enc_mha_base",
+    "enc_mha_base": "enc_mha_base",
+    "dec_causal_base": "dec_causal_base",
+    "cross_big": "cross_big",
+    "cross_mha_big": "cross_big",
+}
+ROTATE_BYTES = 256 << 20   # input sets rotate over at least this many bytes (L2: 129 MB)
+
+
+def sdpa_bytes(w) -> int:
+    """Algorithmic HBM bytes of one attention pass: Q, K, V read once, O written once."""
+    es = 4 if w.dtype == "f32" else 2
+    return es * w.b * w.h * (w.n_q * w.d_k + w.n_k * w.d_k + w.n_k * w.d_v + w.n_q * w.d_v)
+
+
+def mha_flops(w) -> float:
+    """Multi-head forward FLOP: the Q, K, V and W^O products plus the attention."""
+    dm = w.d_model
+    proj = 2.0 * w.b * (w.n_q * dm * w.h * w.d_k + w.n_k * dm * w.h * (w.d_k + w.d_v)
+                        + w.n_q * w.h * w.d_v * dm)
+    return proj + metric_flops(w)
+
+
+def run_config(args, world, rank, local):
+    """One of the smaller configurations, through the same JSON contract.  Each
+    step reads a different set of inputs, and the sets together exceed L2, so
+    no step finds its inputs cached by an earlier one."""
+    import torch
+    import transformer_scaled_dot_02_gb300 as sd
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    sd.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    cur = [stream.cuda_stream]   # the stream the calls go to (the capture stream while capturing)
+    kind = args.workload
+    w = synthetic.WORKLOADS[CONFIG_WORKLOADS[kind]]
+    peaks, peak_src = load_peaks()
+    mha = "_mha_" in kind
+    f32 = w.dtype == "f32"
+    tdt = torch.float32 if f32 else torch.bfloat16
+
+    if mha:
+        xq, xkv, wq, wk, wv, wo, lens = synthetic.mha_inputs(w)
+        self_attn = xkv is xq
+        per_set = (xq.size + (0 if self_attn else xkv.size) + w.b * w.n_q * w.d_model) * 2
+        sets = max(2, -(-ROTATE_BYTES // per_set))
+        hx = [_pinned(xq, tdt)] + ([] if self_attn else [_pinned(xkv, tdt)])
+        xs = [torch.empty((sets,) + tuple(t.shape), dtype=tdt, device=dev) for t in hx]
+        for x, h in zip(xs, hx):
+            x[:] = h.to(dev)
+        weights = [torch.from_numpy(a).to(tdt).to(dev) for a in (wq, wk, wv, wo)]
+        ys = torch.empty((sets, w.b, w.n_q, w.d_model), dtype=tdt, device=dev)
+        ld = None if lens is None else torch.from_numpy(lens).to(dev)
+        ld_ptr = None if ld is None else ld.data_ptr()
+        ws_bytes = sd.mha_workspace_size(w.b, w.n_q, w.n_k, w.h, w.d_k, w.d_v)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        w_ptrs = [t.data_ptr() for t in weights]
+        # device addresses of every set, taken once: the timed loop makes no tensors
+        ptrs = [(xs[0][i].data_ptr(), xs[0 if self_attn else 1][i].data_ptr(), ys[i].data_ptr())
+                for i in range(sets)]
+        counter = [0]
+
+        def call(i):
+            xq_p, xkv_p, y_p = ptrs[i]
+            sd.mha_forward(xq_p, xkv_p, *w_ptrs, y_p, ws.data_ptr(), ws_bytes, w.b, w.n_q, w.n_k,
+                           w.d_model, w.h, w.d_k, w.d_v, w.mask_kind, ld_ptr, 0.0, cur[0])
+
+        def step():
+            i = counter[0] % sets
+            counter[0] += 1
+            call(i)
+
+        hy = torch.empty(ys.shape[1:], dtype=tdt).pin_memory()
+        e2e_x = [x[0] for x in xs]
+
+        def e2e_step():
+            for dst, src in zip(e2e_x, hx):
+                dst.copy_(src, non_blocking=True)
+            call(0)
+            hy.copy_(ys[0], non_blocking=True)
+
+        h2d = sum(t.numel() * t.element_size() for t in hx)
+        d2h = hy.numel() * hy.element_size()
+        work, unit, launches = mha_flops(w), "TFLOP/s", 3
+        metric = "multi-head attention fwd TFLOP/s (Q/K/V projections, attention, W^O) (1 GPU)"
+        kernel = "gemm_bf16_tc (Q, K, V) + sdpa_fwd_one_tile + gemm_bf16_tc (W^O): one mha_forward"
+        bound, peak = "tensor", float(peaks["bf16_tflops"])
+        rot = "X and Y rotate over %d sets (%d MB); weights and workspace stay resident" % (
+            sets, sets * per_set >> 20)
+        desc = {"enc_mha_base": "base-model encoder multi-head self-attention: X [32,128,512], "
+                                "h8 d64, key padding 64..128",
+                "cross_mha_big": "big-model multi-head cross-attention: X_dec [32,256,1024], "
+                                 "X_enc [32,384,1024], h16 d64, key padding 192..384"}[kind]
+        sample_b = min(w.b, args.cpu_rows or (4 if w.d_model <= 512 else 2))
+
+        def oracle_sample():
+            import oracle
+            threads = oracle.default_threads()
+            rows = np.arange(sample_b * w.n_q, dtype=np.int64)
+            t = time.perf_counter()
+            oracle.mha(xq, xkv, wq, wk, wv, wo, w.h, w.d_k, w.d_v, w.mask_kind, lens, rows=rows,
+                       threads=threads)
+            dt = time.perf_counter() - t
+            return (mha_flops(w) * sample_b / w.b / dt / 1e12, threads,
+                    "every output row of the first %d of the %d batch entries (fp64 C oracle, %.1f s)"
+                    % (sample_b, w.b, dt))
+    else:
+        q, k, v, lens = synthetic.sdpa_inputs(w)
+        masks = [w.mask_kind] if not f32 else [synthetic.MASK_NONE, synthetic.MASK_CAUSAL]
+        per_set = sdpa_bytes(w)
+        step_bytes = per_set * len(masks)   # each call reads Q, K, V and writes O
+        sets = max(2, -(-ROTATE_BYTES // per_set))
+        hq, hk, hv = _pinned(q, tdt), _pinned(k, tdt), _pinned(v, tdt)
+        qs, ks, vs = (torch.empty((sets,) + tuple(h.shape), dtype=tdt, device=dev)
+                      for h in (hq, hk, hv))
+        for x, h in ((qs, hq), (ks, hk), (vs, hv)):
+            x[:] = h.to(dev)
+        os_ = torch.empty((sets, w.b, w.h, w.n_q, w.d_v), dtype=tdt, device=dev)
+        ld = None if lens is None else torch.from_numpy(lens).to(dev)
+        ld_ptr = None if ld is None else ld.data_ptr()
+        fwd = sd.sdpa_forward_f32 if f32 else sd.sdpa_forward
+        # device addresses of every set, taken once: the timed loop makes no tensors
+        ptrs = [(qs[i].data_ptr(), ks[i].data_ptr(), vs[i].data_ptr(), os_[i].data_ptr())
+                for i in range(sets)]
+        counter = [0]
+
+        def call(i):
+            for m in masks:
+                fwd(*ptrs[i], w.b, w.h, w.n_q, w.n_k, w.d_k, w.d_v, m, ld_ptr, 0.0, cur[0])
+
+        def step():
+            i = counter[0] % sets
+            counter[0] += 1
+            call(i)
+
+        ho = torch.empty(os_.shape[1:], dtype=tdt).pin_memory()
+
+        def e2e_step():
+            for dst, src in ((qs[0], hq), (ks[0], hk), (vs[0], hv)):
+                dst.copy_(src, non_blocking=True)
+            call(0)
+            ho.copy_(os_[0], non_blocking=True)
+
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size()
+        import dataclasses
+        work = sum(metric_flops(dataclasses.replace(w, mask_kind=m)) for m in masks)
+        unit, launches = "TFLOP/s", len(masks)
+        metric = METRIC if not f32 else "attention fwd TFLOP/s, fp32 (1 GPU)"
+        kernel = ("sdpa_fwd_f32_simt (unmasked and causal)" if f32 else
+                  "sdpa_fwd_one_tile<64, %d>" % (32 if kind == "cross_big" else 64))
+        bound, peak = "hbm", float(peaks["hbm_gbs"])
+        rot = "Q, K, V, O rotate over %d sets (%d MB)" % (sets, sets * per_set >> 20)
+        desc = {"tiny_f32": "tiny fp32 attention b1 h1 n16 d64, unmasked and causal (two calls)",
+                "enc_base": "base-model encoder attention core b32 h8 n128 d64 bf16, key padding "
+                            "64..128",
+                "dec_causal_base": "base-model decoder causal self-attention b16 h8 n512 d64 bf16",
+                "cross_big": "big-model cross-attention core b32 h16 n_q256 n_k384 d64 bf16, key "
+                             "padding 192..384"}[kind]
+        n_rows = w.b * w.h * w.n_q
+
+        def oracle_sample():
+            import oracle
+            threads = oracle.default_threads()
+            reps = max(1, args.cpu_rows or (2000 if f32 else 1))
+            t = time.perf_counter()
+            for _ in range(reps):
+                for m in masks:
+                    oracle.sdpa(q, k, v, m, lens, threads=threads)
+            dt = time.perf_counter() - t
+            return (work * reps / dt / 1e12, threads,
+                    "%severy one of the %d query rows of the workload (fp64 C oracle, %.1f s)"
+                    % ("%d passes over " % reps if reps > 1 else "", n_rows, dt))
+
+    # Eager: one C-ABI call per step from Python, an event pair around each.
+    eager_ms, eager_launch_ms, _ = _time_steps(step, args, stream, pg, dev, local)
+    # Timed: the same K steps captured once into a CUDA graph and replayed
+    # between two events, so host launch gaps do not enter the device time.
+    total_ms, clocks = _time_graph(step, args, pg, dev, local, cur)
+    launch_ms = [total_ms / args.steps]
+    e2e_ms, e2e_steps = _time_e2e(e2e_step, args, stream, pg, dev)
+    value = world * work * args.steps / (total_ms * 1e-3) / 1e12
+    mean_ms = float(np.mean(launch_ms))
+    roof = {"bound": bound, "peak": peak, "kernel": kernel,
+            "launch_ms_mean": round(mean_ms, 5), "launch_ms_min": round(float(np.min(launch_ms)), 5)}
+    if bound == "hbm":
+        gbs = step_bytes / (mean_ms * 1e-3) / 1e9
+        roof.update({"achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "peak_source": "%s hbm_gbs" % peak_src,
+                     "algorithmic_bytes": step_bytes,
+                     "tflops": round(work / (mean_ms * 1e-3) / 1e12, 3),
+                     "traffic": recorded_traffic(kind)})
+    else:
+        tf = work / (mean_ms * 1e-3) / 1e12
+        roof.update({"achieved": round(tf, 2), "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                     "peak_source": "%s bf16_tflops (burst)" % peak_src, "traffic": None})
+    line = {
+        "metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if f32 else "bf16", "data": "synthetic",
+        "config": {"workload": desc, "b": w.b, "h": w.h, "n_q": w.n_q, "n_k": w.n_k,
+                   "d_k": w.d_k, "d_v": w.d_v, "d_model": w.d_model if mha else None,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: " + rot},
+        "roofline": roof,
+        "e2e": {"value": round(world * work * e2e_steps / (e2e_ms * 1e-3) / 1e12, 4), "unit": unit,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "steps": e2e_steps, "path": "pinned host inputs copied in, the C-ABI call, "
+                                            "the output copied back, one stream"},
+        "gpu_launches": args.steps * launches,
+        "timing": "K steps captured in one CUDA graph, replayed between two events; "
+                  "eager (one call per step from Python): %.5f ms per step, %.5f ms per "
+                  "step between its own events" % (eager_ms / args.steps,
+                                                    float(np.mean(eager_launch_ms))),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        val, threads, sample = oracle_sample()
+        line["cpu_baseline"] = {"value": val, "unit": unit, "cores": threads, "kind": "oracle",
+                                "cpu": cpu_model(), "sample": sample}
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------- oracle timing
 def _sample_rows(w, n_rows, seed):
     rng = np.random.default_rng(seed)
@@ -686,8 +982,10 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=("long_causal",) + ROW_WORKLOADS, default="long_causal",
-                    help="the headline workload, or one of the widened rows")
+    ap.add_argument("--workload", choices=("long_causal",) + ROW_WORKLOADS + tuple(CONFIG_WORKLOADS),
+                    default="long_causal",
+                    help="the headline workload, one of the widened rows, or one of the smaller "
+                         "configurations")
     ap.add_argument("--cpu-rows", type=int, default=None,
                     help="size of the oracle's timed CPU sample (query rows; the backward: "
                          "a causal prefix length)")
@@ -702,6 +1000,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank, local)
+    elif args.workload in CONFIG_WORKLOADS:
+        run_config(args, world, rank, local)
     elif args.workload != "long_causal":
         run_row(args, world, rank, local)
     else:

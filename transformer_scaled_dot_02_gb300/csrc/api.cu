@@ -97,6 +97,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr long long kOneTileMaxKeys = 3072;
 constexpr long long kOneTileShortKeys = 2048;   // d = 64: 32-key tiles up to this span
 constexpr long long kOneTileMaxKeysWindowed = 4352;   // r up to 4096
+constexpr long long kKvBytesOneGroup = 32ll << 20;    // K + V of all heads: one work group
 
 // 4-D bf16 map over (d, n, h, b) with the given element strides of n, h, b;
 // boxes of min(d, 64) x 128, swizzled at the row width, zero fill outside.
@@ -279,6 +280,16 @@ sdpa_status launch_attention_tc(const void* q, const void* k, const void* v, voi
   p.win_left = win_left;
   p.win_right = win_right;
   p.lse = lse;
+  // One-tile kernel: heads in groups of 8 keep their K and V in L2 on long
+  // sequences; when the K and V of all heads fit in a quarter of L2 the
+  // whole grid is one group, so the longest causal query tiles of every
+  // head start first and the short ones fill in behind them.
+  p.head_group = 8;
+  if (one_tile) {
+    const long long kv_bytes = 2ll * b * h * n_k * (d_k + d_v);
+    const int units = b * h * (d_k == 512 ? 2 : 1);
+    if (kv_bytes <= kKvBytesOneGroup) p.head_group = units;
+  }
   const cudaError_t err = one_tile ? sdpa::launch_sdpa_one_tile(p, d_k, kv_rows, stream)
                                    : sdpa::launch_sdpa_tc(p, d_k, d_v, stream);
   return err == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;

@@ -27,6 +27,9 @@ struct SdpaTcParams {
   int win_left, win_right;
   float* lse;                 // optional [b, h, n_q] natural log-sum-exp per row
   int pdl = 0;                // launched with a programmatic dependency on the previous kernel
+  // One-tile kernel: CTAs take (head, d_v slice) units in groups of this
+  // many, the longest query tiles of a group first (>= 1).
+  int head_group = 8;
 };
 constexpr int kWindowUnbounded = 1 << 30;
 

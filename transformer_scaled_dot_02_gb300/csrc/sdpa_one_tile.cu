@@ -43,7 +43,6 @@ constexpr int kBlockM = 128;
 constexpr int kThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kHeadGroup = 8;              // (head, d_v slice) units sharing L2
 constexpr float kRescaleThreshold = 8.0f;  // log2 units, as in the 64/128 kernel
 
 // KT: keys per tile, 32 or 64 (64 for d >= 128).
@@ -135,21 +134,25 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work: units = (batch*head, d_v slice) in groups of kHeadGroup; inside
-  // a group the longest query tiles (causal) go first.
+  // ---- work: units = (batch*head, d_v slice) in groups of p.head_group;
+  // inside a group the longest query tiles (causal) go first.  Groups of a
+  // few units keep their K and V in L2 on long sequences; when every unit's
+  // K and V fit in L2 together the host makes one group of all units, so the
+  // longest tiles of the whole grid start first.
   const int units = p.b * p.h * C::kChunks;
   const int nqb = p.num_q_blocks;
-  const int group_ctas = kHeadGroup * nqb;
-  const int full_groups = units / kHeadGroup;
+  const int head_group = p.head_group;
+  const int group_ctas = head_group * nqb;
+  const int full_groups = units / head_group;
   const int idx = static_cast<int>(blockIdx.x);
-  int g = idx / group_ctas, r = idx % group_ctas, in_group = kHeadGroup;
+  int g = idx / group_ctas, r = idx % group_ctas, in_group = head_group;
   if (g >= full_groups) {
     g = full_groups;
     r = idx - full_groups * group_ctas;
-    in_group = units - full_groups * kHeadGroup;
+    in_group = units - full_groups * head_group;
   }
   const int qb = nqb - 1 - r / in_group;
-  const int unit = g * kHeadGroup + r % in_group;
+  const int unit = g * head_group + r % in_group;
   const int chunk = unit % C::kChunks;
   const int bh = unit / C::kChunks;
   const int bi = bh / p.h;
