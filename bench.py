@@ -477,6 +477,9 @@ def run_row(args, world, rank, local):
     else:
         w = synthetic.WORKLOADS[{"restricted": "long_restricted", "decode": "decode_big",
                                  "wide512": "wide_d512"}[kind]]
+    if kind == "decode" and args.decode_queries != w.n_q:
+        import dataclasses
+        w = dataclasses.replace(w, n_q=args.decode_queries)
     q, k, v, _ = synthetic.sdpa_inputs(w)
     hq, hk, hv = _pinned(q, bf), _pinned(k, bf), _pinned(v, bf)
     qd, kd, vd = hq.to(dev), hk.to(dev), hv.to(dev)
@@ -538,7 +541,8 @@ def run_row(args, world, rank, local):
         ins, outs = [(qd, hq)], [(ho, od)]
         work = 2.0 * bh * w.n_k * (w.d_k + w.d_v)    # K and V caches, bf16, read once
         metric = "decode step: K/V cache read GB/s (1 GPU)"
-        desc = "one decoding step, b32 h16, 1 query against 8192-token K/V caches, d128 bf16"
+        desc = ("one decoding step, b32 h16, %d quer%s against 8192-token K/V caches, d128 bf16"
+                % (w.n_q, "y" if w.n_q == 1 else "ies"))
         kernel = "sdpa_decode_split + sdpa_decode_combine"
         unit, bound, peak = "GB/s", "hbm", float(peaks["hbm_gbs"])
         launches = 2
@@ -991,6 +995,8 @@ def main():
                          "a causal prefix length)")
     ap.add_argument("--ref-rows", type=int, default=2048,
                     help="query rows per step of the reference (oracle) arm")
+    ap.add_argument("--decode-queries", type=int, default=1,
+                    help="new queries per sequence and head of the decode workload (1 to 8)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

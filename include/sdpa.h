@@ -181,10 +181,14 @@ sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* 
  *   n_q positions of each sequence, so query i sees keys j <= len_b - n_q + i
  *   (the causal rule of section 3.2.3); a query with no visible key gives 0.
  *   workspace: device buffer of ws_bytes >= sdpa_decode_workspace_size(...)
- *   (may be NULL when that size is 0), 16-byte aligned, caller-owned.
+ *   (may be NULL when that size is 0), 16-byte aligned, caller-owned.  The
+ *   size depends on the current device's SM count: ask on the device the
+ *   step runs on.
  * The step is bound by reading the caches once from HBM; it runs on the CUDA
  * cores with the cache split across CTAs and a merge of the partial softmax
- * states.  Supported: d_k == d_v in {64, 128}, b * h <= 65535.
+ * states.  Supported (else SDPA_ERR_UNSUPPORTED), the head shapes of the
+ * paper's Table 3: d_k == d_v in {16, 32, 64, 128, 256, 512}, and d_k in
+ * {16, 32} with d_v = 64 (rows (B)); b * h <= 65535.
  */
 size_t sdpa_decode_workspace_size(int b, int h, int n_q, int n_k, int d_v);
 

@@ -21,12 +21,15 @@ def _gpu(q, k, v, lens=None, scale=0.0):
     return host(out)
 
 
-@pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("n_q", [1, 2, 4, 5, 8])
+@pytest.mark.parametrize("d_k,d_v", [(16, 16), (32, 32), (64, 64), (128, 128), (256, 256),
+                                     (512, 512), (16, 64), (32, 64)])
+@pytest.mark.parametrize("n_q", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("b,h,n_k", [(1, 1, 1), (2, 3, 37), (4, 2, 1000), (1, 4, 5000)])
-def test_decode_shapes(d, n_q, b, h, n_k):
-    rng = np.random.default_rng(9000 + d + 10 * n_q + n_k)
-    q, k, v = _rand(rng, (b, h, n_q, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+def test_decode_shapes(d_k, d_v, n_q, b, h, n_k):
+    """Every head shape of Table 3 (rows (A), (B), (C)), one to eight new
+    queries, caches of 1 to 5000 keys (one or many splits)."""
+    rng = np.random.default_rng(9000 + d_k + 3 * d_v + 10 * n_q + n_k)
+    q, k, v = _rand(rng, (b, h, n_q, d_k)), _rand(rng, (b, h, n_k, d_k)), _rand(rng, (b, h, n_k, d_v))
     lens = rng.integers(0, n_k + 1, size=b).astype(np.int32)
     lens[0] = n_k
     got = _gpu(q, k, v, lens)
@@ -60,7 +63,20 @@ def test_decode_matches_causal_attention_rows():
     assert parity_err(step, full[:, :, n - n_q:]) <= TOL_BF16
 
 
-@pytest.mark.parametrize("n_q", [1, 4])
+def test_decode_unscaled_and_sharp():
+    """scale 1 with large queries: peaked weights that move the running max
+    from tile to tile."""
+    rng = np.random.default_rng(95)
+    b, h, n_q, n_k, d = 2, 2, 4, 3000, 64
+    q = _rand(rng, (b, h, n_q, d), 0.4)
+    k = synthetic.round_to_bf16(_rand(rng, (b, h, n_k, d)) *
+                                np.linspace(0.2, 2.0, n_k, dtype=np.float32)[None, None, :, None])
+    v = _rand(rng, (b, h, n_k, d))
+    got = _gpu(q, k, v, None, 1.0)
+    assert parity_err(got, oracle.decode(q, k, v, None, 1.0)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("n_q", [1, 4, 8])
 def test_decode_workload(n_q):
     """Decoding step at serving size: 32 sequences, 16 heads, d=128, caches of
     8192 positions filled to lengths in [4096, 8192]."""

@@ -184,16 +184,17 @@ def sdpa_decode(q, k, v, out, workspace, ws_bytes, b, h, n_q, n_k, d_k, d_v, kv_
 
 def decode_step(q, k, v, kv_lengths=None, scale=0.0, workspace=None, stream=None):
     """Allocates the output (and, if needed, the workspace) with torch and
-    calls sdpa_decode on q [b,h,n_q,d], k/v [b,h,n_k,d] bf16 tensors."""
+    calls sdpa_decode on q [b,h,n_q,d_k], k [b,h,n_k,d_k], v [b,h,n_k,d_v]
+    bf16 tensors."""
     import torch
-    b, h, n_q, d = q.shape
-    n_k = k.shape[2]
-    need = sdpa_decode_workspace_size(b, h, n_q, n_k, d)
+    b, h, n_q, d_k = q.shape
+    n_k, d_v = k.shape[2], v.shape[3]
+    need = sdpa_decode_workspace_size(b, h, n_q, n_k, d_v)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    out = torch.empty((b, h, n_q, d), dtype=q.dtype, device=q.device)
+    out = torch.empty((b, h, n_q, d_v), dtype=q.dtype, device=q.device)
     sdpa_decode(q, k, v, out, workspace, 0 if workspace is None else workspace.numel(), b, h, n_q,
-                n_k, d, d, kv_lengths, scale, stream)
+                n_k, d_k, d_v, kv_lengths, scale, stream)
     return out
 
 

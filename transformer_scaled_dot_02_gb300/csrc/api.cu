@@ -306,6 +306,12 @@ bool fill_gemm_problem(GemmProblem* pr, const void* x, const void* w, void* y, i
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Decode: enough splits for about kDecodeWaves waves of the shape's resident
+// CTAs; the workspace is sized for the most any shape can take.
+int decode_target_ctas(int resident) {
+  return sdpa::kDecodeWaves * resident * sdpa::device_sm_count();
+}
+
 }  // namespace
 
 namespace sdpa {
@@ -493,7 +499,8 @@ sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* 
 
 size_t sdpa_decode_workspace_size(int b, int h, int n_q, int n_k, int d_v) {
   if (b < 1 || h < 1 || n_q < 1 || n_k < 0 || d_v < 1) return 0;
-  const int splits = sdpa::decode_splits(b, h, n_k);
+  const int splits =
+      sdpa::decode_splits(b, h, n_k, decode_target_ctas(sdpa::kDecodeMaxResident));
   if (splits <= 1) return 0;
   const size_t rows = static_cast<size_t>(b) * h * n_q;
   return round256(static_cast<size_t>(splits) * rows * d_v * 4) +
@@ -510,8 +517,9 @@ sdpa_status sdpa_decode(const void* q, const void* k, const void* v, void* out, 
   if (kv_lengths != nullptr && (reinterpret_cast<uintptr_t>(kv_lengths) & 3u) != 0)
     return SDPA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return SDPA_ERR_INVALID_ARG;
-  if (d_k != d_v || (d_k != 64 && d_k != 128) || n_q > sdpa::kDecodeMaxQueries ||
-      1ll * b * h > 65535 || n_k >= sdpa::kWindowUnbounded)
+  if (!sdpa::decode_supports(d_k, d_v) || n_q > sdpa::kDecodeMaxQueries ||
+      1ll * b * h > 65535 || n_k >= sdpa::kWindowUnbounded ||
+      1ll * b * h * n_k * (d_k > d_v ? d_k : d_v) > (1ll << 38))
     return SDPA_ERR_UNSUPPORTED;
   const size_t need = sdpa_decode_workspace_size(b, h, n_q, n_k, d_v);
   if (need > 0 && (workspace == nullptr || !aligned16(workspace) || ws_bytes < need))
@@ -520,26 +528,31 @@ sdpa_status sdpa_decode(const void* q, const void* k, const void* v, void* out, 
   sdpa_status st = current_device(&status);
   if (st != SDPA_OK) return st;
   sdpa::DecodeParams p;
+  const int tk = sdpa::decode_keys_per_tile(d_k);
+  if (!make_map_4d(&p.tm_k, k, d_k, n_k, h, b, d_k, 1ll * n_k * d_k, 1ll * h * n_k * d_k, tk) ||
+      !make_map_4d(&p.tm_v, v, d_v, n_k, h, b, d_v, 1ll * n_k * d_v, 1ll * h * n_k * d_v, tk))
+    return SDPA_ERR_CUDA;
   p.q = static_cast<const uint16_t*>(q);
-  p.k = static_cast<const uint16_t*>(k);
-  p.v = static_cast<const uint16_t*>(v);
   p.out = static_cast<uint16_t*>(out);
   p.kv_lengths = kv_lengths;
+  p.status = status;
   p.b = b;
   p.h = h;
   p.n_q = n_q;
   p.n_k = n_k;
-  p.splits = sdpa::decode_splits(b, h, n_k);
+  // never more splits than the workspace was sized for (resident <= the maximum)
+  p.splits = sdpa::decode_splits(b, h, n_k,
+                                 decode_target_ctas(sdpa::decode_resident_ctas(d_k, d_v)));
   const int per = (n_k + p.splits - 1) / p.splits;
-  p.keys_per_split = ((per + 7) / 8) * 8;
+  p.keys_per_split = (per + tk - 1) / tk * tk;
   const size_t rows = static_cast<size_t>(b) * h * n_q;
-  p.part_o = need > 0 ? static_cast<float*>(workspace) : nullptr;
-  p.part_ml = need > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                                  round256(static_cast<size_t>(p.splits) * rows *
-                                                           d_v * 4))
-                       : nullptr;
+  p.part_o = p.splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.part_ml = p.splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                      round256(static_cast<size_t>(p.splits) *
+                                                               rows * d_v * 4))
+                           : nullptr;
   p.scale_log2 = effective_scale(scale, d_k) * 1.4426950408889634f;
-  return sdpa::launch_sdpa_decode(p, d_k, static_cast<cudaStream_t>(stream)) == cudaSuccess
+  return sdpa::launch_sdpa_decode(p, d_k, d_v, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SDPA_OK
              : SDPA_ERR_CUDA;
 }

@@ -73,21 +73,33 @@ int gemm_bn_pin();
 
 // One decoding step over a K/V cache on the CUDA cores, split across CTAs.
 struct DecodeParams {
-  const uint16_t *q, *k, *v;  // bf16 BHSD: q [b,h,n_q,d], k/v [b,h,n_k,d]
-  uint16_t* out;              // bf16 [b,h,n_q,d]
-  float* part_o;              // [splits][b*h*n_q][d]  (splits > 1)
+  CUtensorMap tm_k, tm_v;     // 4-D (d, n, h, b) bf16 maps of the caches, boxes of
+                              // min(d, 64) columns x decode_keys_per_tile(d_k) rows
+  const uint16_t* q;          // bf16 [b,h,n_q,d_k]
+  uint16_t* out;              // bf16 [b,h,n_q,d_v]
+  float* part_o;              // [splits][b*h*n_q][d_v]  (splits > 1)
   float* part_ml;             // [splits][b*h*n_q][2]  (splits > 1)
   const int32_t* kv_lengths;  // device [b] or null
+  unsigned* status;           // device error word
   int b, h, n_q, n_k;
   int splits, keys_per_split;
   float scale_log2;
 };
 constexpr int kDecodeMaxQueries = 8;
-constexpr int kDecodeTargetCtas = 152 * 4;   // four CTAs per SM of a GB300
 constexpr int kDecodeMinKeysPerSplit = 256;
 constexpr int kDecodeMaxSplits = 256;
-int decode_splits(int b, int h, int n_k);
-cudaError_t launch_sdpa_decode(const DecodeParams& p, int head_dim, cudaStream_t stream);
+constexpr int kDecodeWaves = 4;             // split CTAs: about this many waves of resident CTAs
+constexpr int kDecodeMaxResident = 4;       // resident split CTAs per SM, at most
+// (d_k, d_v) pairs the decode kernels are built for: every Table 3 head shape.
+bool decode_supports(int d_k, int d_v);
+// Keys per tile (TMA box rows) of the decode kernel for a key size.
+int decode_keys_per_tile(int d_k);
+// Split CTAs of one shape that share an SM.
+int decode_resident_ctas(int d_k, int d_v);
+// Splits of each sequence's cache for about target_ctas CTAs in all (each
+// split at least kDecodeMinKeysPerSplit keys, at most kDecodeMaxSplits).
+int decode_splits(int b, int h, int n_k, int target_ctas);
+cudaError_t launch_sdpa_decode(const DecodeParams& p, int d_k, int d_v, cudaStream_t stream);
 
 // Gradients of attention (bf16 BHSD tensors, fp32 accumulation).
 struct SdpaBwdParams {
