@@ -88,7 +88,7 @@ def _check(q, k, v, do, mask, lens, r=0, scale=0.0):
     return errs
 
 
-@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("mask", [0, 1, 2, 3])
 def test_backward_shapes(d, mask):
     b, h, n = 2, 3, 300
@@ -98,9 +98,10 @@ def test_backward_shapes(d, mask):
     _check(q, k, v, do, mask, lens)
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("n", [1, 17, 127, 128, 129, 256, 383])
-def test_backward_ragged_lengths(n):
-    q, k, v, do = _inputs(9100 + n, 1, 2, n, n, 128)
+def test_backward_ragged_lengths(d, n):
+    q, k, v, do = _inputs(9100 + n + d, 1, 2, n, n, d)
     _check(q, k, v, do, 1, None)
 
 
@@ -186,6 +187,23 @@ def test_backward_long_causal():
     assert max(errs.values()) <= TOL_BF16
 
 
+@pytest.mark.parametrize("r", [1, 64, 129, 300])
+@pytest.mark.parametrize("mask", [0, 1, 3])
+def test_backward_wide_head_restricted(r, mask):
+    """Table 3, row (A): two heads of 256 at d_model 512 (dK, dV, dQ in two
+    128-column chunks, one CTA each), with the restricted window."""
+    b, h, n = 2, 2, 520
+    q, k, v, do = _inputs(9250 + r + mask, b, h, n, n, 256)
+    lens = np.array([n, 290], np.int32) if mask & 2 else None
+    _check(q, k, v, do, mask, lens, r=r)
+
+
+def test_backward_wide_head_long_causal():
+    """d = 256, causal n = 2048 (16 key tiles, up to 32 query steps each)."""
+    q, k, v, do = _inputs(9650, 1, 2, 2048, 2048, 256, std=0.5)
+    _check(q, k, v, do, 1, None)
+
+
 @pytest.mark.parametrize("d", [16, 32])
 @pytest.mark.parametrize("n", [1, 65, 300])
 def test_backward_small_heads(d, n):
@@ -226,10 +244,10 @@ def test_backward_rejects_bad_arguments():
     ws = t.empty(sd.sdpa_backward_workspace_size(1, 1, 64, 64), dtype=t.uint8, device="cuda")
     with pytest.raises(sd.SdpaError, match="WORKSPACE"):
         sd.sdpa_backward(x, x, x, x, x, lse, x, x, x, ws, ws.numel() - 16, 1, 1, 64, 64, 64, 64)
-    x256 = t.zeros((1, 1, 64, 256), dtype=t.bfloat16, device="cuda")
+    x512 = t.zeros((1, 1, 64, 512), dtype=t.bfloat16, device="cuda")
     with pytest.raises(sd.SdpaError, match="UNSUPPORTED"):
-        sd.sdpa_backward(x256, x256, x256, x256, x256, lse, x256, x256, x256, ws, ws.numel(), 1, 1,
-                         64, 64, 256, 256)
+        sd.sdpa_backward(x512, x512, x512, x512, x512, lse, x512, x512, x512, ws, ws.numel(), 1, 1,
+                         64, 64, 512, 512)
     with pytest.raises(sd.SdpaError, match="INVALID_ARG"):
         sd.sdpa_backward(x, x, x, x, None, lse, x, x, x, ws, ws.numel(), 1, 1, 64, 64, 64, 64)
     # unequal head sizes other than Table 3's rows (B)

@@ -123,16 +123,17 @@ bool make_map_4d(CUtensorMap* map, const void* base, int d, int n, int h, int b,
 }
 
 // 3-D fp32 map over the backward's dQ accumulator [bh][n_q][d]: boxes of
-// min(32, d) columns x 64 rows, unswizzled, for the kernel's tensor
+// min(32, d) columns x box_rows rows, unswizzled, for the kernel's tensor
 // reduce-adds; rows past n_q are clipped by the copy engine.
-bool make_map_dq(CUtensorMap* map, const float* base, int d, int n_q, int bh) {
+bool make_map_dq(CUtensorMap* map, const float* base, int d, int n_q, int bh, int box_rows) {
   auto enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_q > 0 ? n_q : 1),
                               static_cast<cuuint64_t>(bh)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                  static_cast<cuuint64_t>(n_q > 0 ? n_q : 1) * d * 4};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 32 ? d : 32), 64, 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d < 32 ? d : 32),
+                             static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -187,10 +188,10 @@ bool tc_head_sizes(int d_k, int d_v) {
   return d_v == 64 && (d_k == 16 || d_k == 32);
 }
 
-// Head shapes the backward supports: equal sizes up to 128 and Table 3's
+// Head shapes the backward supports: equal sizes up to 256 and Table 3's
 // rows (B), where the keys are smaller than the values.
 bool bwd_head_sizes(int d_k, int d_v) {
-  if (d_k == d_v) return d_k == 16 || d_k == 32 || d_k == 64 || d_k == 128;
+  if (d_k == d_v) return d_k == 16 || d_k == 32 || d_k == 64 || d_k == 128 || d_k == 256;
   return d_v == 64 && (d_k == 16 || d_k == 32);
 }
 
@@ -429,7 +430,8 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
       !make_map_4d(&bp.tm_v, v, d_v, n_k, h, b, dv_, n_k * dv_, h * n_k * dv_) ||
       !make_map_4d(&bp.tm_do, dout, d_v, n_q, h, b, dv_, n_q * dv_, h * n_q * dv_, q_rows))
     return SDPA_ERR_CUDA;
-  if (!make_map_dq(&bp.tm_dq, dq_acc, d_k, n_q, b * h)) return SDPA_ERR_CUDA;
+  // heads wider than 128 reduce dQ 32 query rows at a time
+  if (!make_map_dq(&bp.tm_dq, dq_acc, d_k, n_q, b * h, d_k > 128 ? 32 : 64)) return SDPA_ERR_CUDA;
   bp.neg_lse2 = neg_lse2;
   bp.neg_dvec = neg_dvec;
   bp.dq_acc = dq_acc;

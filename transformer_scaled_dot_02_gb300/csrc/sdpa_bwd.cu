@@ -105,8 +105,6 @@ struct Lay {
   static constexpr int kQBox = 64 * kRowBytes;              // kBoxCols x 64 queries
   static constexpr int kKVTile = kBoxes * kKVBox;
   static constexpr int kQTile = kBoxes * kQBox;
-  static constexpr int kHalfCols = D / 2;                   // dK / dV columns per compute warp
-  static constexpr int kChunk = kHalfCols < 32 ? kHalfCols : 32;
   static_assert(kQBox % 1024 == 0 && kKVBox % 1024 == 0, "align");
 };
 
@@ -121,25 +119,37 @@ struct Cfg {
   using LK = Lay<DK>;
   using LV = Lay<DV>;
   static constexpr bool kPairDq = DK + DV <= 128;
-  static constexpr int kDsBufs = kPairDq ? 4 : 2;
-  static constexpr int kDqRows = kPairDq ? 2 * kBN : kBN;   // staged dQ rows per epilogue warp
+  // Heads wider than 128 (d_k = d_v = 256): dK, dV and dQ in 128-column
+  // chunks, one CTA per chunk, each recomputing S^T and dP^T over the whole
+  // head.  K and V stay resident (128 KB), which leaves room for one stage
+  // of Q and dO and one dS^T buffer, so the steps run in order: products of
+  // step i, then the loads and scores of step i + 1.
+  static constexpr bool kWide = DK > 128;
+  static constexpr int kColsK = kWide ? 128 : DK;           // dK / dQ columns of a CTA
+  static constexpr int kColsV = kWide ? 128 : DV;           // dV columns of a CTA
+  static constexpr int kChunks = kWide ? DK / 128 : 1;      // CTAs per key tile
+  static constexpr int kStagesQ = kWide ? 1 : kStages;      // Q / dO stages
+  static constexpr int kDsBufs = kPairDq ? 4 : (kWide ? 1 : 2);
+  // staged dQ rows per epilogue warp (the wide heads stage 32 query rows at a time)
+  static constexpr int kDqRows = kPairDq ? 2 * kBN : (kWide ? 32 : kBN);
   static constexpr uint32_t kDqCol = 384;                   // paired dQ^T: 128 columns
   static constexpr int kDCols = DK < 32 ? DK : 32;          // dQ columns per epilogue warp
   static constexpr int kKOff = 0;
   static constexpr int kVOff = LK::kKVTile;
   static constexpr int kStageOff = kVOff + LV::kKVTile;     // Q then dO, per stage
   static constexpr int kStageBytes = LK::kQTile + LV::kQTile;
-  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;   // dS^T buffers
+  static constexpr int kDsOff = kStageOff + kStagesQ * kStageBytes;   // dS^T buffers
   static constexpr int kStagingOff = kDsOff + kDsBufs * kDsTile;  // 4 warps x [kDqRows][kDCols] fp32
   static constexpr int kVecOff = kStagingOff + 4 * kDqRows * kDCols * 4;
-  static constexpr int kBarOff = kVecOff + kStages * kVecBytes;
+  static constexpr int kBarOff = kVecOff + kStagesQ * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-  static constexpr uint32_t kIdescDV = idesc_bf16(kBM, DV, false, true);  // dV (A in TMEM)
-  static constexpr uint32_t kIdescDK = idesc_bf16(kBM, DK, false, true);  // dK (A in TMEM)
-  static constexpr uint32_t kDkCol = 256 + DV;
+  static constexpr uint32_t kIdescDV = idesc_bf16(kBM, kColsV, false, true);  // dV (A in TMEM)
+  static constexpr uint32_t kIdescDK = idesc_bf16(kBM, kColsK, false, true);  // dK (A in TMEM)
+  static constexpr uint32_t kDkCol = 256 + kColsV;
   static_assert(kSmemBytes <= 232448, "shared memory");
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
-  static_assert(kDkCol + DK <= (kPairDq ? kDqCol : 512u), "tensor memory");
+  static_assert(kDkCol + kColsK <= (kPairDq ? kDqCol : 512u), "tensor memory");
+  static_assert(!kWide || (DK == DV && DK % 128 == 0), "wide heads: equal sizes, 128-column chunks");
   // dQ^T's 128 lanes read 128 / kBoxCols boxes from K onward: all inside the CTA's memory
   static_assert((128 / LK::kBoxCols) * LK::kKVBox <= kBarOff, "dQ^T reads in bounds");
 };
@@ -207,17 +217,20 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh_count = p.b * p.h;
-  // Heads in groups of kHeadGroup, each group's key tiles in ascending order
-  // (the longest causal walks first): the dQ accumulator and the Q / dO rows
-  // of the heads in flight stay in L2.
+  // Column chunk of dK, dV and dQ (wide heads; else 0), then heads in groups
+  // of kHeadGroup, each group's key tiles in ascending order (the longest
+  // causal walks first): the dQ accumulator and the Q / dO rows of the heads
+  // in flight stay in L2.
+  const int chunk = static_cast<int>(blockIdx.x) % C::kChunks;
+  const int idx = static_cast<int>(blockIdx.x) / C::kChunks;
   const int group_ctas = kHeadGroup * p.num_kv_tiles;
   const int full_groups = bh_count / kHeadGroup;
-  int g = static_cast<int>(blockIdx.x) / group_ctas;
-  int rr = static_cast<int>(blockIdx.x) % group_ctas;
+  int g = idx / group_ctas;
+  int rr = idx % group_ctas;
   int heads_in_group = kHeadGroup;
   if (g >= full_groups) {
     g = full_groups;
-    rr = static_cast<int>(blockIdx.x) - full_groups * group_ctas;
+    rr = idx - full_groups * group_ctas;
     heads_in_group = bh_count - full_groups * kHeadGroup;
   }
   const int jt = rr / heads_in_group;
@@ -276,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * LV::kKVBox, c * LV::kBoxCols, key0, hi, bi);
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % kStages;
-        const uint32_t use = static_cast<uint32_t>(it / kStages);
-        if (it >= kStages && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
+        const int s = it % C::kStagesQ;
+        const uint32_t use = static_cast<uint32_t>(it / C::kStagesQ);
+        if (it >= C::kStagesQ && !mbar_wait(q_empty + s, (use - 1) & 1u, ab)) break;
         uint8_t* st = smem + C::kStageOff + s * C::kStageBytes;
         const int q0 = (i_lo + it) * kBN;
         mbar_arrive_expect_tx(q_full + s, C::kStageBytes + kVecBytes);
@@ -294,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         issued = it + 1;
       }
       mbar_wait_drain(kv_full, 0);
-      for (int it = max(0, issued - kStages); it < issued; ++it)
-        mbar_wait_drain(q_full + it % kStages, static_cast<uint32_t>(it / kStages) & 1u);
+      for (int it = max(0, issued - C::kStagesQ); it < issued; ++it)
+        mbar_wait_drain(q_full + it % C::kStagesQ, static_cast<uint32_t>(it / C::kStagesQ) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // The whole warp runs this loop in step (warp-uniform waits and
@@ -309,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       // S^T(it) = K_j Q_i^T (dp false) or dP^T(it) = V_j dO_i^T (dp true) into buffer it & 1
       auto issue_s = [&](int it, bool dp) {
-        const uint32_t st = smem_base + C::kStageOff + (it % kStages) * C::kStageBytes;
+        const uint32_t st = smem_base + C::kStageOff + (it % C::kStagesQ) * C::kStageBytes;
         const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
         auto product = [&](auto lay, uint32_t a_addr, uint32_t b_addr, int dsize) {
           using L = decltype(lay);
@@ -340,7 +353,61 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         // is never signalled, so the compute warps' bounded wait runs out and
         // every other role leaves through the abort flag or its own limit)
       }
-      for (int it = 0; ok && it < n_it; ++it) {
+      if constexpr (C::kWide) {
+        // One stage of Q / dO: step i's products free it, then step i + 1
+        // loads and its scores run.  This CTA's chunk of dV, dK and dQ^T
+        // reads the matching 128 columns (two boxes) of dO, Q and K.
+        const uint32_t col_boxes = static_cast<uint32_t>(chunk * (128 / LK::kBoxCols));
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int b = it & 1;
+          ok = mbar_wait_warp(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t st = smem_base + C::kStageOff;
+          const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
+          const uint32_t bdo = lo(st + LK::kQTile + col_boxes * LV::kQBox, LV::kQBox);
+          const uint32_t bq = lo(st + col_boxes * LK::kQBox, LK::kQBox);
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k) {
+            const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
+            mma_bf16_ts_warp(tmem + 256, buf + col,
+                             bdo + (static_cast<uint32_t>(k * 16 * LV::kRowBytes) >> 4), LV::kDescHi,
+                             C::kIdescDV, (it > 0 || k > 0) ? 1u : 0u);
+            mma_bf16_ts_warp(tmem + C::kDkCol, buf + 64 + col,
+                             bq + (static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4), LK::kDescHi,
+                             C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit_warp(q_empty);
+          // dQ^T(it) = K_j[:, chunk]^T dS^T(it) into the dP^T half of buffer b
+          // (dP^T(it) is consumed: the compute warps released P(it))
+          const uint32_t ak = lo(smem_base + C::kKOff + col_boxes * LK::kKVBox, LK::kKVBox);
+          const uint32_t bds = lo(smem_base + C::kDsOff, kDsTile);
+#pragma unroll
+          for (int k = 0; k < kBM / 16; ++k) {
+            const uint32_t ka = static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4;
+            const uint32_t kb = static_cast<uint32_t>(k * 16 * 128) >> 4;
+            mma_bf16_ss_warp(buf + 64, ak + ka, LK::kDescHi, bds + kb, kDsHi, kIdescQ,
+                             k > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(dq_full + b);
+          if (it + 1 < n_it) {
+            const int nx = it + 1;
+            ok = mbar_wait_warp(q_full, static_cast<uint32_t>(nx) & 1u, ab);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(nx, false);
+            // dP^T(it+1) lands where dQ^T(it-1) was: its epilogue must have read it
+            if (it >= 1) {
+              ok = mbar_wait_warp(dq_empty + (nx & 1), static_cast<uint32_t>((it - 1) >> 1) & 1u, ab);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(nx, true);
+            mma_commit_warp(s_full + (nx & 1));
+          }
+        }
+      }
+      for (int it = 0; !C::kWide && ok && it < n_it; ++it) {
         const int b = it & 1;
         if (it + 1 < n_it) {
           const int nx = it + 1;
@@ -477,6 +544,34 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
           tma_store_commit();
         }
       }
+    } else if constexpr (C::kWide) {
+      // 64 query rows of this warp's 32 d columns (of the CTA's chunk), staged
+      // and reduced 32 rows at a time
+      for (int j = 0; j < n_it; ++j) {
+        const int b = j & 1;
+        if (!mbar_wait_warp(dq_full + b, static_cast<uint32_t>(j >> 1) & 1u, ab)) break;
+        tc_fence_after();
+        uint32_t g0[32], g1[32];
+        load_half(static_cast<uint32_t>(b * 128 + 64), g0, g1);
+        tc_fence_before();
+        mbar_arrive(dq_empty + b);
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          // this warp's previous reduce has finished reading the staging tile
+          if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          __syncwarp();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            staging[e * C::kDCols + lane] = __uint_as_float(hq ? g1[e] : g0[e]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&p.tm_dq, staging, chunk * 128 + quarter * 32,
+                              (i_lo + j) * kBN + hq * 32, bh);
+            tma_store_commit();
+          }
+        }
+      }
     } else {
       for (int j = 0; j < n_it; ++j) {
         const int b = j & 1;
@@ -511,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1;
-      const int s = it % kStages;
-      ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / kStages) & 1u, ab) &&
+      const int s = it % C::kStagesQ;
+      ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / C::kStagesQ) & 1u, ab) &&
            mbar_wait_warp(s_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
       if (!ok) break;
       tc_fence_after();
@@ -589,15 +684,16 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tc_fence_after();
       }
       if (have || n_it == 0) {
-        // one tensor of `cols` columns per row: TMEM at `tcol`, bf16 to `row`, times `mul`
-        auto write_rows = [&](auto lay, uint32_t tcol, uint16_t* row, float mul) {
-          using L = decltype(lay);
-          constexpr int N = L::kChunk;
+        // one tensor's `2 kHalf` columns of this CTA per row: TMEM at `tcol`,
+        // bf16 to `row` (already at the CTA's first column), times `mul`
+        auto write_rows = [&](auto cols, uint32_t tcol, uint16_t* row, float mul) {
+          constexpr int kHalf = decltype(cols)::value / 2;
+          constexpr int N = kHalf < 32 ? kHalf : 32;
 #pragma unroll
-          for (int c = 0; c < L::kHalfCols / N; ++c) {
+          for (int c = 0; c < kHalf / N; ++c) {
             uint32_t a[N];
             if (have) {
-              tmem_ld_n(lane_base + tcol + half * L::kHalfCols + c * N, a);
+              tmem_ld_n(lane_base + tcol + half * kHalf + c * N, a);
               tmem_ld_wait();
               reg_fence(a);
             } else {
@@ -612,13 +708,15 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
               v.z = pack_bf16x2(__uint_as_float(a[q4 * 8 + 4]) * mul, __uint_as_float(a[q4 * 8 + 5]) * mul);
               v.w = pack_bf16x2(__uint_as_float(a[q4 * 8 + 6]) * mul, __uint_as_float(a[q4 * 8 + 7]) * mul);
               if (key < p.n_k)
-                *reinterpret_cast<uint4*>(row + half * L::kHalfCols + c * N + q4 * 8) = v;
+                *reinterpret_cast<uint4*>(row + half * kHalf + c * N + q4 * 8) = v;
             }
           }
         };
         const long long krow = static_cast<long long>(bh) * p.n_k + key;
-        write_rows(LV{}, 256u, p.dv + krow * DV, 1.f);
-        write_rows(LK{}, C::kDkCol, p.dk + krow * DK, p.scale);
+        write_rows(std::integral_constant<int, C::kColsV>{}, 256u,
+                   p.dv + krow * DV + chunk * C::kColsV, 1.f);
+        write_rows(std::integral_constant<int, C::kColsK>{}, C::kDkCol,
+                   p.dk + krow * DK + chunk * C::kColsK, p.scale);
       }
     }
   }
@@ -642,13 +740,15 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
   constexpr int kLanes = DV / 8;
   constexpr int kRowsPerBlock = 256 / kLanes;
   constexpr int kZero = DK / kLanes;   // 2, 4 or 8 accumulator floats per lane
+  static_assert(kLanes <= 32, "one row per warp at most");
   const int sub = threadIdx.x % kLanes;
   const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanes;
   const long long rows = static_cast<long long>(p.b) * p.h * p.n_q_pad;
   if (row >= rows) return;   // whole groups of kLanes lanes leave together
   const long long bh = row / p.n_q_pad;
   const int i = static_cast<int>(row % p.n_q_pad);
-  const unsigned group = ((1u << kLanes) - 1u) << (threadIdx.x & 31 & ~(kLanes - 1));
+  const unsigned group =
+      kLanes == 32 ? 0xffffffffu : ((1u << (kLanes % 32)) - 1u) << (threadIdx.x & 31 & ~(kLanes - 1));
   if (i >= p.n_q) {
     if (sub == 0) {
       p.neg_dvec[row] = 0.f;
@@ -714,7 +814,8 @@ cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cud
   err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64<DK, DV>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  const long long blocks = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h;
+  const long long blocks =
+      static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h * n64::Cfg<DK, DV>::kChunks;
   if (blocks > 0) {
     err = launch_kernel(n64::sdpa_bwd_tc_n64<DK, DV>, dim3(static_cast<unsigned>(blocks)),
                         dim3(n64::kThreads), smem, stream, prep, bp);
@@ -736,6 +837,7 @@ cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp
     if (d_k == 32) return launch_n64<32, 32>(bp, pp, stream);
     if (d_k == 64) return launch_n64<64, 64>(bp, pp, stream);
     if (d_k == 128) return launch_n64<128, 128>(bp, pp, stream);
+    if (d_k == 256) return launch_n64<256, 256>(bp, pp, stream);
   }
   // Table 3, rows (B): smaller keys than values
   if (d_k == 16 && d_v == 64) return launch_n64<16, 64>(bp, pp, stream);
