@@ -269,9 +269,10 @@ def run_ours(args, world, rank, local):
     vh = torch.from_numpy(v).to(torch.bfloat16).pin_memory()
     oh = torch.empty(od.shape, dtype=torch.bfloat16).pin_memory()
 
-    # The public host-buffer entry point: per (batch, 8-head) chunk, the copy
-    # in, the attention call and the copy out run on three streams, so the
-    # copies of one chunk overlap the attention of another.
+    # The public host-buffer entry point (sdpa_forward_host in the C ABI): per
+    # (batch, 8-head) chunk, the copy in, the attention and the copy out run on
+    # the library's three streams, so the copies of one chunk overlap the
+    # attention of another.
     def e2e_step():
         sd.attention_from_host(qh, kh, vh, oh, qd, kd, vd, od, w.mask_kind, None, 0.0,
                                heads_per_chunk=E2E_HEADS_PER_CHUNK, stream=stream)
@@ -329,8 +330,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": int(qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2),
                 "d2h_bytes_per_step": int(oh.numel() * 2), "steps": e2e_steps,
-                "path": "attention_from_host: (batch, %d-head) chunks, copy in / attention / "
-                        "copy out on three streams" % E2E_HEADS_PER_CHUNK},
+                "path": "sdpa_forward_host (C ABI): (batch, %d-head) chunks, copy in / "
+                        "attention / copy out on the library's three streams"
+                        % E2E_HEADS_PER_CHUNK},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
     }

@@ -161,6 +161,35 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
                           float scale, void* stream);
 
 /*
+ * The bf16 attention of sdpa_forward over HOST buffers, for callers whose
+ * inputs and outputs live in host memory (section 3.2.1, Eq. (1), with the
+ * masks above).
+ *   q_host, k_host, v_host, out_host: BHSD bf16 host buffers, shapes as in
+ *     sdpa_forward; page-locked (cudaHostAlloc / cudaHostRegister) for the
+ *     copies to run asynchronously and overlap; pageable memory works but
+ *     each copy then blocks the calling thread.
+ *   q_dev, k_dev, v_dev, out_dev: caller-owned device buffers of the same
+ *     shapes, used as staging; they hold the inputs and the output after
+ *     the call completes.
+ *   heads_per_chunk: the work is cut into (batch entry, heads_per_chunk
+ *     heads) chunks (0: all heads of a batch entry).  Each chunk's copy in,
+ *     attention and copy out go on three streams of the library's own, so
+ *     the copies of one chunk overlap the attention of another.
+ *   stream: the work starts after what is queued on `stream`, and `stream`
+ *     waits for the last copy back: synchronise it before reading out_host.
+ * The first call on a device creates the library's three streams and four
+ * events there, kept for the process; concurrent calls on one device are
+ * serialised on the host while they enqueue.  Argument rules and statuses
+ * are sdpa_forward's, plus SDPA_ERR_INVALID_ARG for a null host pointer or a
+ * negative heads_per_chunk.
+ */
+sdpa_status sdpa_forward_host(const void* q_host, const void* k_host, const void* v_host,
+                              void* out_host, void* q_dev, void* k_dev, void* v_dev,
+                              void* out_dev, int b, int h, int n_q, int n_k, int d_k, int d_v,
+                              int mask_kind, const int32_t* kv_lengths, float scale,
+                              int heads_per_chunk, void* stream);
+
+/*
  * The same operation in fp32 throughout (fp32 inputs, exact fp32 exponentials
  * and sums on the CUDA cores), for small fp32 problems and the worked
  * examples.  Layouts as sdpa_forward with float elements; any

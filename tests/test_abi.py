@@ -214,3 +214,19 @@ def test_noalloc_limit_matches_the_header():
     m = re.search(r"#define\s+SDPA_MHA_NOALLOC_MAX_WORKSPACE\s+\((\d+)u\s*<<\s*(\d+)\)", text)
     assert m, "SDPA_MHA_NOALLOC_MAX_WORKSPACE not found"
     assert int(m.group(1)) << int(m.group(2)) == sd.MHA_NOALLOC_MAX_WORKSPACE
+
+
+def test_host_pipeline_argument_checks(lib):
+    """sdpa_forward_host: null host pointers and a negative chunk size are
+    rejected on the host; valid arguments stop at the device check here."""
+    def call(**kw):
+        a = dict(qh=A, kh=A, vh=A, oh=A, hc=0, d=64)
+        a.update(kw)
+        return lib.sdpa_forward_host(a["qh"], a["kh"], a["vh"], a["oh"], A, A, A, A, 2, 4, 128, 128,
+                                     a["d"], a["d"], 0, None, ctypes.c_float(0.0), a["hc"], None)
+    assert call(qh=None) == INVALID
+    assert call(oh=None) == INVALID
+    assert call(hc=-1) == INVALID
+    assert call(d=48) == UNSUPPORTED
+    if not _gpu_visible():
+        assert call() == NODEV

@@ -31,7 +31,7 @@ STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTE
                 6: "SDPA_ERR_DEVICE_TIMEOUT"}
 
 # Every symbol include/sdpa.h declares.
-EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_lse",
+EXPORTS = ("sdpa_forward", "sdpa_forward_restricted", "sdpa_forward_lse", "sdpa_forward_host",
            "sdpa_backward_workspace_size", "sdpa_backward", "sdpa_forward_f32",
            "sdpa_decode_workspace_size", "sdpa_decode", "mha_workspace_size",
            "mha_forward",
@@ -73,6 +73,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sdpa_backward.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, P, I, F,
                                   P]
     lib.sdpa_backward.restype = I
+    lib.sdpa_forward_host.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, F, I, P]
+    lib.sdpa_forward_host.restype = I
     lib.sdpa_forward_f32.argtypes = attn
     lib.sdpa_forward_f32.restype = I
     lib.sdpa_decode_workspace_size.argtypes = [I, I, I, I, I]
@@ -330,49 +332,27 @@ def attention_backward(q, k, v, out, lse, dout, mask_kind=SDPA_MASK_NONE, kv_len
     return dq, dk, dv
 
 
-_copy_streams = {}
+
+
+def sdpa_forward_host(q_host, k_host, v_host, out_host, q_dev, k_dev, v_dev, out_dev, b, h, n_q,
+                      n_k, d_k, d_v, mask_kind=SDPA_MASK_NONE, kv_lengths=None, scale=0.0,
+                      heads_per_chunk=0, stream=None) -> None:
+    """bf16 attention over host buffers, chunked and pipelined inside the
+    library (see include/sdpa.h)."""
+    _check(load_library().sdpa_forward_host(
+        _addr(q_host), _addr(k_host), _addr(v_host), _addr(out_host), _addr(q_dev), _addr(k_dev),
+        _addr(v_dev), _addr(out_dev), b, h, n_q, n_k, d_k, d_v, mask_kind, _addr(kv_lengths),
+        float(scale), int(heads_per_chunk or 0), _stream(stream)), "sdpa_forward_host")
 
 
 def attention_from_host(qh, kh, vh, oh, qd, kd, vd, od, mask_kind=SDPA_MASK_NONE, kv_lengths=None,
                         scale=0.0, heads_per_chunk=None, stream=None):
-    """Attention over pinned HOST tensors: qh/kh/vh [b,h,n,d] bf16 -> oh.
-
-    qd/kd/vd/od are caller-owned device buffers of the same shapes.  The work
-    is cut into (batch, head-range) chunks of `heads_per_chunk` heads; each
-    chunk's host->device copy, sdpa_forward call and device->host copy go on
-    three streams, so copies of one chunk overlap the attention of another.
-    Ordered after prior work on `stream` (default: the current stream), which
-    waits for the last copy back.  kv_lengths: device int32 [b] or None."""
-    import torch
-    main = stream or torch.cuda.current_stream()
-    dev = qd.device
-    if dev not in _copy_streams:
-        _copy_streams[dev] = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
-    s_in, s_cmp, s_out = _copy_streams[dev]
-    b, h, n_q, d = qh.shape
-    n_k = kh.shape[2]
-    hc = heads_per_chunk or h
-    start = torch.cuda.Event()
-    start.record(main)
-    for s in (s_in, s_cmp, s_out):
-        s.wait_event(start)
-    for bi in range(b):
-        for h0 in range(0, h, hc):
-            h1 = min(h, h0 + hc)
-            with torch.cuda.stream(s_in):
-                for dst, src in ((qd, qh), (kd, kh), (vd, vh)):
-                    dst[bi, h0:h1].copy_(src[bi, h0:h1], non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(s_in)
-            s_cmp.wait_event(ev)
-            lens = None if kv_lengths is None else kv_lengths[bi:bi + 1]
-            sdpa_forward(qd[bi, h0:h1], kd[bi, h0:h1], vd[bi, h0:h1], od[bi, h0:h1], 1, h1 - h0, n_q,
-                         n_k, d, d, mask_kind, lens, scale, s_cmp)
-            ev = torch.cuda.Event()
-            ev.record(s_cmp)
-            s_out.wait_event(ev)
-            with torch.cuda.stream(s_out):
-                oh[bi, h0:h1].copy_(od[bi, h0:h1], non_blocking=True)
-    end = torch.cuda.Event()
-    end.record(s_out)
-    main.wait_event(end)
+    """Attention over pinned HOST tensors qh/kh/vh [b,h,n,d] bf16 -> oh, with
+    qd/kd/vd/od caller-owned device buffers of the same shapes: one call of
+    sdpa_forward_host (the library pipelines the chunks' copies and kernels
+    on its own streams).  `stream` (default: the current stream) waits for
+    the last copy back.  kv_lengths: device int32 [b] or None."""
+    b, h, n_q, d_k = qh.shape
+    n_k, d_v = kh.shape[2], vh.shape[3]
+    sdpa_forward_host(qh, kh, vh, oh, qd, kd, vd, od, b, h, n_q, n_k, d_k, d_v, mask_kind,
+                      kv_lengths, scale, heads_per_chunk or 0, stream)

@@ -307,6 +307,42 @@ bool fill_gemm_problem(GemmProblem* pr, const void* x, const void* w, void* y, i
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Streams and events of the host-buffer pipeline (sdpa_forward_host), made
+// once per device on its first call and kept for the process.
+struct HostPipeline {
+  bool ready = false;
+  cudaStream_t copy_in = nullptr, compute = nullptr, copy_out = nullptr;
+  cudaEvent_t start = nullptr, in_done = nullptr, cmp_done = nullptr, end = nullptr;
+  std::mutex mutex;   // one enqueue at a time: the events are re-recorded per chunk
+};
+HostPipeline g_pipelines[kMaxDevices];
+
+sdpa_status host_pipeline(HostPipeline** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return SDPA_ERR_UNSUPPORTED_DEVICE;
+  }
+  HostPipeline& hp = g_pipelines[dev];
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!hp.ready) {
+    const unsigned sf = cudaStreamNonBlocking, ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&hp.copy_in, sf) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.compute, sf) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.copy_out, sf) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.start, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.in_done, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.cmp_done, ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.end, ef) != cudaSuccess) {
+      cudaGetLastError();
+      return SDPA_ERR_CUDA;
+    }
+    hp.ready = true;
+  }
+  *out = &hp;
+  return SDPA_OK;
+}
+
 // Decode: enough splits for about kDecodeWaves waves of the shape's resident
 // CTAs; the workspace is sized for the most any shape can take.
 int decode_target_ctas(int resident) {
@@ -467,6 +503,80 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   return sdpa::launch_sdpa_bwd(bp, pp, d_k, d_v, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SDPA_OK
              : SDPA_ERR_CUDA;
+}
+
+sdpa_status sdpa_forward_host(const void* q_host, const void* k_host, const void* v_host,
+                              void* out_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
+                              int b, int h, int n_q, int n_k, int d_k, int d_v, int mask_kind,
+                              const int32_t* kv_lengths, float scale, int heads_per_chunk,
+                              void* stream) {
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr)
+    return SDPA_ERR_INVALID_ARG;
+  sdpa_status st = check_attention_args(q_dev, k_dev, v_dev, out_dev, b, h, n_q, n_k, d_k, d_v,
+                                        mask_kind, kv_lengths, scale);
+  if (st != SDPA_OK) return st;
+  if (heads_per_chunk < 0) return SDPA_ERR_INVALID_ARG;
+  if (!tc_head_sizes(d_k, d_v)) return SDPA_ERR_UNSUPPORTED;
+  unsigned* status = nullptr;
+  st = current_device(&status);
+  if (st != SDPA_OK) return st;
+  if (n_q == 0) return SDPA_OK;
+  HostPipeline* hp = nullptr;
+  st = host_pipeline(&hp);
+  if (st != SDPA_OK) return st;
+  std::lock_guard<std::mutex> lock(hp->mutex);
+  cudaStream_t main = static_cast<cudaStream_t>(stream);
+  const int hc = (heads_per_chunk == 0 || heads_per_chunk > h) ? h : heads_per_chunk;
+  // bytes of one (batch, head) slice of each tensor; a chunk of heads of one
+  // batch entry is contiguous in BHSD
+  const size_t qb = static_cast<size_t>(n_q) * d_k * 2, kb = static_cast<size_t>(n_k) * d_k * 2;
+  const size_t vb = static_cast<size_t>(n_k) * d_v * 2, ob = static_cast<size_t>(n_q) * d_v * 2;
+  auto bad = [](cudaError_t e) {
+    if (e == cudaSuccess) return false;
+    cudaGetLastError();
+    return true;
+  };
+  // everything after the work already queued on the caller's stream
+  if (bad(cudaEventRecord(hp->start, main)) ||
+      bad(cudaStreamWaitEvent(hp->copy_in, hp->start, 0)) ||
+      bad(cudaStreamWaitEvent(hp->compute, hp->start, 0)) ||
+      bad(cudaStreamWaitEvent(hp->copy_out, hp->start, 0)))
+    return SDPA_ERR_CUDA;
+  for (int bi = 0; bi < b; ++bi) {
+    for (int h0 = 0; h0 < h; h0 += hc) {
+      const int nh = h - h0 < hc ? h - h0 : hc;
+      const size_t slice = static_cast<size_t>(bi) * h + h0;
+      auto at = [&](const void* base, size_t bytes) {
+        return static_cast<const uint8_t*>(base) + slice * bytes;
+      };
+      auto at_mut = [&](void* base, size_t bytes) { return static_cast<uint8_t*>(base) + slice * bytes; };
+      if (bad(cudaMemcpyAsync(at_mut(q_dev, qb), at(q_host, qb), nh * qb, cudaMemcpyHostToDevice,
+                              hp->copy_in)) ||
+          bad(cudaMemcpyAsync(at_mut(k_dev, kb), at(k_host, kb), nh * kb, cudaMemcpyHostToDevice,
+                              hp->copy_in)) ||
+          bad(cudaMemcpyAsync(at_mut(v_dev, vb), at(v_host, vb), nh * vb, cudaMemcpyHostToDevice,
+                              hp->copy_in)) ||
+          bad(cudaEventRecord(hp->in_done, hp->copy_in)) ||
+          bad(cudaStreamWaitEvent(hp->compute, hp->in_done, 0)))
+        return SDPA_ERR_CUDA;
+      st = launch_attention_tc(at(q_dev, qb), at(k_dev, kb), at(v_dev, vb), at_mut(out_dev, ob), 1,
+                               nh, n_q, n_k, d_k, d_v, bhsd(nh, n_q, d_k), bhsd(nh, n_k, d_k),
+                               bhsd(nh, n_k, d_v), bhsd(nh, n_q, d_v), mask_kind,
+                               kv_lengths != nullptr ? kv_lengths + bi : nullptr, scale, status,
+                               hp->compute, sdpa::kWindowUnbounded, sdpa::kWindowUnbounded,
+                               nullptr, /*pdl=*/false);
+      if (st != SDPA_OK) return st;
+      if (bad(cudaEventRecord(hp->cmp_done, hp->compute)) ||
+          bad(cudaStreamWaitEvent(hp->copy_out, hp->cmp_done, 0)) ||
+          bad(cudaMemcpyAsync(at_mut(out_host, ob), at(out_dev, ob), nh * ob,
+                              cudaMemcpyDeviceToHost, hp->copy_out)))
+        return SDPA_ERR_CUDA;
+    }
+  }
+  // the caller's stream continues after the last copy back
+  if (bad(cudaEventRecord(hp->end, hp->copy_out)) || bad(cudaStreamWaitEvent(main, hp->end, 0)))
+    return SDPA_ERR_CUDA;
+  return SDPA_OK;
 }
 
 sdpa_status sdpa_forward_f32(const void* q, const void* k, const void* v, void* out, int b, int h,
