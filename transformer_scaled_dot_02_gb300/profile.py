@@ -65,13 +65,13 @@ def main():
     elif a.decode:
         q = torch.randn(a.b, a.h, n_q, a.d, device=dev).to(torch.bfloat16)
         k = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
-        v = torch.randn(a.b, a.h, n_k, a.d, device=dev).to(torch.bfloat16)
-        out = torch.empty_like(q)
-        work = torch.empty(max(1, sd.sdpa_decode_workspace_size(a.b, a.h, n_q, n_k, a.d)),
+        v = torch.randn(a.b, a.h, n_k, d_v, device=dev).to(torch.bfloat16)
+        out = torch.empty(a.b, a.h, n_q, d_v, dtype=torch.bfloat16, device=dev)
+        work = torch.empty(max(1, sd.sdpa_decode_workspace_size(a.b, a.h, n_q, n_k, d_v)),
                            dtype=torch.uint8, device=dev)
 
         def run():
-            sd.sdpa_decode(q, k, v, out, work, work.numel(), a.b, a.h, n_q, n_k, a.d, a.d, lens)
+            sd.sdpa_decode(q, k, v, out, work, work.numel(), a.b, a.h, n_q, n_k, a.d, d_v, lens)
     elif a.mha:
         dm = a.d_model
         xq = torch.randn(a.b, n_q, dm, device=dev).to(torch.bfloat16)
@@ -120,6 +120,9 @@ def main():
     line = "mean %.4f ms per call over %d calls" % (ms, a.iters)
     if gemm_mnk:
         line += ", %.1f TFLOP/s" % (2.0 * gm * gn * gk / (ms * 1e-3) / 1e12)
+    elif a.decode:
+        # K and V caches read once (the whole capacity when no lengths are given)
+        line += ", %.0f GB/s of K/V" % (2.0 * a.b * a.h * n_k * (a.d + d_v) / (ms * 1e-3) / 1e9)
     elif not (a.mha or a.decode or a.restricted):
         # 2 n_q n_k per unit of head size: S and O in the forward; S, dP, dV, dK, dQ in the backward
         units = 3 * a.d + 2 * d_v if a.backward else a.d + d_v
