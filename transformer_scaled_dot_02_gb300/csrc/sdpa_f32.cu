@@ -11,6 +11,7 @@
 #include <cmath>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace sdpa {
 namespace {
@@ -34,6 +35,43 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Copies rows [0, rows) of a row-major [*, d] fp32 matrix (rows at and past
+// `valid` read as 0) into a shared tile [rows][kPad].  With d a multiple of 4
+// every thread issues all its 16-byte loads before any store, so their
+// latencies overlap instead of adding up; other d take one float at a time.
+template <int kRows>
+__device__ __forceinline__ void load_tile(float (*dst)[kPad], const float* src, int valid, int d) {
+  if ((d & 3) == 0) {
+    constexpr int kPerThread = kRows * (kMaxD / 4) / (kWarps * 32);
+    const int vpr = d / 4;   // 16-byte pieces per row
+    float4 buf[kPerThread];
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      const int idx = threadIdx.x + i * kWarps * 32;
+      const int r = idx / vpr, c4 = idx % vpr;
+      buf[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < kRows && r < valid)
+        buf[i] = *reinterpret_cast<const float4*>(src + static_cast<long long>(r) * d + c4 * 4);
+    }
+#pragma unroll
+    for (int i = 0; i < kPerThread; ++i) {
+      const int idx = threadIdx.x + i * kWarps * 32;
+      const int r = idx / vpr, c4 = idx % vpr;
+      if (r < kRows) {
+        dst[r][c4 * 4 + 0] = buf[i].x;
+        dst[r][c4 * 4 + 1] = buf[i].y;
+        dst[r][c4 * 4 + 2] = buf[i].z;
+        dst[r][c4 * 4 + 3] = buf[i].w;
+      }
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < kRows * d; idx += kWarps * 32) {
+      const int r = idx / d, c = idx % d;
+      dst[r][c] = r < valid ? src[static_cast<long long>(r) * d + c] : 0.f;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
 sdpa_fwd_f32_simt(const SdpaF32Params p) {
   __shared__ float q_s[kRowsPerCta][kPad];
@@ -51,6 +89,10 @@ sdpa_fwd_f32_simt(const SdpaF32Params p) {
   float* out = p.out + static_cast<long long>(bh) * p.n_q * p.d_v;
 
   const bool causal = (p.mask_kind & 1) != 0;
+  // the next kernel may launch now; this grid's inputs may come from the
+  // previous kernel in the stream, so wait for it before reading them
+  griddep_launch_dependents();
+  griddep_wait();
   int kv_len = p.n_k;
   if ((p.mask_kind & 2) && p.kv_lengths != nullptr) {
     kv_len = p.kv_lengths[bi];
@@ -60,10 +102,7 @@ sdpa_fwd_f32_simt(const SdpaF32Params p) {
   int key_end = kv_len;
   if (causal) key_end = min(key_end, row0 + kRowsPerCta);
 
-  for (int idx = threadIdx.x; idx < kRowsPerCta * p.d_k; idx += blockDim.x) {
-    const int r = idx / p.d_k, c = idx % p.d_k;
-    q_s[r][c] = (row0 + r < p.n_q) ? q[static_cast<long long>(row0 + r) * p.d_k + c] : 0.f;
-  }
+  load_tile<kRowsPerCta>(q_s, q + static_cast<long long>(row0) * p.d_k, p.n_q - row0, p.d_k);
 
   float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][kMaxD / 32];
 #pragma unroll
@@ -76,14 +115,8 @@ sdpa_fwd_f32_simt(const SdpaF32Params p) {
 
   for (int key0 = 0; key0 < key_end; key0 += kKeyTile) {
     __syncthreads();  // previous tile fully consumed (and q_s written)
-    for (int idx = threadIdx.x; idx < kKeyTile * p.d_k; idx += blockDim.x) {
-      const int j = idx / p.d_k, c = idx % p.d_k;
-      k_s[j][c] = (key0 + j < p.n_k) ? k[static_cast<long long>(key0 + j) * p.d_k + c] : 0.f;
-    }
-    for (int idx = threadIdx.x; idx < kKeyTile * p.d_v; idx += blockDim.x) {
-      const int j = idx / p.d_v, c = idx % p.d_v;
-      v_s[j][c] = (key0 + j < p.n_k) ? v[static_cast<long long>(key0 + j) * p.d_v + c] : 0.f;
-    }
+    load_tile<kKeyTile>(k_s, k + static_cast<long long>(key0) * p.d_k, p.n_k - key0, p.d_k);
+    load_tile<kKeyTile>(v_s, v + static_cast<long long>(key0) * p.d_v, p.n_k - key0, p.d_v);
     __syncthreads();
 
 #pragma unroll
@@ -135,8 +168,9 @@ cudaError_t launch_sdpa_f32(const SdpaF32Params& p, cudaStream_t stream) {
   if (bh == 0 || p.n_q == 0) return cudaSuccess;
   if (bh > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid((p.n_q + kRowsPerCta - 1) / kRowsPerCta, static_cast<unsigned>(bh));
-  sdpa_fwd_f32_simt<<<grid, kWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependency on the previous kernel: the kernel reads
+  // global memory only after griddep_wait()
+  return launch_kernel(sdpa_fwd_f32_simt, grid, dim3(kWarps * 32), 0, stream, true, p);
 }
 
 }  // namespace sdpa
