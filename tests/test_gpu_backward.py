@@ -179,6 +179,16 @@ def test_backward_matches_across_calls_and_reuses_workspace():
         assert rel_err(host(x), host(y)) <= 1e-2 * TOL_BF16
 
 
+def test_backward_workload_length():
+    """The backward workload's full sequence (causal n8192 d128, values
+    0.5 N(0,1), as bench.py --workload backward) on two of its heads: up to
+    128 query steps per key tile, every row of every gradient."""
+    w = synthetic.WORKLOADS["long_causal"]
+    q, k, v, _ = synthetic.sdpa_inputs(w, b=1, h=2)
+    do = synthetic.dout_input(w, b=1, h=2)
+    _check(q, k, v, do, w.mask_kind, None)
+
+
 def test_backward_long_causal():
     """Causal b1 h4 n4096 d128 (up to 32 key tiles per query tile): every
     row of every gradient checked against the oracle."""

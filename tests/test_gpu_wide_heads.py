@@ -108,6 +108,15 @@ def test_wide_long_causal():
     _check(q, k, v, 1, None)
 
 
+def test_wide512_workload_full():
+    """The one-head d = 512 workload at full size (b4 h1 n8192 causal, values
+    0.5 N(0,1)), the benchmark's --workload wide512 launch: every output row
+    under both measures and every row's log-sum-exp."""
+    w = synthetic.WORKLOADS["wide_d512"]
+    q, k, v, lens = synthetic.sdpa_inputs(w)
+    _check(q, k, v, w.mask_kind, lens)
+
+
 @pytest.mark.parametrize("h,d", [(1, 512), (2, 256)])
 def test_table3_row_a_mha(h, d):
     """Multi-head attention at d_model = 512 with one head of 512 (Table 3,
