@@ -627,7 +627,7 @@ def run_row(args, world, rank, local):
                      "frac": round(achieved / peak, 4),
                      "peak_source": "%s %s" % (peak_src, "hbm_gbs" if bound == "hbm"
                                                else "bf16_tflops (burst)"),
-                     "traffic": None, "kernel": kernel,
+                     "traffic": recorded_traffic(kind), "kernel": kernel,
                      "launch_ms_mean": round(mean_ms, 4),
                      "launch_ms_min": round(float(np.min(launch_ms)), 4)},
         "e2e": {"value": round(world * work * e2e_steps / (e2e_ms * 1e-3) / scale, 3), "unit": unit,
