@@ -181,7 +181,11 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
  * events there, kept for the process; concurrent calls on one device are
  * serialised on the host while they enqueue.  Argument rules and statuses
  * are sdpa_forward's, plus SDPA_ERR_INVALID_ARG for a null host pointer or a
- * negative heads_per_chunk.
+ * negative heads_per_chunk; they are checked before anything is enqueued.
+ * If a CUDA call fails while the chunks are being enqueued, the call returns
+ * SDPA_ERR_CUDA at once: chunks enqueued before it may still be running on
+ * the library's streams, and `stream` does not wait for them (synchronise
+ * the device before reusing the buffers).
  */
 sdpa_status sdpa_forward_host(const void* q_host, const void* k_host, const void* v_host,
                               void* out_host, void* q_dev, void* k_dev, void* v_dev,
