@@ -11,10 +11,10 @@
 // CTAs so the whole GPU streams it:
 //   sdpa_decode_split   grid (splits, b*h), 4 warps.  Each warp walks its own
 //                       tiles of TK keys of the CTA's key range, double
-//                       buffered: one lane loads a tile's K and V rows with
-//                       the TMA (rows swizzled at their width, as the
-//                       attention kernels load them) while the warp works on
-//                       the other.  Scores: each key of the tile belongs to
+//                       buffered (single at d = 512, so that two CTAs fit an
+//                       SM): one lane loads a tile's K and V rows with the
+//                       TMA (rows swizzled at their width, as the attention
+//                       kernels load them) while the warp works on the other.  Scores: each key of the tile belongs to
 //                       LK lanes (one lane up to d_k = 64), which form its
 //                       dot products with every query from their share of the
 //                       columns; the queries sit in shared memory, pre-scaled
@@ -42,7 +42,6 @@ namespace {
 
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = 32 * kDecWarps;
-constexpr int kDecStages = 2;
 
 template <int DK, int DV, int MAXQ>
 struct DCfg {
@@ -58,6 +57,8 @@ struct DCfg {
   static constexpr int KBYTES = (DK / KBOX) * KBOXB;                // TK x DK x 2
   static constexpr int VBYTES = (DV / VBOX) * VBOXB;
   static constexpr int STAGE = KBYTES + VBYTES;
+  // two stages per warp; one at d = 512 (16 KB a stage), so that two CTAs share an SM
+  static constexpr int kStages = STAGE >= 16384 ? 1 : 2;
   // value columns: CV contiguous ones per lane; below 32 columns the warp
   // splits into KS slices of lanes that take alternate keys
   static constexpr int CV = DV >= 32 ? DV / 32 : 1;
@@ -65,15 +66,16 @@ struct DCfg {
   static constexpr int QROW = KCOLS + 4;                            // floats per (query, part)
   // shared memory, from a 1024-byte aligned base
   static constexpr int kStageOff = 0;                               // [warp][stage]: K, V
-  static constexpr int kQOff = kDecWarps * kDecStages * STAGE;
+  static constexpr int kQOff = kDecWarps * kStages * STAGE;
   static constexpr int kQBytes = MAXQ * LK * QROW * 4;
   static constexpr int kPOff = kQOff + kQBytes;                     // [warp][TK][MAXQ]
   static constexpr int kPBytes = kDecWarps * TK * MAXQ * 4;
   static constexpr int kBarOff = (kPOff + kPBytes + 7) / 8 * 8;
-  static constexpr int kSmemBytes = kBarOff + kDecWarps * kDecStages * 8 + 16 + 1024;
-  // the warps' merge reuses the stage buffers once every tile is consumed
+  static constexpr int kSmemBytes = kBarOff + kDecWarps * kStages * 8 + 16 + 1024;
+  // the warps' merge reuses the stage buffers and the queries once every
+  // tile is consumed
   static constexpr int kMergeBytes = kDecWarps * MAXQ * (DV + 2) * 4;
-  static_assert(kMergeBytes <= kQOff, "merge buffer");
+  static_assert(kMergeBytes <= kPOff, "merge buffer");
   static_assert(KBOXB % 1024 == 0 && VBOXB % 1024 == 0, "swizzle atoms");
   static_assert(DK % (8 * LK) == 0 && KCOLS % 8 == 0, "score chunks");
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const __grid_co
   uint8_t* smem = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   float* q_s = reinterpret_cast<float*>(smem + C::kQOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kDecWarps * kDecStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kDecWarps * C::kStages);
   const AbortState ab{abort_flag, p.status};
 
   const int warp = threadIdx.x >> 5;
@@ -117,11 +119,11 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const __grid_co
   const int bh = blockIdx.y;
   const int bi = bh / p.h;
   const int hi = bh % p.h;
-  uint64_t* full = bars + warp * kDecStages;
+  uint64_t* full = bars + warp * C::kStages;
   float* p_s = reinterpret_cast<float*>(smem + C::kPOff) + warp * TK * MAXQ;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecWarps * kDecStages; ++i) mbar_init(bars + i, 1);
+    for (int i = 0; i < kDecWarps * C::kStages; ++i) mbar_init(bars + i, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -154,8 +156,8 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const __grid_co
   const int my_tiles = n_tiles > warp ? (n_tiles - warp + kDecWarps - 1) / kDecWarps : 0;
   auto tile_key = [&](int u) { return c0 + (warp + u * kDecWarps) * TK; };
   auto load_tile = [&](int u) {
-    const int s = u & 1;
-    uint8_t* kst = smem + C::kStageOff + (warp * kDecStages + s) * C::STAGE;
+    const int s = u % C::kStages;
+    uint8_t* kst = smem + C::kStageOff + (warp * C::kStages + s) * C::STAGE;
     mbar_arrive_expect_tx(full + s, C::STAGE);
     const int j0 = tile_key(u);
 #pragma unroll
@@ -166,9 +168,9 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const __grid_co
       tma_load_4d(&p.tm_v, full + s, kst + C::KBYTES + c * C::VBOXB, c * C::VBOX, j0, hi, bi);
   };
   if (lane == 0) {
-    for (int u = 0; u < my_tiles && u < kDecStages; ++u) load_tile(u);
+    for (int u = 0; u < my_tiles && u < C::kStages; ++u) load_tile(u);
   }
-  int issued = my_tiles < kDecStages ? my_tiles : kDecStages;
+  int issued = my_tiles < C::kStages ? my_tiles : C::kStages;
 
   // scores: key kj = lane / LK of the tile, columns [part * KCOLS, +KCOLS)
   const int kj = lane / LK;
@@ -187,12 +189,12 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const __grid_co
   const int nq = p.n_q;
   bool ok = true;
   for (int u = 0; u < my_tiles; ++u) {
-    const int s = u & 1;
-    if (!mbar_wait_warp(full + s, static_cast<uint32_t>(u >> 1) & 1u, ab)) {
+    const int s = u % C::kStages;
+    if (!mbar_wait_warp(full + s, static_cast<uint32_t>(u / C::kStages) & 1u, ab)) {
       ok = false;
       break;
     }
-    const uint8_t* kst = smem + C::kStageOff + (warp * kDecStages + s) * C::STAGE;
+    const uint8_t* kst = smem + C::kStageOff + (warp * C::kStages + s) * C::STAGE;
     const uint8_t* vst = kst + C::KBYTES;
     const int j0 = tile_key(u);
 
@@ -316,8 +318,8 @@ __global__ void __launch_bounds__(kDecThreads) sdpa_decode_split(const __grid_co
   // them land before the buffers are reused or the CTA exits
   if (!ok && lane == 0) {
     const int last = (issued < my_tiles ? issued : my_tiles);
-    for (int u = last - kDecStages < 0 ? 0 : last - kDecStages; u < last; ++u)
-      mbar_wait_drain(full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
+    for (int u = last - C::kStages < 0 ? 0 : last - C::kStages; u < last; ++u)
+      mbar_wait_drain(full + u % C::kStages, static_cast<uint32_t>(u / C::kStages) & 1u);
   }
 
   // ---- per-warp totals: the row sums over lanes (one lane per key counted),
@@ -422,7 +424,7 @@ int resident_ctas() {
   // CTAs of the largest-query variant that share an SM (shared memory bound)
   constexpr int smem = DCfg<DK, DV, 8>::kSmemBytes + 1024;
   const int by_smem = 232448 / smem;
-  return by_smem < 1 ? 1 : (by_smem > 4 ? 4 : by_smem);
+  return by_smem < 1 ? 1 : (by_smem > kDecodeMaxResident ? kDecodeMaxResident : by_smem);
 }
 
 }  // namespace
