@@ -6,9 +6,14 @@ inputs with fp32 accumulation):
   - whole tensor: max|gpu - ref| / max|ref| over the compared entries, the
     absolute error relative to the output's scale;
   - per row: for every row i (every index but the last: one query's output
-    row, or one key's row of dK and dV), max_c|gpu_ic - ref_ic| / max_c|ref_ic|.
-    A row whose reference is all zero (a query that sees no key, a hidden key)
-    is compared in absolute terms, so it must come out as zero.
+    row, or one key's row of dK and dV), max_c|gpu_ic - ref_ic| / s_i with
+    s_i = max(max_c|ref_ic|, 1e-4 max|ref|).  The floor is the fp32 bar: a
+    row whose exact value is far below its terms (a one-hot softmax row of
+    dQ, where dS cancels to about 1e-6 of the tensor's scale) keeps the fp32
+    rounding of those terms, about 1e-7 of the tensor's scale, and no
+    arithmetic resolves it further.  A row that must be zero (a query that
+    sees no key, a hidden key) is thereby held to 1e-4 of the tensor's scale
+    times the bar.
 The whole-tensor figure alone is set by the largest rows.  In a long causal
 output the first rows are single value rows (|O| about max|V|) while rows
 thousands of keys long average down to a few hundredths of that, so a dropped
@@ -62,15 +67,19 @@ def rel_err(got, ref):
     return float(np.abs(got - ref).max() / scale)
 
 
+ROW_FLOOR = 1e-4   # floor of a row's scale, as a fraction of the tensor's
+
+
 def row_errs(got, ref):
-    """Per-row errors: max_c|got_ic - ref_ic| / max_c|ref_ic| for every row
-    (absolute where the reference row is 0), flattened over the leading axes."""
+    """Per-row errors: max_c|got_ic - ref_ic| / max(max_c|ref_ic|, ROW_FLOOR
+    max|ref|) for every row (absolute if the whole reference is 0),
+    flattened over the leading axes."""
     got, ref = _pair(got, ref)
     if ref.size == 0:
         return np.zeros(0)
     g = got.reshape(-1, got.shape[-1])
     r = ref.reshape(-1, ref.shape[-1])
-    scale = np.abs(r).max(axis=1)
+    scale = np.maximum(np.abs(r).max(axis=1), ROW_FLOOR * np.abs(r).max())
     err = np.abs(g - r).max(axis=1)
     return np.where(scale > 0, err / np.where(scale > 0, scale, 1.0), err)
 

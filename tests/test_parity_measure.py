@@ -79,14 +79,23 @@ def test_dropped_tile_moves_the_log_sum_exp_past_its_bar():
     assert full - cut > 1e-2
 
 
-def test_zero_rows_are_compared_in_absolute_terms():
+def test_rows_are_floored_at_the_fp32_bar():
+    """A row's scale is floored at 1e-4 of the tensor's: a row that must be
+    zero is held to that, and a nearly-zero row is not held to less."""
     ref = np.zeros((2, 3, 4))
     ref[1] = 1.0
     got = ref.copy()
     assert row_err(got, ref) == 0.0
     got[0, 1, 2] = 1e-3     # a row that must be zero is not
-    assert row_err(got, ref) == 1e-3
+    assert abs(row_err(got, ref) - 10.0) < 1e-9
     assert rel_err(got, ref) == 1e-3
+    got = ref.copy()
+    ref2 = ref.copy()
+    ref2[0, 0, 0] = 1e-9    # a row far below the floor, off by 1e-6 of the tensor's scale
+    got[0, 0, 0] = 1e-6
+    assert abs(row_err(got, ref2) - (1e-6 - 1e-9) / 1e-4) < 1e-12
+    # the whole reference zero: absolute
+    assert row_err(np.full((2, 3), 1e-3), np.zeros((2, 3))) == 1e-3
 
 
 def test_gradient_rows_with_a_dropped_tile_are_caught():
