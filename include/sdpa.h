@@ -146,10 +146,9 @@ sdpa_status sdpa_forward_lse(const void* q, const void* k, const void* v, void* 
  * P is recomputed from lse, never stored; the products run on the tensor
  * cores with bf16 operands (P and dS rounded to bf16) and fp32 accumulation;
  * dQ is accumulated in fp32 across key tiles, then rounded.  Hidden keys get
- * zero gradient.  Supported: d_k == d_v in {16, 32, 64, 128, 256}, and
- * (d_k, d_v) in {(16, 64), (32, 64)} (Table 3, rows (B)).  d = 512 (Table 3,
- * row (A), one head) returns SDPA_ERR_UNSUPPORTED: a 128-key tile's K and V
- * alone would fill 256 KB of the SM's 227 KB of shared memory.
+ * zero gradient.  Supported: d_k == d_v in {16, 32, 64, 128, 256, 512}
+ * (every head size of Table 3), and (d_k, d_v) in {(16, 64), (32, 64)}
+ * (Table 3, rows (B)); other sizes return SDPA_ERR_UNSUPPORTED.
  * The forward output `out` enters only through D_i = dO_i . out_i.
  */
 size_t sdpa_backward_workspace_size(int b, int h, int n_q, int d);

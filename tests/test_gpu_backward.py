@@ -88,7 +88,7 @@ def _check(q, k, v, do, mask, lens, r=0, scale=0.0):
     return errs
 
 
-@pytest.mark.parametrize("d", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("d", [16, 32, 64, 128, 256, 512])
 @pytest.mark.parametrize("mask", [0, 1, 2, 3])
 def test_backward_shapes(d, mask):
     b, h, n = 2, 3, 300
@@ -98,8 +98,8 @@ def test_backward_shapes(d, mask):
     _check(q, k, v, do, mask, lens)
 
 
-@pytest.mark.parametrize("d", [128, 256])
-@pytest.mark.parametrize("n", [1, 17, 127, 128, 129, 256, 383])
+@pytest.mark.parametrize("d", [128, 256, 512])
+@pytest.mark.parametrize("n", [1, 17, 63, 64, 65, 127, 128, 129, 256, 383])
 def test_backward_ragged_lengths(d, n):
     q, k, v, do = _inputs(9100 + n + d, 1, 2, n, n, d)
     _check(q, k, v, do, 1, None)
@@ -214,6 +214,40 @@ def test_backward_wide_head_long_causal():
     _check(q, k, v, do, 1, None)
 
 
+@pytest.mark.parametrize("r", [1, 64, 129, 300])
+@pytest.mark.parametrize("mask", [0, 1, 3])
+def test_backward_head512_restricted(r, mask):
+    """Table 3, row (A): one head of 512 (64-key tiles, two CTAs per key
+    tile for the two halves of d, 32-query steps), with the restricted window."""
+    b, h, n = 2, 1, 520
+    q, k, v, do = _inputs(9270 + r + mask, b, h, n, n, 512)
+    lens = np.array([n, 290], np.int32) if mask & 2 else None
+    _check(q, k, v, do, mask, lens, r=r)
+
+
+def test_backward_head512_empty_rows():
+    """d = 512: a batch whose every key is hidden gets zero gradients, and
+    keys past a length get zero dK and dV."""
+    q, k, v, do = _inputs(9280, 2, 1, 200, 200, 512)
+    lens = np.array([0, 77], np.int32)
+    out, lse, dq, dk, dv = _gpu_forward_backward(q, k, v, do, 2, lens)
+    assert np.all(np.isneginf(lse[0])) and not np.isneginf(lse[1]).any()
+    assert not dq[0].any() and not dk[0].any() and not dv[0].any()
+    assert not dk[1, :, 77:].any() and not dv[1, :, 77:].any()
+    _check(q, k, v, do, 2, lens)
+
+
+def test_backward_head512_workload_length():
+    """The 512-wide workload's full sequence (causal n8192 d512, values
+    0.5 N(0,1), as bench.py --workload wide512) on one of its batch entries:
+    128 key tiles with up to 256 query steps each, every row of every
+    gradient."""
+    w = synthetic.WORKLOADS["wide_d512"]
+    q, k, v, _ = synthetic.sdpa_inputs(w, b=1, h=1)
+    do = synthetic.dout_input(w, b=1, h=1)
+    _check(q, k, v, do, w.mask_kind, None)
+
+
 @pytest.mark.parametrize("d", [16, 32])
 @pytest.mark.parametrize("n", [1, 65, 300])
 def test_backward_small_heads(d, n):
@@ -254,8 +288,14 @@ def test_backward_rejects_bad_arguments():
     ws = t.empty(sd.sdpa_backward_workspace_size(1, 1, 64, 64), dtype=t.uint8, device="cuda")
     with pytest.raises(sd.SdpaError, match="WORKSPACE"):
         sd.sdpa_backward(x, x, x, x, x, lse, x, x, x, ws, ws.numel() - 16, 1, 1, 64, 64, 64, 64)
-    x512 = t.zeros((1, 1, 64, 512), dtype=t.bfloat16, device="cuda")
+    # a head size outside Table 3
+    x96 = t.zeros((1, 1, 64, 96), dtype=t.bfloat16, device="cuda")
     with pytest.raises(sd.SdpaError, match="UNSUPPORTED"):
+        sd.sdpa_backward(x96, x96, x96, x96, x96, lse, x96, x96, x96, ws, ws.numel(), 1, 1,
+                         64, 64, 96, 96)
+    # 512-wide heads need the larger dQ accumulator
+    x512 = t.zeros((1, 1, 64, 512), dtype=t.bfloat16, device="cuda")
+    with pytest.raises(sd.SdpaError, match="WORKSPACE"):
         sd.sdpa_backward(x512, x512, x512, x512, x512, lse, x512, x512, x512, ws, ws.numel(), 1, 1,
                          64, 64, 512, 512)
     with pytest.raises(sd.SdpaError, match="INVALID_ARG"):

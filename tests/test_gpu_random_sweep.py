@@ -67,8 +67,6 @@ def test_forward_and_lse(seed):
 @pytest.mark.parametrize("seed", range(24))
 def test_backward(seed):
     rng, (b, h, n_q, n_k, d_k, d_v, mask, window, lens, scale), (q, k, v) = _case(seed)
-    if d_k == 512:
-        pytest.skip("the backward has no 512-wide heads")
     t = __import__("torch")
     do = _rand(rng, (b, h, n_q, d_v))
     w = window or None

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdpa.so")
 SOURCES = ["api.cu", "sdpa_tc.cu", "sdpa_one_tile.cu", "sdpa_bwd.cu", "sdpa_f32.cu", "gemm_tc.cu",
-           "decode.cu", "mha_noalloc.cu"]
+           "decode.cu", "mha_noalloc.cu", "sdpa_bwd_wide.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

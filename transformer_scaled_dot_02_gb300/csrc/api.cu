@@ -188,10 +188,10 @@ bool tc_head_sizes(int d_k, int d_v) {
   return d_v == 64 && (d_k == 16 || d_k == 32);
 }
 
-// Head shapes the backward supports: equal sizes up to 256 and Table 3's
+// Head shapes the backward supports: every equal size of Table 3 and its
 // rows (B), where the keys are smaller than the values.
 bool bwd_head_sizes(int d_k, int d_v) {
-  if (d_k == d_v) return d_k == 16 || d_k == 32 || d_k == 64 || d_k == 128 || d_k == 256;
+  if (d_k == d_v) return tc_head_size(d_k);
   return d_v == 64 && (d_k == 16 || d_k == 32);
 }
 
@@ -459,11 +459,12 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   float* dq_acc = reinterpret_cast<float*>(ws + 2 * round256(rows_pad * 4));
   sdpa::SdpaBwdParams bp;
   const long long dk_ = d_k, dv_ = d_v;
-  // the backward steps through the queries 64 at a time
-  const int q_rows = 64;
+  // the backward steps through the queries 64 (32 for 512-wide heads) at a
+  // time, against key tiles of 128 (64) rows
+  const int q_rows = sdpa::bwd_query_step(d_k), key_rows = sdpa::bwd_key_tile(d_k);
   if (!make_map_4d(&bp.tm_q, q, d_k, n_q, h, b, dk_, n_q * dk_, h * n_q * dk_, q_rows) ||
-      !make_map_4d(&bp.tm_k, k, d_k, n_k, h, b, dk_, n_k * dk_, h * n_k * dk_) ||
-      !make_map_4d(&bp.tm_v, v, d_v, n_k, h, b, dv_, n_k * dv_, h * n_k * dv_) ||
+      !make_map_4d(&bp.tm_k, k, d_k, n_k, h, b, dk_, n_k * dk_, h * n_k * dk_, key_rows) ||
+      !make_map_4d(&bp.tm_v, v, d_v, n_k, h, b, dv_, n_k * dv_, h * n_k * dv_, key_rows) ||
       !make_map_4d(&bp.tm_do, dout, d_v, n_q, h, b, dv_, n_q * dv_, h * n_q * dv_, q_rows))
     return SDPA_ERR_CUDA;
   // heads wider than 128 reduce dQ 32 query rows at a time
@@ -481,7 +482,7 @@ sdpa_status sdpa_backward(const void* q, const void* k, const void* v, const voi
   bp.n_k = n_k;
   bp.n_q_pad = n_q_pad;
   bp.mask_kind = mask_kind;
-  bp.num_kv_tiles = (n_k + 127) / 128;
+  bp.num_kv_tiles = (n_k + key_rows - 1) / key_rows;
   const float sc = effective_scale(scale, d_k);
   bp.scale_log2 = sc * 1.4426950408889634f;
   bp.scale = sc;

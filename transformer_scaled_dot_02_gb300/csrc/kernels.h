@@ -104,7 +104,7 @@ cudaError_t launch_sdpa_decode(const DecodeParams& p, int d_k, int d_v, cudaStre
 // Gradients of attention (bf16 BHSD tensors, fp32 accumulation).
 struct SdpaBwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 4-D (d, n, h, b) bf16 maps; d = d_k for Q, K
-  CUtensorMap tm_dq;          // 3-D (d_k, n_q, b*h) fp32 map of dq_acc, 32 x 64 boxes
+  CUtensorMap tm_dq;          // 3-D (d_k, n_q, b*h) fp32 map of dq_acc, 32-column boxes
   const float* neg_lse2;      // [b*h][n_q_pad] -lse_i log2(e) (-inf past n_q)
   const float* neg_dvec;      // [b*h][n_q_pad] -D_i = -dO_i . O_i
   float* dq_acc;              // [b*h][n_q][d_k] fp32 accumulator (zeroed by the prep kernel)
@@ -125,6 +125,13 @@ struct SdpaBwdPrepParams {
 };
 cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, int d_k, int d_v,
                             cudaStream_t stream);
+// Key rows per CTA (the K / V boxes' rows, and n_k's tile size) and query rows
+// per step (the Q / dO boxes' and the dQ reduce boxes' rows) of the backward
+// for a head size: 128 and 64, or 64 and 32 for 512-wide heads.
+int bwd_key_tile(int d_k);
+int bwd_query_step(int d_k);
+// The main kernel for 512-wide heads (after the prep kernel when `after_prep`).
+cudaError_t launch_sdpa_bwd_w512(const SdpaBwdParams& bp, bool after_prep, cudaStream_t stream);
 
 // Exact fp32 attention on the CUDA cores, BHSD contiguous.
 struct SdpaF32Params {

@@ -732,14 +732,16 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 }  // namespace n64
 
 // -D_i = -dO_i . O_i and -lse_i log2(e) (padded rows: 0 and -inf), dQ accumulator = 0.
-// DV / 8 lanes per row, 16 bytes of O and dO per lane; each lane also zeroes
-// DK / (DV / 8) of the row's fp32 dQ accumulator.
+// kElems values of O and dO per lane (8, or 16 for 512-wide rows), so that a
+// row takes at most one warp; each lane also zeroes DK / kLanes of the row's
+// fp32 dQ accumulator.
 template <int DK, int DV>
 __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) {
   griddep_launch_dependents();   // the main kernel may start its set-up now
-  constexpr int kLanes = DV / 8;
+  constexpr int kElems = DV > 256 ? DV / 32 : 8;
+  constexpr int kLanes = DV / kElems;
   constexpr int kRowsPerBlock = 256 / kLanes;
-  constexpr int kZero = DK / kLanes;   // 2, 4 or 8 accumulator floats per lane
+  constexpr int kZero = DK / kLanes;   // 2 to 16 accumulator floats per lane
   static_assert(kLanes <= 32, "one row per warp at most");
   const int sub = threadIdx.x % kLanes;
   const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanes;
@@ -756,15 +758,18 @@ __global__ void __launch_bounds__(256) sdpa_bwd_prep(const SdpaBwdPrepParams p) 
     }
     return;
   }
-  const long long src = (bh * p.n_q + i) * DV + sub * 8;
-  const uint4 o = *reinterpret_cast<const uint4*>(p.out + src);
-  const uint4 g = *reinterpret_cast<const uint4*>(p.dout + src);
-  const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+  const long long src = (bh * p.n_q + i) * DV + sub * kElems;
   float acc = 0.f;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    acc = fmaf(__uint_as_float(ow[w] << 16), __uint_as_float(gw[w] << 16), acc);
-    acc = fmaf(__uint_as_float(ow[w] & 0xffff0000u), __uint_as_float(gw[w] & 0xffff0000u), acc);
+  for (int v8 = 0; v8 < kElems / 8; ++v8) {
+    const uint4 o = *reinterpret_cast<const uint4*>(p.out + src + v8 * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(p.dout + src + v8 * 8);
+    const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      acc = fmaf(__uint_as_float(ow[w] << 16), __uint_as_float(gw[w] << 16), acc);
+      acc = fmaf(__uint_as_float(ow[w] & 0xffff0000u), __uint_as_float(gw[w] & 0xffff0000u), acc);
+    }
   }
   float* z = p.dq_acc + (bh * p.n_q + i) * DK + sub * kZero;
 #pragma unroll
@@ -794,22 +799,36 @@ __global__ void __launch_bounds__(256) sdpa_bwd_dq_convert(const SdpaBwdPrepPara
   *reinterpret_cast<uint4*>(p.dq + idx) = r;
 }
 
+// The prep kernel; reports whether it launched (no query rows: nothing to do).
+template <int DK, int DV>
+cudaError_t launch_prep(const SdpaBwdPrepParams& pp, cudaStream_t stream, bool* launched) {
+  const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
+  *launched = rows > 0;
+  if (rows == 0) return cudaSuccess;
+  constexpr long long kRowsPerBlock = 256 / (DV / (DV > 256 ? DV / 32 : 8));
+  sdpa_bwd_prep<DK, DV><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0,
+                          stream>>>(pp);
+  return cudaGetLastError();
+}
+
+// dQ = scale * accumulator, launched after the main kernel when it ran.
+template <int D>
+cudaError_t launch_convert(const SdpaBwdPrepParams& pp, cudaStream_t stream, bool after_main) {
+  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * D;
+  if (n == 0) return cudaSuccess;
+  return launch_kernel(sdpa_bwd_dq_convert<D>, dim3(static_cast<unsigned>((n / 8 + 255) / 256)),
+                       dim3(256), 0, stream, after_main, pp);
+}
+
 template <int DK, int DV>
 cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(pp.b) * pp.h * pp.n_q_pad;
-  cudaError_t err = cudaSuccess;
   // The main kernel launches with a programmatic dependency on the prep
   // kernel, and the convert kernel on the main one, whenever that kernel was
   // launched: each starts while its predecessor's last CTAs finish and waits
   // (griddep_wait) before reading what it wrote.
-  const bool prep = rows > 0;
-  if (prep) {
-    constexpr long long kRowsPerBlock = 256 / (DV / 8);
-    sdpa_bwd_prep<DK, DV><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256,
-                            0, stream>>>(pp);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-  }
+  bool prep = false;
+  cudaError_t err = launch_prep<DK, DV>(pp, stream, &prep);
+  if (err != cudaSuccess) return err;
   const int smem = n64::Cfg<DK, DV>::kSmemBytes;
   err = cudaFuncSetAttribute(n64::sdpa_bwd_tc_n64<DK, DV>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -821,11 +840,18 @@ cudaError_t launch_n64(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cud
                         dim3(n64::kThreads), smem, stream, prep, bp);
     if (err != cudaSuccess) return err;
   }
-  const long long n = static_cast<long long>(pp.b) * pp.h * pp.n_q * DK;
-  if (n > 0)
-    return launch_kernel(sdpa_bwd_dq_convert<DK>, dim3(static_cast<unsigned>((n / 8 + 255) / 256)),
-                         dim3(256), 0, stream, blocks > 0, pp);
-  return cudaSuccess;
+  return launch_convert<DK>(pp, stream, blocks > 0);
+}
+
+// 512-wide heads: the same prep and convert around the kernel of 64-key tiles.
+cudaError_t launch_w512(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp, cudaStream_t stream) {
+  bool prep = false;
+  cudaError_t err = launch_prep<512, 512>(pp, stream, &prep);
+  if (err != cudaSuccess) return err;
+  err = launch_sdpa_bwd_w512(bp, prep, stream);
+  if (err != cudaSuccess) return err;
+  const bool ran = static_cast<long long>(bp.num_kv_tiles) * bp.b * bp.h > 0;
+  return launch_convert<512>(pp, stream, ran);
 }
 
 }  // namespace
@@ -838,6 +864,7 @@ cudaError_t launch_sdpa_bwd(const SdpaBwdParams& bp, const SdpaBwdPrepParams& pp
     if (d_k == 64) return launch_n64<64, 64>(bp, pp, stream);
     if (d_k == 128) return launch_n64<128, 128>(bp, pp, stream);
     if (d_k == 256) return launch_n64<256, 256>(bp, pp, stream);
+    if (d_k == 512) return launch_w512(bp, pp, stream);
   }
   // Table 3, rows (B): smaller keys than values
   if (d_k == 16 && d_v == 64) return launch_n64<16, 64>(bp, pp, stream);
