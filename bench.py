@@ -9,7 +9,7 @@ causal mask, whole job (all ranks).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload long_causal|restricted|decode|wide512|backward|
-                                   tiny_f32|enc_base|enc_mha_base|dec_causal_base|
+                                   backward512|tiny_f32|enc_base|enc_mha_base|dec_causal_base|
                                    cross_big|cross_mha_big]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (no data-path collective); the timed region is bracketed by a barrier and the
@@ -19,7 +19,8 @@ bounded sample of the same workload on the host cores (rank 0 only).
 `--workload` other than the default measures one of the widened rows with the
 same JSON line (value, roofline, e2e, clocks, an oracle baseline on a bounded
 sample): restricted self-attention (r = 1024), one decoding step against
-8192-token caches, Table 3's single 512-wide head, and the backward pass; or
+8192-token caches, Table 3's single 512-wide head, and the backward pass (at
+d = 128 and at the 512-wide head); or
 one of the smaller configurations of the base and big models: the fp32 tiny
 case, the encoder's attention (core, and with its projections), the
 decoder's causal self-attention, and the big model's cross-attention (core,
@@ -346,7 +347,7 @@ def run_ours(args, world, rank, local):
 
 
 # ------------------------------------------------ the widened rows (--workload)
-ROW_WORKLOADS = ("restricted", "decode", "wide512", "backward")
+ROW_WORKLOADS = ("restricted", "decode", "wide512", "backward", "backward512")
 
 
 def _visible_restricted(w, rows):
@@ -456,7 +457,7 @@ def _pinned(a, dtype):
 
 
 def run_row(args, world, rank, local):
-    """One of the widened rows: restricted, decode, wide512 or backward."""
+    """One of the widened rows: restricted, decode, wide512, backward or backward512."""
     import torch
     import transformer_scaled_dot_02_gb300 as sd
 
@@ -476,6 +477,8 @@ def run_row(args, world, rank, local):
 
     if kind == "backward":
         w = synthetic.WORKLOADS["long_causal"]
+    elif kind == "backward512":
+        w = synthetic.WORKLOADS["wide_d512"]
     else:
         w = synthetic.WORKLOADS[{"restricted": "long_restricted", "decode": "decode_big",
                                  "wide512": "wide_d512"}[kind]]
@@ -582,9 +585,15 @@ def run_row(args, world, rank, local):
         ins = [(qd, hq), (kd, hk), (vd, hv), (fwd_out, hfo), (dod, hdo), (lse, hlse)]
         outs = list(zip(hgrads, grads))
         work = 2.0 * bh * w.n_q * w.n_k * (3 * w.d_k + 2 * w.d_v) / 2
-        metric = "attention backward TFLOP/s (dQ, dK, dV: five products) (1 GPU)"
-        desc = "backward of long causal self-attention b4 h16 n8192 d128 bf16"
-        kernel = "sdpa_bwd_tc_n64<128, 128> (with its prep and convert kernels)"
+        if kind == "backward":
+            metric = "attention backward TFLOP/s (dQ, dK, dV: five products) (1 GPU)"
+            desc = "backward of long causal self-attention b4 h16 n8192 d128 bf16"
+            kernel = "sdpa_bwd_tc_n64<128, 128> (with its prep and convert kernels)"
+        else:
+            metric = ("attention backward TFLOP/s (dQ, dK, dV: five products), one 512-wide "
+                      "head (Table 3 row A) (1 GPU)")
+            desc = "backward of long causal self-attention b4 h1 n8192 d_k=d_v=512 bf16"
+            kernel = "sdpa_bwd_tc_w512 (with its prep and convert kernels)"
         unit, bound, peak = "TFLOP/s", "tensor", float(peaks["bf16_tflops"])
         launches = 3
         prefix = min(args.cpu_rows or w.n_q, w.n_q)   # one whole head of the workload

@@ -7,11 +7,13 @@
 // At d = 512 a 128-key tile's K and V alone would take 256 KB of shared
 // memory, so a CTA here owns 64 keys (K and V resident, 128 KB) and one half
 // (256 columns) of d for its outputs; the two CTAs of a key tile both compute
-// the scores.  The score products run with M = 128: their lanes 64..127 read
-// the 64 rows that follow the tile in shared memory and are discarded.
+// the scores.  The score products run with M = 64, which puts key r in
+// tensor-memory lane (r mod 16) + 32 (r / 16): 16 lanes of each warp's quarter
+// (measured on GB300).  They read half the A bytes of an M = 128 product,
+// and shared-memory operand reads are what bound these small products.
 // dV and dK accumulate transposed, d in the tensor-memory lanes, so the half's
 // 256 columns of both take 256 tensor-memory columns:
-//   S^T = K Q^T,  dP^T = V dO^T        (M = 128 keys, N = 32 queries, K = 512)
+//   S^T = K Q^T,  dP^T = V dO^T        (M = 64 keys, N = 32 queries, K = 512)
 //   dV^T += dO^T P,  dK^T += Q^T dS    (M = 128 of d, N = 64 keys, K = 32 queries)
 //   dQ^T = K^T dS^T                    (M = 128 of d, N = 32 queries, K = 64 keys)
 // P and dS go through shared memory as [key][query] rows.  Queries come in
@@ -57,29 +59,26 @@ constexpr int kNumBars = 1 + 4 + 4 + 2 + 1 + 1 + 2 + 2 + 1 + 1;
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kQnOff % 1024 == 0 && kPOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
-// The score products' discarded lanes read 64 rows (8 KB) past the last K and
-// V boxes: V's first box and Q's first part, both inside the CTA's memory.
-static_assert(kVOff + kBoxes * kKVBox + kKVBox <= kBarOff, "discarded rows in bounds");
 
-// Warps: 0, 1, 4, 5 compute (key lanes 32 (w % 4) .. +32, query half w / 4);
-// 2 TMA producer; 3 MMA issuer; 6..9 dQ^T and, at the end, dV and dK out of
-// tensor memory (lane quarter w % 4).
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 2;
-constexpr int kMmaWarp = 3;
-constexpr int kEpilogueWarp0 = 6;
-constexpr int kCompute = 128;
+// Warps: 0..7 compute (lanes 0..15 of quarter w % 4 hold keys 16 (w % 4) ..
+// +16; query half w / 4); 8 TMA producer; 9 MMA issuer; 10..13 dQ^T and, at
+// the end, dV and dK out of tensor memory (lane quarter w % 4).
+constexpr int kThreads = 448;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEpilogueWarp0 = 10;
+constexpr int kCompute = 256;
 constexpr int kEpilogue = 128;
 constexpr int kHeadGroup = 2;     // heads whose key tiles run together (Q, dO, dQ stay in L2)
 
 // Tensor-memory columns.
-constexpr uint32_t kColS = 0;        // S^T, 32 columns (lanes 0..63 used)
+constexpr uint32_t kColS = 0;        // S^T, 32 columns (M = 64 layout)
 constexpr uint32_t kColDP = 32;      // dP^T
 constexpr uint32_t kColDV = 64;      // dV^T: two 128-lane blocks of d x 64 keys
 constexpr uint32_t kColDK = 192;     // dK^T
 constexpr uint32_t kColDQ = 320;     // dQ^T: two buffers of (two blocks x 32 queries)
 
-constexpr uint32_t kIdescS = idesc_bf16(128, kBN, false, false);     // S^T, dP^T
+constexpr uint32_t kIdescS = idesc_bf16(kKeys, kBN, false, false);   // S^T, dP^T (M = 64)
 constexpr uint32_t kIdescG = idesc_bf16(128, kKeys, true, false);    // dV^T, dK^T
 constexpr uint32_t kIdescQ = idesc_bf16(128, kBN, true, true);       // dQ^T
 // every operand: 128-byte swizzle, 8-row groups 1024 bytes apart
@@ -459,11 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
         }
       }
     }
-  } else if ((warp & 3) < 2) {
+  } else {
     // ------------------------------------------------------- compute warps
+    // Lanes 16..31 read tensor-memory lanes that the M = 64 scores leave
+    // unwritten; they compute on them but store nothing.
     const int quarter = warp & 3;
     const int qh = warp >> 2;                         // queries 16 qh .. +16 of each step
-    const int r = quarter * 32 + lane;                // key lane
+    const bool active = lane < 16;
+    const int r = quarter * 16 + (lane & 15);         // key row of the tile
     const int key = key0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int it = 0; it < n_it; ++it) {
@@ -475,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
       const int q0 = (i_lo + it) * kBN + qh * 16;
       const uint32_t vec = smem_base + kVecOff + b * kVecBytes + qh * 16 * 4;
       // this key sees all 16 queries: no per-element mask
-      const bool all = key < kv_len && (!causal || key <= q0) && key >= q0 + 15 - p.win_left &&
-                       key <= q0 + p.win_right;
+      const bool all = !active || (key < kv_len && (!causal || key <= q0) &&
+                                   key >= q0 + 15 - p.win_left && key <= q0 + p.win_right);
       uint32_t sv[16], dp[16];
       tmem_ld16(lane_base + kColS + qh * 16, sv);
       tmem_ld16(lane_base + kColDP + qh * 16, dp);
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
         rows(std::true_type{});
       // row r of P^T and dS^T, queries [16 qh, +16): 16-byte chunks 2 qh, 2 qh + 1
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 2 && active; ++c) {
         const uint32_t off = sw128_offset(static_cast<uint32_t>(r), static_cast<uint32_t>(qh * 2 + c));
         *reinterpret_cast<uint4*>(smem + kPOff + off) =
             make_uint4(pk[c * 4 + 0], pk[c * 4 + 1], pk[c * 4 + 2], pk[c * 4 + 3]);
