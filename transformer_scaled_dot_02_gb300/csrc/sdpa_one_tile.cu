@@ -32,7 +32,12 @@
 //               running max / sum, P in bf16 over the scores it replaces, the
 //               O rescale when the max moves, and the epilogue.
 // Tensor memory: score buffers S_0 at 0 and S_1 at BN (fp32, BN keys each),
-// O at 2 BN (min(d, 256) fp32 columns).
+// O at 2 BN (min(d, 256) fp32 columns).  For d = 256 and 512 the last 128
+// columns hold the first 256 columns of Q (bf16 pairs): the softmax warps
+// copy their rows there once Q has landed, and those k steps of the scores
+// take A from tensor memory.  A score product with A in shared memory
+// re-reads the 4 KB of Q per k step and is bound by that read (48 clk at
+// N = 64); with A in tensor memory it runs at its compute time (32 clk).
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -76,8 +81,8 @@ struct OCfg {
   static constexpr int kVOff = kKOff + kStages * kKBytes;
   static constexpr int kBarOff = kVOff + kStages * kVBytes;
   // q_full, k_full[2], v_full[2], s_full[2], p_full[2], o_full[2], o_last, drain,
-  // kh_free
-  static constexpr int kNumBars = 1 + 10 + 3;
+  // kh_free, q_tmem
+  static constexpr int kNumBars = 1 + 10 + 4;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
@@ -90,6 +95,13 @@ struct OCfg {
       kOCol + kDvc <= 128 ? 128u : (kOCol + kDvc <= 256 ? 256u : 512u);
   static constexpr int kMinBlocks = static_cast<int>(512u / kTmemCols);
   static_assert(kOCol + kDvc <= kTmemCols, "tensor memory");
+  // Score k steps whose A operand (Q) sits in tensor memory after O: all of a
+  // 256-wide Q, the first half of a 512-wide one (the K half of part 0).
+  static constexpr int kQTmemSteps = DK >= 256 ? 16 : 0;
+  static constexpr uint32_t kQCol = kOCol + kDvc;
+  static_assert(kQCol + kQTmemSteps * 8 <= kTmemCols, "Q in tensor memory");
+  static_assert(kQTmemSteps == 0 || (kRowBytes == 128 && (kQTmemSteps * 16) % kBoxCols == 0),
+                "Q copied by whole 128-byte-swizzled boxes");
   static_assert(kSmemBytes * kMinBlocks <= 232448 - 1024 * kMinBlocks, "CTAs per SM");
 };
 
@@ -127,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
   uint64_t* o_last = o_full + 2;   // once, after the last O += P V
   uint64_t* drain = o_last + 1;
   uint64_t* kh_free = drain + 1;   // one stage: the first half of S(u) is done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(kh_free + 1);
+  uint64_t* q_tmem = kh_free + 1;  // the softmax warps copied Q into tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_tmem + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const AbortState ab{abort_flag, p.status};
 
@@ -171,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
     mbar_init(o_last, 1);
     mbar_init(drain, 1);
     mbar_init(kh_free, 1);
+    mbar_init(q_tmem, kBlockM);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -309,10 +323,13 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
         for (int k = 0; k < kSteps; ++k) {
           if (k < k_begin || k >= k_begin + kSteps / parts) continue;
           constexpr int kS = C::kStepsPerRow;
-          mma_bf16_ss_warp(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
-                           kDescHi,
-                           b0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4),
-                           kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
+          const uint32_t bk = b0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4);
+          if (k < C::kQTmemSteps)
+            mma_bf16_ts_warp(d, tmem + C::kQCol + static_cast<uint32_t>(k * 8), bk, kDescHi,
+                             C::kIdescS, k > 0 ? 1u : 0u);
+          else
+            mma_bf16_ss_warp(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
+                             kDescHi, bk, kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
         }
         if (part + 1 < parts) {
           mma_commit_warp(kh_free);
@@ -341,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
       };
       constexpr int kParts = C::kOneStage ? 2 : 1;
       bool ok = mbar_wait_warp(q_full, 0, ab);
+      if (C::kQTmemSteps > 0 && ok) ok = mbar_wait_warp(q_tmem, 0, ab);
       tc_fence_after();
       for (int part = 0; ok && part < kParts; ++part) ok = issue_s(0, part, kParts);
       for (int u = 0; ok && u < n_kv; ++u) {
@@ -376,7 +394,34 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
     float m_used = -INFINITY;
     float l = 0.f;
     bool ok = true;
-    for (int u = 0; u < n_kv; ++u) {
+    if constexpr (C::kQTmemSteps > 0) {
+      // this thread's row of Q, its first kQTmemSteps * 16 columns, into its
+      // tensor-memory lane as bf16 pairs (the A layout of a K-major product)
+      if (n_kv > 0) {
+        ok = mbar_wait_warp(q_full, 0, ab);
+        if (ok) {
+#pragma unroll 1
+          for (int c = 0; c < C::kQTmemSteps * 16 / C::kBoxCols; ++c) {
+            const uint8_t* box = smem + C::kQOff + c * C::kQBox;
+            uint32_t w[32];
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const uint4 v = *reinterpret_cast<const uint4*>(
+                  box + sw128_offset(static_cast<uint32_t>(row_in_tile), static_cast<uint32_t>(ch)));
+              w[ch * 4 + 0] = v.x;
+              w[ch * 4 + 1] = v.y;
+              w[ch * 4 + 2] = v.z;
+              w[ch * 4 + 3] = v.w;
+            }
+            tmem_st32(lane_base + C::kQCol + static_cast<uint32_t>(c * 32), w);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(q_tmem);
+      }
+    }
+    for (int u = 0; ok && u < n_kv; ++u) {
       const uint32_t s_col = static_cast<uint32_t>((u & 1) * BN);
       ok = mbar_wait_warp(s_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
       if (!ok) break;
