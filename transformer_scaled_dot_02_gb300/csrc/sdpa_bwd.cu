@@ -79,8 +79,9 @@ constexpr int kHeadGroup = 4;            // heads whose key tiles run together
 constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (128-byte rows)
 constexpr int kVecBytes = 2 * kBN * 4;   // -lse2 and -D of one step
 // kv_full, q_full[3], q_empty[3], s_full[2], p_full[2], dq_full[2],
-// dq_empty[2], acc_full, drain
-constexpr int kNumBars = 1 + 2 * kStages + 8 + 2;
+// dq_empty[2], acc_full, drain, then (wide heads) part_full[4],
+// part_empty[4], vec_full[2]
+constexpr int kNumBars = 1 + 2 * kStages + 8 + 2 + 10;
 constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
 // dQ^T = K^T dS^T always with M = 128 lanes of d: for d_k < 128 the upper lanes
 // read the tiles that follow K in shared memory and are discarded.
@@ -122,8 +123,11 @@ struct Cfg {
   // Heads wider than 128 (d_k = d_v = 256): dK, dV and dQ in 128-column
   // chunks, one CTA per chunk, each recomputing S^T and dP^T over the whole
   // head.  K and V stay resident (128 KB), which leaves room for one stage
-  // of Q and dO and one dS^T buffer, so the steps run in order: products of
-  // step i, then the loads and scores of step i + 1.
+  // of Q and dO and one dS^T buffer.  The stage's boxes come in four parts
+  // with barriers of their own: Q's and dO's boxes of the other chunk, free
+  // once the step's scores have read them, and of this CTA's chunk, free
+  // once dV and dK have; so the next step's loads run while this step's
+  // softmax and products do.
   static constexpr bool kWide = DK > 128;
   static constexpr int kColsK = kWide ? 128 : DK;           // dK / dQ columns of a CTA
   static constexpr int kColsV = kWide ? 128 : DV;           // dV columns of a CTA
@@ -141,7 +145,8 @@ struct Cfg {
   static constexpr int kDsOff = kStageOff + kStagesQ * kStageBytes;   // dS^T buffers
   static constexpr int kStagingOff = kDsOff + kDsBufs * kDsTile;  // 4 warps x [kDqRows][kDCols] fp32
   static constexpr int kVecOff = kStagingOff + 4 * kDqRows * kDCols * 4;
-  static constexpr int kBarOff = kVecOff + kStagesQ * kVecBytes;
+  static constexpr int kVecBufs = kWide ? 2 : kStagesQ;       // -lse2 / -D slots
+  static constexpr int kBarOff = kVecOff + kVecBufs * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescDV = idesc_bf16(kBM, kColsV, false, true);  // dV (A in TMEM)
   static constexpr uint32_t kIdescDK = idesc_bf16(kBM, kColsK, false, true);  // dK (A in TMEM)
@@ -210,7 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   uint64_t* dq_empty = dq_full + 2;
   uint64_t* acc_full = dq_empty + 2;
   uint64_t* drain = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // wide heads: parts 0..3 = Q other, dO other, Q own, dO own (box pairs)
+  uint64_t* part_full = drain + 1;
+  uint64_t* part_empty = part_full + 4;
+  uint64_t* vec_full = part_empty + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const AbortState ab{abort_flag, p.status};
 
@@ -263,6 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(part_full + s, 1);
+      mbar_init(part_empty + s, 1);
+    }
+    mbar_init(vec_full, 1);
+    mbar_init(vec_full + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -287,6 +302,56 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tma_load_4d(&p.tm_k, kv_full, smem + C::kKOff + c * LK::kKVBox, c * LK::kBoxCols, key0, hi, bi);
       for (int c = 0; c < LV::kBoxes; ++c)
         tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * LV::kKVBox, c * LV::kBoxCols, key0, hi, bi);
+      if constexpr (C::kWide) {
+        // four parts of two boxes each, in the order the MMA warp frees them:
+        // Q other, dO other (after the step's scores), Q own, dO own (after
+        // dV and dK); the step's vectors go with the first part, into one of
+        // two slots (the slot's last reader, step it - 2, finished before
+        // the scores of step it - 1 were issued)
+        int issued[4] = {0, 0, 0, 0};
+        int vec_issued = 0;
+        bool go = true;
+        uint8_t* st = smem + C::kStageOff;
+        for (int it = 0; go && it < n_it; ++it) {
+          const int q0 = (i_lo + it) * kBN;
+#pragma unroll
+          for (int pt = 0; pt < 4; ++pt) {
+            if (it > 0 && !mbar_wait(part_empty + pt, static_cast<uint32_t>(it - 1) & 1u, ab)) {
+              go = false;
+              break;
+            }
+            const bool is_do = (pt & 1) != 0;
+            const int c0 = 2 * (pt >= 2 ? chunk : 1 - chunk);
+            mbar_arrive_expect_tx(part_full + pt, 2 * LK::kQBox);
+            for (int j = 0; j < 2; ++j) {
+              const int c = c0 + j;
+              if (is_do)
+                tma_load_4d(&p.tm_do, part_full + pt, st + LK::kQTile + c * LV::kQBox,
+                            c * LV::kBoxCols, q0, hi, bi);
+              else
+                tma_load_4d(&p.tm_q, part_full + pt, st + c * LK::kQBox, c * LK::kBoxCols, q0, hi,
+                            bi);
+            }
+            issued[pt] = it + 1;
+            if (pt == 0) {
+              uint64_t* vb = vec_full + (it & 1);
+              const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
+              uint8_t* vec = smem + C::kVecOff + (it & 1) * kVecBytes;
+              mbar_arrive_expect_tx(vb, kVecBytes);
+              tma_load_1d(vec, p.neg_lse2 + vrow, kBN * 4, vb);
+              tma_load_1d(vec + kBN * 4, p.neg_dvec + vrow, kBN * 4, vb);
+              vec_issued = it + 1;
+            }
+          }
+        }
+        // let the copies still in flight land before the CTA can exit
+        mbar_wait_drain(kv_full, 0);
+        for (int pt = 0; pt < 4; ++pt)
+          if (issued[pt] > 0)
+            mbar_wait_drain(part_full + pt, static_cast<uint32_t>(issued[pt] - 1) & 1u);
+        for (int it = max(0, vec_issued - 2); it < vec_issued; ++it)
+          mbar_wait_drain(vec_full + (it & 1), static_cast<uint32_t>(it >> 1) & 1u);
+      } else {
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % C::kStagesQ;
@@ -309,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       mbar_wait_drain(kv_full, 0);
       for (int it = max(0, issued - C::kStagesQ); it < issued; ++it)
         mbar_wait_drain(q_full + it % C::kStagesQ, static_cast<uint32_t>(it / C::kStagesQ) & 1u);
+      }
     }
   } else if (warp == kMmaWarp) {
     // The whole warp runs this loop in step (warp-uniform waits and
@@ -341,22 +407,74 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         else
           product(LK{}, k_smem, st, DK);
       };
-      bool ok = mbar_wait_warp(kv_full, 0, ab) && mbar_wait_warp(q_full, 0, ab);
-      tc_fence_after();
-      if (ok) {
-        issue_s(0, false);
-        issue_s(0, true);
-#ifndef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
-        mma_commit_warp(s_full);
+      // Wide heads: S^T(it) and dP^T(it) part by part as the stage's parts
+      // land, the other chunk's boxes first; frees those two parts, then
+      // commits s_full once this chunk's boxes are in.  dP^T(it) lands where
+      // dQ^T(it - 2) was, so it waits for that step's epilogue.
+      auto wide_scores = [&](int it) -> bool {
+        const uint32_t par = static_cast<uint32_t>(it) & 1u;
+        const uint32_t st = smem_base + C::kStageOff;
+        auto part = [&](bool dp, bool own, bool first) {
+          const int c0 = 2 * (own ? chunk : 1 - chunk);
+          const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int c = c0 + j;
+            const uint32_t a0 = lo((dp ? v_smem : k_smem) + c * LK::kKVBox, 16);
+            const uint32_t b0 = lo(st + (dp ? LK::kQTile : 0) + c * LK::kQBox, 16);
+#pragma unroll
+            for (int kk = 0; kk < LK::kStepsPerRow; ++kk)
+              mma_bf16_ss_warp(d, a0 + static_cast<uint32_t>(kk * 2), LK::kDescHi,
+                               b0 + static_cast<uint32_t>(kk * 2), LK::kDescHi, kIdescS,
+                               (first && j == 0 && kk == 0) ? 0u : 1u);
+          }
+        };
+        if (!mbar_wait_warp(part_full + 0, par, ab)) return false;
+        tc_fence_after();
+        part(false, false, true);
+        if (it >= 2) {
+          if (!mbar_wait_warp(dq_empty + (it & 1), static_cast<uint32_t>((it - 2) >> 1) & 1u, ab))
+            return false;
+          tc_fence_after();
+        }
+        if (!mbar_wait_warp(part_full + 1, par, ab)) return false;
+        tc_fence_after();
+        part(true, false, true);
+        mma_commit_warp(part_empty + 0);
+        mma_commit_warp(part_empty + 1);
+        if (!mbar_wait_warp(part_full + 2, par, ab)) return false;
+        tc_fence_after();
+        part(false, true, false);
+        if (!mbar_wait_warp(part_full + 3, par, ab)) return false;
+        tc_fence_after();
+        part(true, true, false);
+#ifdef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
+        if (it == 0) return true;
 #endif
-        // (test builds only, never in libsdpa.so: the first S^T / dP^T tile
-        // is never signalled, so the compute warps' bounded wait runs out and
-        // every other role leaves through the abort flag or its own limit)
+        mma_commit_warp(s_full + (it & 1));
+        return true;
+      };
+      bool ok = mbar_wait_warp(kv_full, 0, ab);
+      if constexpr (C::kWide) {
+        tc_fence_after();
+        if (ok) ok = wide_scores(0);
+      } else {
+        ok = ok && mbar_wait_warp(q_full, 0, ab);
+        tc_fence_after();
+        if (ok) {
+          issue_s(0, false);
+          issue_s(0, true);
+#ifndef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
+          mma_commit_warp(s_full);
+#endif
+          // (test builds only, never in libsdpa.so: the first S^T / dP^T tile
+          // is never signalled, so the compute warps' bounded wait runs out and
+          // every other role leaves through the abort flag or its own limit)
+        }
       }
       if constexpr (C::kWide) {
-        // One stage of Q / dO: step i's products free it, then step i + 1
-        // loads and its scores run.  This CTA's chunk of dV, dK and dQ^T
-        // reads the matching 128 columns (two boxes) of dO, Q and K.
+        // This CTA's chunk of dV, dK and dQ^T reads the matching 128 columns
+        // (two boxes) of dO, Q and K.
         const uint32_t col_boxes = static_cast<uint32_t>(chunk * (128 / LK::kBoxCols));
         for (int it = 0; ok && it < n_it; ++it) {
           const int b = it & 1;
@@ -377,7 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
                              bq + (static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4), LK::kDescHi,
                              C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit_warp(q_empty);
+          // this chunk's boxes of Q and dO are free
+          mma_commit_warp(part_empty + 2);
+          mma_commit_warp(part_empty + 3);
           // dQ^T(it) = K_j[:, chunk]^T dS^T(it) into the dP^T half of buffer b
           // (dP^T(it) is consumed: the compute warps released P(it))
           const uint32_t ak = lo(smem_base + C::kKOff + col_boxes * LK::kKVBox, LK::kKVBox);
@@ -390,21 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
                              k > 0 ? 1u : 0u);
           }
           mma_commit_warp(dq_full + b);
-          if (it + 1 < n_it) {
-            const int nx = it + 1;
-            ok = mbar_wait_warp(q_full, static_cast<uint32_t>(nx) & 1u, ab);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(nx, false);
-            // dP^T(it+1) lands where dQ^T(it-1) was: its epilogue must have read it
-            if (it >= 1) {
-              ok = mbar_wait_warp(dq_empty + (nx & 1), static_cast<uint32_t>((it - 1) >> 1) & 1u, ab);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            issue_s(nx, true);
-            mma_commit_warp(s_full + (nx & 1));
-          }
+          if (it + 1 < n_it && !(ok = wide_scores(it + 1))) break;
         }
       }
       for (int it = 0; !C::kWide && ok && it < n_it; ++it) {
@@ -606,9 +712,14 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
 
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1;
-      const int s = it % C::kStagesQ;
-      ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / C::kStagesQ) & 1u, ab) &&
-           mbar_wait_warp(s_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
+      // the step's -lse2 and -D: with the stage (narrow heads) or in a slot
+      // of their own (wide heads, whose stage parts are refilled early)
+      const int s = C::kWide ? (it & 1) : it % C::kStagesQ;
+      if constexpr (C::kWide)
+        ok = mbar_wait_warp(vec_full + s, static_cast<uint32_t>(it >> 1) & 1u, ab);
+      else
+        ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / C::kStagesQ) & 1u, ab);
+      ok = ok && mbar_wait_warp(s_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
       if (!ok) break;
       tc_fence_after();
       const int qh0 = (i_lo + it) * kBN + half * 32;
