@@ -596,7 +596,10 @@ def run_row(args, world, rank, local):
             kernel = "sdpa_bwd_tc_w512 (with its prep and convert kernels)"
         unit, bound, peak = "TFLOP/s", "tensor", float(peaks["bf16_tflops"])
         launches = 3
-        prefix = min(args.cpu_rows or w.n_q, w.n_q)   # one whole head of the workload
+        # one whole head of the workload at d = 128 (about 12 s of the oracle);
+        # at d = 512 its first 4096 query and key rows (about 12 s as well)
+        default_rows = w.n_q if w.d_k <= 128 else w.n_q // 2
+        prefix = min(args.cpu_rows or default_rows, w.n_q)
 
         def oracle_sample():
             import oracle
