@@ -87,3 +87,27 @@ def test_mha_ragged_causal(d):
     sd.sdpa_device_check()
     ref = oracle.mha(x, x, *ws, h, d, d, sd.SDPA_MASK_CAUSAL)
     assert parity_err(host(y), ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("h,d_k,d_v", [(1, 512, 512), (2, 256, 256), (4, 128, 128), (16, 32, 32),
+                                       (32, 16, 16), (8, 16, 64), (8, 32, 64)])
+@pytest.mark.parametrize("mask", [1, 2])
+def test_mha_table3_heads(h, d_k, d_v, mask):
+    """Multi-head attention at d_model 512 with Table 3's head shapes (rows
+    (A) and (B), and two heads of 256): causal self-attention, and
+    cross-attention with key padding, ragged lengths."""
+    rng = np.random.default_rng(23 + h + d_k + 7 * d_v + mask)
+    b, dm = 2, 512
+    n_q = 300
+    n_k = n_q if mask & 1 else 170
+    xq = synthetic.round_to_bf16(rng.standard_normal((b, n_q, dm)).astype(np.float32))
+    xkv = xq if mask & 1 else synthetic.round_to_bf16(
+        rng.standard_normal((b, n_k, dm)).astype(np.float32))
+    ws = [synthetic.round_to_bf16((rng.standard_normal(s) / np.sqrt(s[0])).astype(np.float32))
+          for s in [(dm, h * d_k), (dm, h * d_k), (dm, h * d_v), (h * d_v, dm)]]
+    lens = np.array([n_k, 97], np.int32) if mask & 2 else None
+    y = sd.multi_head_attention(dev(xq), dev(xkv), *[dev(a) for a in ws], h, mask,
+                                None if lens is None else dev_int(lens))
+    sd.sdpa_device_check()
+    ref = oracle.mha(xq, xkv, *ws, h, d_k, d_v, mask, lens)
+    assert parity_err(host(y), ref) <= TOL_BF16

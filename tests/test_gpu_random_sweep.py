@@ -102,7 +102,7 @@ def test_decode(seed):
 @pytest.mark.parametrize("seed", range(12))
 def test_multi_head(seed):
     rng = np.random.default_rng(72000 + seed)
-    d = int(rng.choice([16, 32, 64, 128]))
+    d_k, d_v = HEADS[rng.integers(len(HEADS))]
     h = int(rng.integers(1, 5))
     dm = int(rng.choice([64, 256, 520]))
     b = int(rng.integers(1, 4))
@@ -113,12 +113,12 @@ def test_multi_head(seed):
     xq = _rand(rng, (b, n_q, dm))
     xkv = _rand(rng, (b, n_k, dm)) if cross else xq
     ws = [synthetic.round_to_bf16((rng.standard_normal(s) / np.sqrt(s[0])).astype(np.float32))
-          for s in [(dm, h * d)] * 3 + [(h * d, dm)]]
+          for s in [(dm, h * d_k), (dm, h * d_k), (dm, h * d_v), (h * d_v, dm)]]
     lens = None
     if mask & 2:
         lens = rng.integers(0, n_k + 10, size=b).astype(np.int32)
     y = sd.multi_head_attention(dev(xq), dev(xkv), *[dev(a) for a in ws], h, mask,
                                 None if lens is None else dev_int(lens))
     sd.sdpa_device_check()
-    ref = oracle.mha(xq, xkv, *ws, h, d, d, mask, lens)
-    assert parity_err(host(y), ref) <= TOL_BF16, (b, h, n_q, n_k, d, dm, mask)
+    ref = oracle.mha(xq, xkv, *ws, h, d_k, d_v, mask, lens)
+    assert parity_err(host(y), ref) <= TOL_BF16, (b, h, n_q, n_k, d_k, d_v, dm, mask)
