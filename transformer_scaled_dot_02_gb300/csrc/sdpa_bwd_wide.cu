@@ -51,11 +51,15 @@ constexpr int kDsOff = kPOff + kKeys * 128;                // dS^T, same layout
 constexpr int kStagingWarp = kBN * 32 * 4;                 // [32 rows][32 columns] fp32
 constexpr int kStagingOff = kDsOff + kKeys * 128;          // 208 KB: one per epilogue warp
 constexpr int kVecBytes = 2 * kBN * 4;                     // -lse2 and -D of one step
-constexpr int kVecOff = kStagingOff + 4 * kStagingWarp;    // 224 KB: two steps' vectors
-constexpr int kBarOff = kVecOff + 2 * kVecBytes;
-// kv_full, full[4], empty[4], vec_full[2], s_full, p_full, dq_full[2],
+// Three steps' vectors: step it + 2's are loaded once the scores of step
+// it + 1 over the other half have read their Q part, which can be before the
+// softmax of step it has read step it's; step it + 3's only after it has.
+constexpr int kVecSlots = 3;
+constexpr int kVecOff = kStagingOff + 4 * kStagingWarp;    // 224 KB
+constexpr int kBarOff = kVecOff + kVecSlots * kVecBytes;
+// kv_full, full[4], empty[4], vec_full[3], s_full, p_full, dq_full[2],
 // dq_empty[2], acc_full, drain
-constexpr int kNumBars = 1 + 4 + 4 + 2 + 1 + 1 + 2 + 2 + 1 + 1;
+constexpr int kNumBars = 1 + 4 + 4 + kVecSlots + 1 + 1 + 2 + 2 + 1 + 1;
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kQnOff % 1024 == 0 && kPOff % 1024 == 0 && kStagingOff % 1024 == 0, "align");
@@ -71,12 +75,14 @@ constexpr int kCompute = 256;
 constexpr int kEpilogue = 128;
 constexpr int kHeadGroup = 2;     // heads whose key tiles run together (Q, dO, dQ stay in L2)
 
-// Tensor-memory columns.
-constexpr uint32_t kColS = 0;        // S^T, 32 columns (M = 64 layout)
-constexpr uint32_t kColDP = 32;      // dP^T
-constexpr uint32_t kColDV = 64;      // dV^T: two 128-lane blocks of d x 64 keys
-constexpr uint32_t kColDK = 192;     // dK^T
-constexpr uint32_t kColDQ = 320;     // dQ^T: two buffers of (two blocks x 32 queries)
+// Tensor-memory columns.  Two score buffers (step parity): the next step's
+// scores over the other half's boxes run while the softmax works on this
+// step's.
+constexpr uint32_t kColS = 0;        // S^T at kColS + 64 b, 32 columns (M = 64 layout)
+constexpr uint32_t kColDP = 32;      // dP^T at kColDP + 64 b
+constexpr uint32_t kColDV = 128;     // dV^T: two 128-lane blocks of d x 64 keys
+constexpr uint32_t kColDK = 256;     // dK^T
+constexpr uint32_t kColDQ = 384;     // dQ^T: two buffers of (two blocks x 32 queries)
 
 constexpr uint32_t kIdescS = idesc_bf16(kKeys, kBN, false, false);   // S^T, dP^T (M = 64)
 constexpr uint32_t kIdescG = idesc_bf16(128, kKeys, true, false);    // dV^T, dK^T
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
   uint64_t* full = bar + 1;        // Q other, Q own, dO other, dO own
   uint64_t* empty = full + 4;
   uint64_t* vec_full = empty + 4;
-  uint64_t* s_full = vec_full + 2;
+  uint64_t* s_full = vec_full + kVecSlots;
   uint64_t* p_full = s_full + 1;
   uint64_t* dq_full = p_full + 1;
   uint64_t* dq_empty = dq_full + 2;
@@ -202,8 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
       mbar_init(full + s, 1);
       mbar_init(empty + s, 1);
     }
+    for (int v = 0; v < kVecSlots; ++v) mbar_init(vec_full + v, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(vec_full + b, 1);
       mbar_init(dq_full + b, 1);
       mbar_init(dq_empty + b, kEpilogue);
     }
@@ -255,10 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
                         part_box(half, own, j) * kBoxCols, q0, hi, bi);
           issued[s] = it + 1;
           if (s == kQo) {
-            // this step's -lse2 and -D; the buffer's last reader (step it - 2)
-            // finished before the scores of step it - 1 were issued
-            uint64_t* vb = vec_full + (it & 1);
-            uint8_t* vec = smem + kVecOff + (it & 1) * kVecBytes;
+            // this step's -lse2 and -D into slot it % 3; the slot's last
+            // reader (the softmax of step it - 3) finished before the scores
+            // of step it - 1 over the other half were issued, and those
+            // released this Q part
+            uint64_t* vb = vec_full + it % kVecSlots;
+            uint8_t* vec = smem + kVecOff + (it % kVecSlots) * kVecBytes;
             const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
             mbar_arrive_expect_tx(vb, kVecBytes);
             tma_load_1d(vec, p.neg_lse2 + vrow, kBN * 4, vb);
@@ -271,18 +279,18 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
       mbar_wait_drain(kv_full, 0);
       for (int s = 0; s < 4; ++s)
         if (issued[s] > 0) mbar_wait_drain(full + s, static_cast<uint32_t>(issued[s] - 1) & 1u);
-      for (int it = vec_issued > 2 ? vec_issued - 2 : 0; it < vec_issued; ++it)
-        mbar_wait_drain(vec_full + (it & 1), static_cast<uint32_t>(it >> 1) & 1u);
+      for (int it = vec_issued > kVecSlots ? vec_issued - kVecSlots : 0; it < vec_issued; ++it)
+        mbar_wait_drain(vec_full + it % kVecSlots, static_cast<uint32_t>(it / kVecSlots) & 1u);
     }
   } else if (warp == kMmaWarp) {
     // The whole warp runs this loop in step; one elected lane issues.
     if (n_it > 0) {
-      // S^T (dp false) or dP^T (dp true) over the four boxes of one part of
-      // the current step; `first` starts the accumulation
-      auto scores = [&](bool dp, bool own, bool first) {
+      // S^T (dp false) or dP^T (dp true) of step `it` over the four boxes of
+      // one part, into the step's score buffer; `first` starts the accumulation
+      auto scores = [&](int it, bool dp, bool own, bool first) {
         const uint32_t a_base = smem_base + (dp ? kVOff : kKOff);
         const uint32_t b_base = smem_base + part_off(dp ? (own ? kDh : kDo) : (own ? kQh : kQo));
-        const uint32_t d = tmem + (dp ? kColDP : kColS);
+        const uint32_t d = tmem + (dp ? kColDP : kColS) + static_cast<uint32_t>((it & 1) * 64);
 #pragma unroll
         for (int j = 0; j < kHalfBoxes; ++j) {
           const uint32_t a0 = desc_lo(a_base + part_box(half, own, j) * kKVBox, 16);
@@ -294,31 +302,42 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
                              (first && j == 0 && k == 0) ? 0u : 1u);
         }
       };
-      bool ok = mbar_wait_warp(kv_full, 0, ab);
-      tc_fence_after();
-      for (int it = 0; ok && it < n_it; ++it) {
+      // The scores of step it over the other half's boxes (their loads
+      // started earliest), then over this half's, which are loaded once the
+      // previous step's dV and dK are done.
+      auto scores_other = [&](int it) -> bool {
         const uint32_t par = static_cast<uint32_t>(it) & 1u;
-        // scores of step it: the other half's boxes first (their loads started
-        // earliest), then this half's
-        ok = mbar_wait_warp(full + kQo, par, ab);
-        if (!ok) break;
+        if (!mbar_wait_warp(full + kQo, par, ab)) return false;
         tc_fence_after();
-        scores(false, false, true);
-        ok = mbar_wait_warp(full + kDo, par, ab);
-        if (!ok) break;
+        scores(it, false, false, true);
+        if (!mbar_wait_warp(full + kDo, par, ab)) return false;
         tc_fence_after();
-        scores(true, false, true);
+        scores(it, true, false, true);
         mma_commit_warp(empty + kQo);
         mma_commit_warp(empty + kDo);
-        ok = mbar_wait_warp(full + kQh, par, ab);
-        if (!ok) break;
+        return true;
+      };
+      auto scores_own = [&](int it) -> bool {
+        const uint32_t par = static_cast<uint32_t>(it) & 1u;
+        if (!mbar_wait_warp(full + kQh, par, ab)) return false;
         tc_fence_after();
-        scores(false, true, false);
-        ok = mbar_wait_warp(full + kDh, par, ab);
-        if (!ok) break;
+        scores(it, false, true, false);
+        if (!mbar_wait_warp(full + kDh, par, ab)) return false;
         tc_fence_after();
-        scores(true, true, false);
+        scores(it, true, true, false);
         mma_commit_warp(s_full);
+        return true;
+      };
+      bool ok = mbar_wait_warp(kv_full, 0, ab);
+      tc_fence_after();
+      ok = ok && scores_other(0) && scores_own(0);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const uint32_t par = static_cast<uint32_t>(it) & 1u;
+        // the next step's scores over the other half's boxes go into the
+        // other score buffer while the softmax works on this step's (that
+        // buffer's last reader, the softmax of step it - 1, is done: its
+        // P was waited for before step it - 1's products)
+        if (it + 1 < n_it && !(ok = scores_other(it + 1))) break;
         // P^T and dS^T of step it are in shared memory
         ok = mbar_wait_warp(p_full, par, ab);
         if (!ok) break;
@@ -362,6 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
           }
         }
         mma_commit_warp(dq_full + b);
+        // this half's scores of the next step; its commit of s_full covers
+        // this step's products, so the softmax may then overwrite P and dS
+        if (it + 1 < n_it && !(ok = scores_own(it + 1))) break;
       }
       if (ok) mma_commit_warp(acc_full);
       mma_commit_warp(drain);
@@ -470,18 +492,26 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int it = 0; it < n_it; ++it) {
       const int b = it & 1;
-      const bool ok = mbar_wait_warp(vec_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab) &&
-                      mbar_wait_warp(s_full, static_cast<uint32_t>(it) & 1u, ab);
-      if (!ok) break;
+      // the step's -lse2 and -D into registers while the scores still run
+      const int vs = it % kVecSlots;
+      if (!mbar_wait_warp(vec_full + vs, static_cast<uint32_t>(it / kVecSlots) & 1u, ab)) break;
+      const uint32_t vec = smem_base + kVecOff + vs * kVecBytes + qh * 16 * 4;
+      float4 nlv[4], ndv[4];
+#pragma unroll
+      for (int e4 = 0; e4 < 4; ++e4) {
+        nlv[e4] = lds_f4(vec + e4 * 16);
+        ndv[e4] = lds_f4(vec + kBN * 4 + e4 * 16);
+      }
+      if (!mbar_wait_warp(s_full, static_cast<uint32_t>(it) & 1u, ab)) break;
       tc_fence_after();
       const int q0 = (i_lo + it) * kBN + qh * 16;
-      const uint32_t vec = smem_base + kVecOff + b * kVecBytes + qh * 16 * 4;
       // this key sees all 16 queries: no per-element mask
       const bool all = !active || (key < kv_len && (!causal || key <= q0) &&
                                    key >= q0 + 15 - p.win_left && key <= q0 + p.win_right);
       uint32_t sv[16], dp[16];
-      tmem_ld16(lane_base + kColS + qh * 16, sv);
-      tmem_ld16(lane_base + kColDP + qh * 16, dp);
+      const uint32_t sbuf = static_cast<uint32_t>(b * 64);   // this step's score buffer
+      tmem_ld16(lane_base + kColS + sbuf + qh * 16, sv);
+      tmem_ld16(lane_base + kColDP + sbuf + qh * 16, dp);
       tmem_ld_wait();
       reg_fence(sv);
       reg_fence(dp);
@@ -490,8 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
       auto rows = [&](auto masked) {
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4) {
-          const float4 nl = lds_f4(vec + e4 * 16);
-          const float4 nd = lds_f4(vec + kBN * 4 + e4 * 16);
+          const float4 nl = nlv[e4];
+          const float4 nd = ndv[e4];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = e4 * 4 + u * 2;
