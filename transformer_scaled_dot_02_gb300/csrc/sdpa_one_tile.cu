@@ -7,12 +7,10 @@
 //     fp32 O does not fit the two-tile plan in 512 tensor-memory columns:
 //       d = 256: key tiles of 64; one CTA per query tile.
 //       d = 512: key tiles of 64; two CTAs per query tile, one per half of
-//                d_v, each recomputing the scores (Q, 128 KB, stays in
-//                shared memory).  K and V have one stage each; K comes
-//                in two halves, and the next tile's first half loads
-//                while the scores run over the second.  The scores of the
-//                next tile are issued in two parts around O += P V, so
-//                that product never waits for a K load.
+//                d_v, each recomputing the scores.  Q (128 KB) lands in
+//                shared memory; once the softmax warps have copied its
+//                first half into tensor memory, that 64 KB holds the
+//                second stage of K.  V has one stage.
 //   - d = 64 and 128 where the key walk is short: key tiles of 64, 256
 //     tensor-memory columns, two CTAs per SM, so short sequences get twice
 //     the CTAs in flight and half the serial chain per CTA.  At d = 64 the
@@ -55,11 +53,12 @@ template <int DK, int KT>
 struct OCfg {
   static constexpr int BN = KT;                             // keys per tile
   static_assert(KT == 32 || (KT == 64 && DK >= 64), "key tile");
-  // d = 512: one K stage and one V stage (Q alone takes 128 KB), K loaded
-  // and released in two halves so that the next tile's first half lands
-  // while the scores still run over the second.
-  static constexpr bool kOneStage = DK == 512;
-  static constexpr int kStages = kOneStage ? 1 : 2;
+  // K has two stages.  At d = 512 (Q alone takes 128 KB) the second lies over
+  // the first half of Q, free once the softmax warps have copied it into
+  // tensor memory, and V has one stage.
+  static constexpr bool kKInQ = DK == 512;
+  static constexpr int kKRegionStages = kKInQ ? 1 : 2;     // K stages after Q
+  static constexpr int kVStages = kKInQ ? 1 : 2;
   static constexpr int kDvc = DK < 256 ? DK : 256;          // O columns per CTA
   static constexpr int kChunks = DK / kDvc;                 // CTAs per query tile
   // Tiles move as boxes of kBoxCols columns, rows of kRowBytes swizzled at
@@ -78,11 +77,11 @@ struct OCfg {
   static constexpr int kVBytes = (kDvc / kBoxCols) * kKVBox;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
-  static constexpr int kVOff = kKOff + kStages * kKBytes;
-  static constexpr int kBarOff = kVOff + kStages * kVBytes;
+  static constexpr int kVOff = kKOff + kKRegionStages * kKBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kVBytes;
   // q_full, k_full[2], v_full[2], s_full[2], p_full[2], o_full[2], o_last, drain,
-  // kh_free, q_tmem
-  static constexpr int kNumBars = 1 + 10 + 4;
+  // q_tmem
+  static constexpr int kNumBars = 1 + 10 + 3;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
@@ -100,6 +99,8 @@ struct OCfg {
   static constexpr int kQTmemSteps = DK >= 256 ? 16 : 0;
   static constexpr uint32_t kQCol = kOCol + kDvc;
   static_assert(kQCol + kQTmemSteps * 8 <= kTmemCols, "Q in tensor memory");
+  // the second K stage fits in the part of Q that tensor memory holds
+  static_assert(!kKInQ || kQTmemSteps * 16 / kBoxCols * kQBox >= kKBytes, "K stage over Q");
   static_assert(kQTmemSteps == 0 || (kRowBytes == 128 && (kQTmemSteps * 16) % kBoxCols == 0),
                 "Q copied by whole 128-byte-swizzled boxes");
   static_assert(kSmemBytes * kMinBlocks <= 232448 - 1024 * kMinBlocks, "CTAs per SM");
@@ -138,8 +139,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
   uint64_t* o_full = p_full + 2;   // o_full[u & 1]: one phase per O += P(u) V_u
   uint64_t* o_last = o_full + 2;   // once, after the last O += P V
   uint64_t* drain = o_last + 1;
-  uint64_t* kh_free = drain + 1;   // one stage: the first half of S(u) is done
-  uint64_t* q_tmem = kh_free + 1;  // the softmax warps copied Q into tensor memory
+  uint64_t* q_tmem = drain + 1;    // the softmax warps copied Q into tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_tmem + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const AbortState ab{abort_flag, p.status};
@@ -183,7 +183,6 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
     }
     mbar_init(o_last, 1);
     mbar_init(drain, 1);
-    mbar_init(kh_free, 1);
     mbar_init(q_tmem, kBlockM);
     *abort_flag = 0;
     fence_mbar_init();
@@ -233,41 +232,52 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
       for (int c = 0; c < DK / C::kBoxCols; ++c)
         tma_load_4d(&p.tm_q, q_full, smem + C::kQOff + c * C::kQBox, c * C::kBoxCols, qs, hi, bi);
       int k_issued = 0, v_issued = 0;
-      if constexpr (C::kOneStage) {
-        // k_full[h]: half h of the K tile (one phase per tile); v_full[0]: V.
-        constexpr int kHalfBoxes = DK / C::kBoxCols / 2;
-        int k0_issued = 0;
-        for (int u = 0; u < n_kv; ++u) {
-          const int j0 = key_base + u * BN;   // first key of the tile
-          const uint32_t prev = static_cast<uint32_t>(u - 1);
-          // S(u-1)'s first half read this half last; kh_free cannot be a
-          // phase ahead of it, since S(u) needs the half loaded here.
-          if (u >= 1 && !mbar_wait(kh_free, prev & 1u, ab)) break;
-          mbar_arrive_expect_tx(k_full, C::kKBytes / 2);
-          for (int c = 0; c < kHalfBoxes; ++c)
-            tma_load_4d(&p.tm_k, k_full, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols, j0,
-                        hi, bi);
-          k0_issued = u + 1;
-          // all of S(u-1) read the second half (s_full of its buffer)
-          if (u >= 1 && !mbar_wait(s_full + (prev & 1u), (prev >> 1) & 1u, ab)) break;
-          mbar_arrive_expect_tx(k_full + 1, C::kKBytes / 2);
-          for (int c = kHalfBoxes; c < 2 * kHalfBoxes; ++c)
-            tma_load_4d(&p.tm_k, k_full + 1, smem + C::kKOff + c * C::kKVBox, c * C::kBoxCols,
-                        j0, hi, bi);
-          k_issued = u + 1;
-          // O += P(u-1) V(u-1) read V last (o_full of its parity)
-          if (u >= 1 && !mbar_wait(o_full + (prev & 1u), (prev >> 1) & 1u, ab)) break;
+      // K stage of tile u (u & 1), and where it lies
+      auto k_stage = [&](int u) -> uint8_t* {
+        return (u & 1) ? (C::kKInQ ? smem + C::kQOff : smem + C::kKOff + C::kKBytes)
+                       : smem + C::kKOff;
+      };
+      auto load_k = [&](int u) {
+        uint8_t* dst = k_stage(u);
+        mbar_arrive_expect_tx(k_full + (u & 1), C::kKBytes);
+        for (int c = 0; c < DK / C::kBoxCols; ++c)
+          tma_load_4d(&p.tm_k, k_full + (u & 1), dst + c * C::kKVBox, c * C::kBoxCols,
+                      key_base + u * BN, hi, bi);
+      };
+      if constexpr (C::kKInQ) {
+        // K_{u+1} goes ahead of V_u: it needs only the scores of tile u - 1
+        // to be done with its stage, V_u the product of tile u - 1 with V.
+        bool go = true;
+        load_k(0);
+        k_issued = 1;
+        for (int u = 0; go && u < n_kv; ++u) {
+          const int nk = u + 1;
+          if (nk < n_kv) {
+            // stage 1's first use: the softmax warps have copied Q's first
+            // half into tensor memory; later uses: S(nk - 2) is done
+            const bool free_ok = nk == 1 ? mbar_wait(q_tmem, 0, ab)
+                                         : mbar_wait(s_full + (nk & 1),
+                                                     static_cast<uint32_t>((nk >> 1) - 1) & 1u, ab);
+            if (!free_ok) break;
+            load_k(nk);
+            k_issued = nk + 1;
+          }
+          // the one V stage: O += P(u-1) V_{u-1} is done with it
+          if (u >= 1 && !mbar_wait(o_full + ((u - 1) & 1), static_cast<uint32_t>((u - 1) >> 1) & 1u, ab)) {
+            go = false;
+            break;
+          }
           mbar_arrive_expect_tx(v_full, C::kVBytes);
           for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
             tma_load_4d(&p.tm_v, v_full, smem + C::kVOff + c * C::kKVBox,
-                        chunk * C::kDvc + c * C::kBoxCols, j0, hi, bi);
+                        chunk * C::kDvc + c * C::kBoxCols, key_base + u * BN, hi, bi);
           v_issued = u + 1;
         }
         mbar_wait_drain(q_full, 0);
         // each load was issued only after the previous one into the same
         // place had been consumed, so only the last of each can be in flight
-        if (k0_issued > 0) mbar_wait_drain(k_full, static_cast<uint32_t>(k0_issued - 1) & 1u);
-        if (k_issued > 0) mbar_wait_drain(k_full + 1, static_cast<uint32_t>(k_issued - 1) & 1u);
+        for (int u = max(0, k_issued - 2); u < k_issued; ++u)
+          mbar_wait_drain(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
         if (v_issued > 0) mbar_wait_drain(v_full, static_cast<uint32_t>(v_issued - 1) & 1u);
       } else {
         for (int u = 0; u < n_kv; ++u) {
@@ -306,22 +316,18 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
       constexpr uint32_t kDescHi = C::kDescHi;
       auto lo = [](uint32_t addr, uint32_t lbo) { return (addr >> 4) | ((lbo >> 4) << 16); };
       const uint32_t q_lo = lo(smem_base + C::kQOff, 16);
-      // S(u) = Q K_u^T into score buffer u & 1, part `part` of `parts`: waits
-      // for that part of K_u, issues its k steps, and commits kh_free after a
-      // first half or s_full after the last part.  One stage: K_u comes in
-      // two halves; two stages: in one piece.
-      auto issue_s = [&](int u, int part, int parts) -> bool {
+      // S(u) = Q K_u^T into score buffer u & 1: waits for K_u in its stage
+      // (u & 1; at d = 512 stage 1 lies over the first half of Q), issues the
+      // k steps, and commits s_full.
+      auto issue_s = [&](int u) -> bool {
         const uint32_t d = tmem + static_cast<uint32_t>((u & 1) * BN);
-        const int stage = C::kOneStage ? 0 : (u & 1);
-        const uint32_t b0 = lo(smem_base + C::kKOff + stage * C::kKBytes, 16);
-        const uint32_t ph = static_cast<uint32_t>(C::kOneStage ? u : (u >> 1)) & 1u;
-        if (!mbar_wait_warp(k_full + (C::kOneStage ? part : (u & 1)), ph, ab)) return false;
+        const uint32_t k_base = (u & 1) ? (C::kKInQ ? C::kQOff : C::kKOff + C::kKBytes) : C::kKOff;
+        const uint32_t b0 = lo(smem_base + k_base, 16);
+        if (!mbar_wait_warp(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab)) return false;
         tc_fence_after();
         constexpr int kSteps = DK / 16;
-        const int k_begin = part * (kSteps / parts);
 #pragma unroll
         for (int k = 0; k < kSteps; ++k) {
-          if (k < k_begin || k >= k_begin + kSteps / parts) continue;
           constexpr int kS = C::kStepsPerRow;
           const uint32_t bk = b0 + static_cast<uint32_t>(((k / kS) * C::kKVBox + (k % kS) * 32) >> 4);
           if (k < C::kQTmemSteps)
@@ -330,10 +336,6 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           else
             mma_bf16_ss_warp(d, q_lo + static_cast<uint32_t>(((k / kS) * C::kQBox + (k % kS) * 32) >> 4),
                              kDescHi, bk, kDescHi, C::kIdescS, k > 0 ? 1u : 0u);
-        }
-        if (part + 1 < parts) {
-          mma_commit_warp(kh_free);
-          return true;
         }
 #ifdef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
         // (test builds only, never in libsdpa.so: the first score tile is
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
       };
       auto issue_pv = [&](int u) {
         const uint32_t pa = tmem + static_cast<uint32_t>((u & 1) * BN);
-        const int stage = C::kOneStage ? 0 : (u & 1);
+        const int stage = C::kVStages == 1 ? 0 : (u & 1);
         const uint32_t b0 = lo(smem_base + C::kVOff + stage * C::kVBytes, C::kKVBox);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
@@ -356,20 +358,16 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
                            (u > 0 || k > 0) ? 1u : 0u);
         }
       };
-      constexpr int kParts = C::kOneStage ? 2 : 1;
       bool ok = mbar_wait_warp(q_full, 0, ab);
       if (C::kQTmemSteps > 0 && ok) ok = mbar_wait_warp(q_tmem, 0, ab);
       tc_fence_after();
-      for (int part = 0; ok && part < kParts; ++part) ok = issue_s(0, part, kParts);
+      ok = ok && issue_s(0);
       for (int u = 0; ok && u < n_kv; ++u) {
         // S(u+1) into the buffer of P(u-1): PV(u-1) was issued before it.
-        // One stage: only its first half goes ahead of O += P(u) V_u; the
-        // second half waits for K data that is loaded once S(u) is done, and
-        // O += P(u) V_u should not queue behind that load.
         const bool next = u + 1 < n_kv;
-        if (next && !(ok = issue_s(u + 1, 0, kParts))) break;
-        const uint32_t vs = C::kOneStage ? 0u : static_cast<uint32_t>(u & 1);
-        const uint32_t vph = static_cast<uint32_t>(C::kOneStage ? u : (u >> 1)) & 1u;
+        if (next && !(ok = issue_s(u + 1))) break;
+        const uint32_t vs = C::kVStages == 1 ? 0u : static_cast<uint32_t>(u & 1);
+        const uint32_t vph = static_cast<uint32_t>(C::kVStages == 1 ? u : (u >> 1)) & 1u;
         ok = mbar_wait_warp(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
              mbar_wait_warp(v_full + vs, vph, ab);
         if (!ok) break;
@@ -377,7 +375,6 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
         issue_pv(u);
         mma_commit_warp(o_full + (u & 1));
         if (u + 1 == n_kv) mma_commit_warp(o_last);
-        if (kParts == 2 && next && !(ok = issue_s(u + 1, 1, kParts))) break;
       }
       mma_commit_warp(drain);
       mbar_wait_drain(drain, 0);
