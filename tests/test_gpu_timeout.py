@@ -31,7 +31,8 @@ def faulty_lib():
     sd_build.build()
     d = tempfile.mkdtemp(prefix="sdpa_timeout_")
     nvcc = sd_build._nvcc()
-    hooked = ["sdpa_tc.cu", "sdpa_one_tile.cu", "sdpa_bwd.cu"]   # every attention kernel carries the hook
+    # every attention kernel carries the hook
+    hooked = ["sdpa_tc.cu", "sdpa_one_tile.cu", "sdpa_bwd.cu", "sdpa_bwd_wide.cu"]
     objs = []
     for src in hooked:
         obj = os.path.join(d, src.replace(".cu", "_withhold.o"))
@@ -77,11 +78,15 @@ def test_bounded_wait_times_out_and_reports(faulty_lib, kernel, d, pin_kernels):
     assert parity_err(got, oracle.sdpa(q, k, v, sd.SDPA_MASK_CAUSAL)) <= TOL_BF16
 
 
-def test_backward_bounded_wait_times_out_and_reports(faulty_lib):
+@pytest.mark.parametrize("d", [64, 512])
+def test_backward_bounded_wait_times_out_and_reports(faulty_lib, d):
+    """d = 64: one key tile, one CTA; d = 512: one 64-key tile, two CTAs
+    (one per half of d)."""
     import ctypes
     import torch
     rng = np.random.default_rng(2)
-    b, h, n, d = 1, 1, 128, 64   # one key tile: one CTA of the backward
+    b, h = 1, 1
+    n = 128 if d <= 256 else 64
     q, k, v, do = (synthetic.round_to_bf16(rng.standard_normal((b, h, n, d)).astype(np.float32))
                    for _ in range(4))
     qd, kd, vd, dod = dev(q), dev(k), dev(v), dev(do)

@@ -325,6 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
         if (!mbar_wait_warp(full + kDh, par, ab)) return false;
         tc_fence_after();
         scores(it, true, true, false);
+#ifdef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
+        // (test builds only, never in libsdpa.so: the first score tile is
+        // never signalled, so the compute warps' bounded wait runs out and
+        // every other role leaves through the abort flag or its own limit)
+        if (it == 0) return true;
+#endif
         mma_commit_warp(s_full);
         return true;
       };
