@@ -350,22 +350,26 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
         tc_fence_after();
         const uint32_t bp = desc_lo(smem_base + kPOff, 16);
         const uint32_t bds = desc_lo(smem_base + kDsOff, 16);
+        // dK first: its commit frees this half's Q part, the first of the
+        // next step's own parts that the producer refills, while dV and dQ^T
+        // run; dV's commit then frees the dO part
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb) {
-          // 128 columns of d: boxes 2 mb, 2 mb + 1 of the own parts, 4 KB apart
-          const uint32_t ado = desc_lo(smem_base + kDohOff + 2 * mb * kQBox, kQBox);
-          const uint32_t aq = desc_lo(smem_base + kQhOff + 2 * mb * kQBox, kQBox);
+        for (int g = 0; g < 2; ++g) {
+          const bool dv = g == 1;
 #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k) {
-            const uint32_t ka = static_cast<uint32_t>(k * 16 * 128) >> 4;   // 16 query rows
-            const uint32_t kb = static_cast<uint32_t>(k * 32) >> 4;         // 16 queries of a row
-            const uint32_t acc = (it > 0 || k > 0) ? 1u : 0u;
-            mma_bf16_ss_warp(tmem + kColDV + mb * 64, ado + ka, kDescHi, bp + kb, kDescHi, kIdescG, acc);
-            mma_bf16_ss_warp(tmem + kColDK + mb * 64, aq + ka, kDescHi, bds + kb, kDescHi, kIdescG, acc);
+          for (int mb = 0; mb < 2; ++mb) {
+            // 128 columns of d: boxes 2 mb, 2 mb + 1 of the own part, 4 KB apart
+            const uint32_t a = desc_lo(smem_base + (dv ? kDohOff : kQhOff) + 2 * mb * kQBox, kQBox);
+#pragma unroll
+            for (int k = 0; k < kBN / 16; ++k) {
+              const uint32_t ka = static_cast<uint32_t>(k * 16 * 128) >> 4;   // 16 query rows
+              const uint32_t kb = static_cast<uint32_t>(k * 32) >> 4;         // 16 queries of a row
+              mma_bf16_ss_warp(tmem + (dv ? kColDV : kColDK) + mb * 64, a + ka, kDescHi,
+                               (dv ? bp : bds) + kb, kDescHi, kIdescG, (it > 0 || k > 0) ? 1u : 0u);
+            }
           }
+          mma_commit_warp(empty + (dv ? kDh : kQh));
         }
-        mma_commit_warp(empty + kQh);
-        mma_commit_warp(empty + kDh);
         // dQ^T(it) = K[:, half]^T dS^T(it) into buffer it & 1, once the
         // epilogue has read what step it - 2 left there
         const int b = it & 1;
