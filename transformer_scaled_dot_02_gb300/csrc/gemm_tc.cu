@@ -46,12 +46,6 @@ struct GCfg {
   static_assert((BN / 64) * kCBoxBytes <= kBarOff, "the epilogue stages Y over the ring");
 };
 
-template <int N>
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
-}
-
 template <int BN>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     gemm_bf16_tc(const __grid_constant__ GemmParams p) {

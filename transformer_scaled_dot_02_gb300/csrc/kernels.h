@@ -132,6 +132,22 @@ int bwd_key_tile(int d_k);
 int bwd_query_step(int d_k);
 // The main kernel for 512-wide heads (after the prep kernel when `after_prep`).
 cudaError_t launch_sdpa_bwd_w512(const SdpaBwdParams& bp, bool after_prep, cudaStream_t stream);
+#ifdef __CUDACC__
+// The steps [lo, hi) of Step queries that hold a query able to see one of the
+// Keys keys from key0 (below kv_len), under the causal mask and the window.
+template <int Keys, int Step>
+__device__ __forceinline__ int2 bwd_query_steps(const SdpaBwdParams& p, int key0, int kv_len) {
+  const int key_hi = min(key0 + Keys, kv_len) - 1;
+  if (key_hi < key0) return make_int2(0, 0);
+  long long q_lo = static_cast<long long>(key0) - p.win_right;
+  if (p.mask_kind & 1) q_lo = q_lo > key0 ? q_lo : key0;
+  if (q_lo < 0) q_lo = 0;
+  long long q_hi = static_cast<long long>(key_hi) + p.win_left + 1;
+  if (q_hi > p.n_q) q_hi = p.n_q;
+  if (q_hi <= q_lo) return make_int2(0, 0);
+  return make_int2(static_cast<int>(q_lo / Step), static_cast<int>((q_hi + Step - 1) / Step));
+}
+#endif
 
 // Exact fp32 attention on the CUDA cores, BHSD contiguous.
 struct SdpaF32Params {

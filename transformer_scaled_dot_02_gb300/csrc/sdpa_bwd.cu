@@ -29,21 +29,6 @@
 namespace sdpa {
 namespace {
 
-template <int N>
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ------------------------------------------------------------------------
 // 64-query steps with S^T / dP^T double-buffered in tensor memory, so the
 // tensor core computes the next step's products while the compute warps turn
@@ -159,43 +144,6 @@ struct Cfg {
   static_assert((128 / LK::kBoxCols) * LK::kKVBox <= kBarOff, "dQ^T reads in bounds");
 };
 
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
-__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[8]) { tmem_ld8(taddr, r); }
-
-// Adds a [64][32] fp32 box from shared memory into the tensor at (x, y, z).
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
-                                                  int y, int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          map),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Query steps [i_lo, i_hi) of 64 holding a query that can see a key of this tile.
-__device__ __forceinline__ int2 query_steps(const SdpaBwdParams& p, int key0, int kv_len) {
-  const int key_hi = min(key0 + kBM, kv_len) - 1;
-  if (key_hi < key0) return make_int2(0, 0);
-  long long q_lo = static_cast<long long>(key0) - p.win_right;
-  if (p.mask_kind & 1) q_lo = q_lo > key0 ? q_lo : key0;
-  if (q_lo < 0) q_lo = 0;
-  long long q_hi = static_cast<long long>(key_hi) + p.win_left + 1;
-  if (q_hi > p.n_q) q_hi = p.n_q;
-  if (q_hi <= q_lo) return make_int2(0, 0);
-  return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
-}
-
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_constant__ SdpaBwdParams p) {
   using C = Cfg<DK, DV>;
@@ -255,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
     kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
   }
   const int key0 = jt * kBM;
-  const int2 qr = query_steps(p, key0, kv_len);
+  const int2 qr = bwd_query_steps<kBM, kBN>(p, key0, kv_len);
   const int i_lo = qr.x, n_it = qr.y - qr.x;
 
   if (threadIdx.x == 0) {
@@ -804,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
           for (int c = 0; c < kHalf / N; ++c) {
             uint32_t a[N];
             if (have) {
-              tmem_ld_n(lane_base + tcol + half * kHalf + c * N, a);
+              tmem_ld_chunk(lane_base + tcol + half * kHalf + c * N, a);
               tmem_ld_wait();
               reg_fence(a);
             } else {

@@ -94,51 +94,6 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
   return (addr >> 4) | ((lbo >> 4) << 16);
 }
 
-__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
-                                                  int y, int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          map),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-template <int N>
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
-#pragma unroll
-  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-// Query steps [lo, hi) of 32 holding a query that can see a key of this tile.
-__device__ __forceinline__ int2 query_steps(const SdpaBwdParams& p, int key0, int kv_len) {
-  const int key_hi = min(key0 + kKeys, kv_len) - 1;
-  if (key_hi < key0) return make_int2(0, 0);
-  long long q_lo = static_cast<long long>(key0) - p.win_right;
-  if (p.mask_kind & 1) q_lo = q_lo > key0 ? q_lo : key0;
-  if (q_lo < 0) q_lo = 0;
-  long long q_hi = static_cast<long long>(key_hi) + p.win_left + 1;
-  if (q_hi > p.n_q) q_hi = p.n_q;
-  if (q_hi <= q_lo) return make_int2(0, 0);
-  return make_int2(static_cast<int>(q_lo / kBN), static_cast<int>((q_hi + kBN - 1) / kBN));
-}
-
 // Column box of part box j: this half's boxes (own) or the other half's.
 __device__ __forceinline__ int part_box(int half, bool own, int j) {
   return (own ? half : 1 - half) * kHalfBoxes + j;
@@ -199,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_w512(const __grid_con
     kv_len = kv_len < 0 ? 0 : (kv_len > p.n_k ? p.n_k : kv_len);
   }
   const int key0 = jt * kKeys;
-  const int2 qr = query_steps(p, key0, kv_len);
+  const int2 qr = bwd_query_steps<kKeys, kBN>(p, key0, kv_len);
   const int i_lo = qr.x, n_it = qr.y - qr.x;
 
   if (threadIdx.x == 0) {
