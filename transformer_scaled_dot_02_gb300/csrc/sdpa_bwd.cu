@@ -65,8 +65,8 @@ constexpr int kDsTile = kBM * kBN * 2;   // dS^T: 128 keys x 64 queries bf16 (12
 constexpr int kVecBytes = 2 * kBN * 4;   // -lse2 and -D of one step
 // kv_full, q_full[3], q_empty[3], s_full[2], p_full[2], dq_full[2],
 // dq_empty[2], acc_full, drain, then (wide heads) part_full[4],
-// part_empty[4], vec_full[2]
-constexpr int kNumBars = 1 + 2 * kStages + 8 + 2 + 10;
+// part_empty[4], vec_full[3]
+constexpr int kNumBars = 1 + 2 * kStages + 8 + 2 + 11;
 constexpr uint32_t kIdescS = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
 // dQ^T = K^T dS^T always with M = 128 lanes of d: for d_k < 128 the upper lanes
 // read the tiles that follow K in shared memory and are discarded.
@@ -130,7 +130,8 @@ struct Cfg {
   static constexpr int kDsOff = kStageOff + kStagesQ * kStageBytes;   // dS^T buffers
   static constexpr int kStagingOff = kDsOff + kDsBufs * kDsTile;  // 4 warps x [kDqRows][kDCols] fp32
   static constexpr int kVecOff = kStagingOff + 4 * kDqRows * kDCols * 4;
-  static constexpr int kVecBufs = kWide ? 2 : kStagesQ;       // -lse2 / -D slots
+  static constexpr int kVecBufs = kWide ? 3 : kStagesQ;       // -lse2 / -D slots
+  static_assert(!kWide || kVecBufs == 3, "three vec_full barriers");
   static constexpr int kBarOff = kVecOff + kVecBufs * kVecBytes;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kIdescDV = idesc_bf16(kBM, kColsV, false, true);  // dV (A in TMEM)
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
   uint64_t* part_full = drain + 1;
   uint64_t* part_empty = part_full + 4;
   uint64_t* vec_full = part_empty + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vec_full + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const AbortState ab{abort_flag, p.status};
 
@@ -224,8 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       mbar_init(part_full + s, 1);
       mbar_init(part_empty + s, 1);
     }
-    mbar_init(vec_full, 1);
-    mbar_init(vec_full + 1, 1);
+    for (int s = 0; s < 3; ++s) mbar_init(vec_full + s, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -252,10 +252,11 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         tma_load_4d(&p.tm_v, kv_full, smem + C::kVOff + c * LV::kKVBox, c * LV::kBoxCols, key0, hi, bi);
       if constexpr (C::kWide) {
         // four parts of two boxes each, in the order the MMA warp frees them:
-        // Q other, dO other (after the step's scores), Q own, dO own (after
-        // dV and dK); the step's vectors go with the first part, into one of
-        // two slots (the slot's last reader, step it - 2, finished before
-        // the scores of step it - 1 were issued)
+        // Q other, dO other (after the step's scores over them), Q own (after
+        // dK), dO own (after dV); the step's vectors go with the first part,
+        // into one of three slots (the slot's last reader, the softmax of
+        // step it - 3, finished before the scores of step it - 1 over the
+        // other chunk were issued, and those freed this part)
         int issued[4] = {0, 0, 0, 0};
         int vec_issued = 0;
         bool go = true;
@@ -282,9 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
             }
             issued[pt] = it + 1;
             if (pt == 0) {
-              uint64_t* vb = vec_full + (it & 1);
+              uint64_t* vb = vec_full + it % C::kVecBufs;
               const long long vrow = static_cast<long long>(bh) * p.n_q_pad + q0;
-              uint8_t* vec = smem + C::kVecOff + (it & 1) * kVecBytes;
+              uint8_t* vec = smem + C::kVecOff + (it % C::kVecBufs) * kVecBytes;
               mbar_arrive_expect_tx(vb, kVecBytes);
               tma_load_1d(vec, p.neg_lse2 + vrow, kBN * 4, vb);
               tma_load_1d(vec + kBN * 4, p.neg_dvec + vrow, kBN * 4, vb);
@@ -297,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         for (int pt = 0; pt < 4; ++pt)
           if (issued[pt] > 0)
             mbar_wait_drain(part_full + pt, static_cast<uint32_t>(issued[pt] - 1) & 1u);
-        for (int it = max(0, vec_issued - 2); it < vec_issued; ++it)
-          mbar_wait_drain(vec_full + (it & 1), static_cast<uint32_t>(it >> 1) & 1u);
+        for (int it = max(0, vec_issued - C::kVecBufs); it < vec_issued; ++it)
+          mbar_wait_drain(vec_full + it % C::kVecBufs, static_cast<uint32_t>(it / C::kVecBufs) & 1u);
       } else {
       int issued = 0;
       for (int it = 0; it < n_it; ++it) {
@@ -356,30 +357,31 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
           product(LK{}, k_smem, st, DK);
       };
       // Wide heads: S^T(it) and dP^T(it) part by part as the stage's parts
-      // land, the other chunk's boxes first; frees those two parts, then
-      // commits s_full once this chunk's boxes are in.  dP^T(it) lands where
-      // dQ^T(it - 2) was, so it waits for that step's epilogue.
-      auto wide_scores = [&](int it) -> bool {
-        const uint32_t par = static_cast<uint32_t>(it) & 1u;
+      // land.  wide_scores_other issues them over the other chunk's boxes and
+      // frees those two parts; wide_scores_own adds this chunk's boxes and
+      // commits s_full.  dP^T(it) lands where dQ^T(it - 2) was, so it waits
+      // for that step's epilogue.
+      auto wide_part = [&](int it, bool dp, bool own, bool first) {
         const uint32_t st = smem_base + C::kStageOff;
-        auto part = [&](bool dp, bool own, bool first) {
-          const int c0 = 2 * (own ? chunk : 1 - chunk);
-          const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
+        const int c0 = 2 * (own ? chunk : 1 - chunk);
+        const uint32_t d = tmem + static_cast<uint32_t>((it & 1) * 128 + (dp ? 64 : 0));
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int c = c0 + j;
-            const uint32_t a0 = lo((dp ? v_smem : k_smem) + c * LK::kKVBox, 16);
-            const uint32_t b0 = lo(st + (dp ? LK::kQTile : 0) + c * LK::kQBox, 16);
+        for (int j = 0; j < 2; ++j) {
+          const int c = c0 + j;
+          const uint32_t a0 = lo((dp ? v_smem : k_smem) + c * LK::kKVBox, 16);
+          const uint32_t b0 = lo(st + (dp ? LK::kQTile : 0) + c * LK::kQBox, 16);
 #pragma unroll
-            for (int kk = 0; kk < LK::kStepsPerRow; ++kk)
-              mma_bf16_ss_warp(d, a0 + static_cast<uint32_t>(kk * 2), LK::kDescHi,
-                               b0 + static_cast<uint32_t>(kk * 2), LK::kDescHi, kIdescS,
-                               (first && j == 0 && kk == 0) ? 0u : 1u);
-          }
-        };
+          for (int kk = 0; kk < LK::kStepsPerRow; ++kk)
+            mma_bf16_ss_warp(d, a0 + static_cast<uint32_t>(kk * 2), LK::kDescHi,
+                             b0 + static_cast<uint32_t>(kk * 2), LK::kDescHi, kIdescS,
+                             (first && j == 0 && kk == 0) ? 0u : 1u);
+        }
+      };
+      auto wide_scores_other = [&](int it) -> bool {
+        const uint32_t par = static_cast<uint32_t>(it) & 1u;
         if (!mbar_wait_warp(part_full + 0, par, ab)) return false;
         tc_fence_after();
-        part(false, false, true);
+        wide_part(it, false, false, true);
         if (it >= 2) {
           if (!mbar_wait_warp(dq_empty + (it & 1), static_cast<uint32_t>((it - 2) >> 1) & 1u, ab))
             return false;
@@ -387,15 +389,19 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         }
         if (!mbar_wait_warp(part_full + 1, par, ab)) return false;
         tc_fence_after();
-        part(true, false, true);
+        wide_part(it, true, false, true);
         mma_commit_warp(part_empty + 0);
         mma_commit_warp(part_empty + 1);
+        return true;
+      };
+      auto wide_scores_own = [&](int it) -> bool {
+        const uint32_t par = static_cast<uint32_t>(it) & 1u;
         if (!mbar_wait_warp(part_full + 2, par, ab)) return false;
         tc_fence_after();
-        part(false, true, false);
+        wide_part(it, false, true, false);
         if (!mbar_wait_warp(part_full + 3, par, ab)) return false;
         tc_fence_after();
-        part(true, true, false);
+        wide_part(it, true, true, false);
 #ifdef SDPA_TEST_WITHHOLD_FIRST_S_COMMIT
         if (it == 0) return true;
 #endif
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       bool ok = mbar_wait_warp(kv_full, 0, ab);
       if constexpr (C::kWide) {
         tc_fence_after();
-        if (ok) ok = wide_scores(0);
+        ok = ok && wide_scores_other(0) && wide_scores_own(0);
       } else {
         ok = ok && mbar_wait_warp(q_full, 0, ab);
         tc_fence_after();
@@ -426,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
         const uint32_t col_boxes = static_cast<uint32_t>(chunk * (128 / LK::kBoxCols));
         for (int it = 0; ok && it < n_it; ++it) {
           const int b = it & 1;
+          // the next step's scores over the other chunk's boxes go into the
+          // other buffer while the compute warps work on this step's
+          if (it + 1 < n_it && !(ok = wide_scores_other(it + 1))) break;
           ok = mbar_wait_warp(p_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);
           if (!ok) break;
           tc_fence_after();
@@ -433,18 +442,24 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
           const uint32_t buf = tmem + static_cast<uint32_t>(b * 128);
           const uint32_t bdo = lo(st + LK::kQTile + col_boxes * LV::kQBox, LV::kQBox);
           const uint32_t bq = lo(st + col_boxes * LK::kQBox, LK::kQBox);
+          // dK first: its commit frees this chunk's Q boxes, the first own
+          // part the producer refills, while dV and dQ^T run; dV's commit
+          // then frees the dO boxes
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k) {
+            const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
+            mma_bf16_ts_warp(tmem + C::kDkCol, buf + 64 + col,
+                             bq + (static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4), LK::kDescHi,
+                             C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit_warp(part_empty + 2);
 #pragma unroll
           for (int k = 0; k < kBN / 16; ++k) {
             const uint32_t col = static_cast<uint32_t>((k >> 1) * 32 + (k & 1) * 8);
             mma_bf16_ts_warp(tmem + 256, buf + col,
                              bdo + (static_cast<uint32_t>(k * 16 * LV::kRowBytes) >> 4), LV::kDescHi,
                              C::kIdescDV, (it > 0 || k > 0) ? 1u : 0u);
-            mma_bf16_ts_warp(tmem + C::kDkCol, buf + 64 + col,
-                             bq + (static_cast<uint32_t>(k * 16 * LK::kRowBytes) >> 4), LK::kDescHi,
-                             C::kIdescDK, (it > 0 || k > 0) ? 1u : 0u);
           }
-          // this chunk's boxes of Q and dO are free
-          mma_commit_warp(part_empty + 2);
           mma_commit_warp(part_empty + 3);
           // dQ^T(it) = K_j[:, chunk]^T dS^T(it) into the dP^T half of buffer b
           // (dP^T(it) is consumed: the compute warps released P(it))
@@ -458,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
                              k > 0 ? 1u : 0u);
           }
           mma_commit_warp(dq_full + b);
-          if (it + 1 < n_it && !(ok = wide_scores(it + 1))) break;
+          if (it + 1 < n_it && !(ok = wide_scores_own(it + 1))) break;
         }
       }
       for (int it = 0; !C::kWide && ok && it < n_it; ++it) {
@@ -662,9 +677,9 @@ __global__ void __launch_bounds__(kThreads, 1) sdpa_bwd_tc_n64(const __grid_cons
       const int b = it & 1;
       // the step's -lse2 and -D: with the stage (narrow heads) or in a slot
       // of their own (wide heads, whose stage parts are refilled early)
-      const int s = C::kWide ? (it & 1) : it % C::kStagesQ;
+      const int s = it % (C::kWide ? C::kVecBufs : C::kStagesQ);
       if constexpr (C::kWide)
-        ok = mbar_wait_warp(vec_full + s, static_cast<uint32_t>(it >> 1) & 1u, ab);
+        ok = mbar_wait_warp(vec_full + s, static_cast<uint32_t>(it / C::kVecBufs) & 1u, ab);
       else
         ok = mbar_wait_warp(q_full + s, static_cast<uint32_t>(it / C::kStagesQ) & 1u, ab);
       ok = ok && mbar_wait_warp(s_full + b, static_cast<uint32_t>(it >> 1) & 1u, ab);

@@ -5,7 +5,9 @@
 // the restricted window of section 4).  It serves two cases:
 //   - wide heads, d_k = d_v in {256, 512} (Table 3, rows (A)), whose 128 x d
 //     fp32 O does not fit the two-tile plan in 512 tensor-memory columns:
-//       d = 256: key tiles of 64; one CTA per query tile.
+//       d = 256: key tiles of 64; one CTA per query tile.  All of Q moves
+//                into tensor memory, and its 64 KB of shared memory then
+//                holds a third stage of K and V.
 //       d = 512: key tiles of 64; two CTAs per query tile, one per half of
 //                d_v, each recomputing the scores.  Q (128 KB) lands in
 //                shared memory; once the softmax warps have copied its
@@ -22,7 +24,8 @@
 //     swizzled at that width.
 // Roles:
 //   warp 4      TMA producer: Q once, K_j and V_j (this CTA's d_v slice) in
-//               two stages each.
+//               two stages each (three at d = 256; at d = 512 K has two and
+//               V one).
 //   warp 5      MMA issuer (the whole warp; one elected lane issues each
 //               instruction): S(j+1) = Q K_{j+1}^T into the free score buffer,
 //               then O += P(j) V_j with P(j) read from tensor memory.
@@ -57,8 +60,13 @@ struct OCfg {
   // the first half of Q, free once the softmax warps have copied it into
   // tensor memory, and V has one stage.
   static constexpr bool kKInQ = DK == 512;
+  // At d = 256 all of Q moves to tensor memory, so its 64 KB holds a third
+  // stage of K and of V: the loads run two tiles ahead of the products.
+  static constexpr bool kKVOverQ = DK == 256;
+  static constexpr int kRing = kKVOverQ ? 3 : 2;            // K / V stages (s_full, o_full)
   static constexpr int kKRegionStages = kKInQ ? 1 : 2;     // K stages after Q
-  static constexpr int kVStages = kKInQ ? 1 : 2;
+  static constexpr int kVStages = kKInQ ? 1 : kRing;
+  static_assert(!kKInQ || kRing == 2, "the 512-wide plan indexes its barriers by u & 1");
   static constexpr int kDvc = DK < 256 ? DK : 256;          // O columns per CTA
   static constexpr int kChunks = DK / kDvc;                 // CTAs per query tile
   // Tiles move as boxes of kBoxCols columns, rows of kRowBytes swizzled at
@@ -79,9 +87,9 @@ struct OCfg {
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + kKRegionStages * kKBytes;
   static constexpr int kBarOff = kVOff + kVStages * kVBytes;
-  // q_full, k_full[2], v_full[2], s_full[2], p_full[2], o_full[2], o_last, drain,
-  // q_tmem
-  static constexpr int kNumBars = 1 + 10 + 3;
+  // q_full, k_full[kRing], v_full[kRing], s_full[kRing], o_full[kRing],
+  // p_full[2], o_last, drain, q_tmem
+  static constexpr int kNumBars = 1 + 4 * kRing + 2 + 3;
   static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
   static constexpr uint32_t kOCol = 2 * BN;
   static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, BN, false, false);
@@ -103,6 +111,10 @@ struct OCfg {
   static_assert(!kKInQ || kQTmemSteps * 16 / kBoxCols * kQBox >= kKBytes, "K stage over Q");
   static_assert(kQTmemSteps == 0 || (kRowBytes == 128 && (kQTmemSteps * 16) % kBoxCols == 0),
                 "Q copied by whole 128-byte-swizzled boxes");
+  // the third K and V stage fits in Q, none of which the scores read from shared memory
+  static_assert(!kKVOverQ || (kQTmemSteps * 16 == DK && kKBytes + kVBytes <= kQBytes &&
+                              kKBytes % 1024 == 0 && !kKInQ),
+                "K and V stage over Q");
   static_assert(kSmemBytes * kMinBlocks <= 232448 - 1024 * kMinBlocks, "CTAs per SM");
 };
 
@@ -121,11 +133,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
   // A K stage is free again once the scores that read it are done (s_full),
   // a V stage once the O += P V that read it is done (o_full): no separate
   // "empty" barriers, so each key tile costs two commits instead of four.
-  uint64_t* v_full = k_full + 2;
-  uint64_t* s_full = v_full + 2;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_full = p_full + 2;   // o_full[u & 1]: one phase per O += P(u) V_u
-  uint64_t* o_last = o_full + 2;   // once, after the last O += P V
+  // Key tile u uses stage u % kRing and those two barriers of that index; the
+  // score buffer and p_full are u & 1.
+  constexpr int R = C::kRing;
+  uint64_t* v_full = k_full + R;
+  uint64_t* s_full = v_full + R;
+  uint64_t* o_full = s_full + R;   // o_full[u % R]: one phase per O += P(u) V_u
+  uint64_t* p_full = o_full + R;
+  uint64_t* o_last = p_full + 2;   // once, after the last O += P V
   uint64_t* drain = o_last + 1;
   uint64_t* q_tmem = drain + 1;    // the softmax warps copied Q into tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_tmem + 1);
@@ -162,13 +177,13 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < R; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(v_full + s, 1);
       mbar_init(o_full + s, 1);
       mbar_init(s_full + s, 1);
-      mbar_init(p_full + s, kBlockM);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(p_full + s, kBlockM);
     mbar_init(o_last, 1);
     mbar_init(drain, 1);
     mbar_init(q_tmem, kBlockM);
@@ -270,30 +285,34 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
       } else {
         for (int u = 0; u < n_kv; ++u) {
           const int j0 = key_base + u * BN;   // first key of the tile
-          const int s = u & 1;
-          const uint32_t use = static_cast<uint32_t>(u >> 1);
-          // S(u-2) read this stage last.  s_full[s] cannot be two phases
+          const int s = u % R;
+          const uint32_t use = static_cast<uint32_t>(u / R);
+          // S(u-R) read this stage last.  s_full[s] cannot be two phases
           // ahead: S(u) needs the K_u loaded below.
-          if (u >= 2 && !mbar_wait(s_full + s, (use - 1) & 1u, ab)) break;
+          if (u >= R && !mbar_wait(s_full + s, (use - 1) & 1u, ab)) break;
+          // the stage over Q: free once the softmax warps have copied Q into
+          // tensor memory (the scores never read Q from shared memory here)
+          if (C::kKVOverQ && u == 2 && !mbar_wait(q_tmem, 0, ab)) break;
+          uint8_t* kdst = s == 2 ? smem + C::kQOff : smem + C::kKOff + s * C::kKBytes;
           mbar_arrive_expect_tx(k_full + s, C::kKBytes);
           for (int c = 0; c < DK / C::kBoxCols; ++c)
-            tma_load_4d(&p.tm_k, k_full + s, smem + C::kKOff + s * C::kKBytes + c * C::kKVBox,
-                        c * C::kBoxCols, j0, hi, bi);
+            tma_load_4d(&p.tm_k, k_full + s, kdst + c * C::kKVBox, c * C::kBoxCols, j0, hi, bi);
           k_issued = u + 1;
-          // O += P(u-2) V(u-2) read this stage last; o_full[s] cannot be two
+          // O += P(u-R) V(u-R) read this stage last; o_full[s] cannot be two
           // phases ahead either (O += P(u) V_u needs V_u).
-          if (u >= 2 && !mbar_wait(o_full + s, (use - 1) & 1u, ab)) break;
+          if (u >= R && !mbar_wait(o_full + s, (use - 1) & 1u, ab)) break;
+          uint8_t* vdst = s == 2 ? smem + C::kQOff + C::kKBytes : smem + C::kVOff + s * C::kVBytes;
           mbar_arrive_expect_tx(v_full + s, C::kVBytes);
           for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
-            tma_load_4d(&p.tm_v, v_full + s, smem + C::kVOff + s * C::kVBytes + c * C::kKVBox,
-                        chunk * C::kDvc + c * C::kBoxCols, j0, hi, bi);
+            tma_load_4d(&p.tm_v, v_full + s, vdst + c * C::kKVBox, chunk * C::kDvc + c * C::kBoxCols,
+                        j0, hi, bi);
           v_issued = u + 1;
         }
         mbar_wait_drain(q_full, 0);
-        for (int u = max(0, k_issued - 2); u < k_issued; ++u)
-          mbar_wait_drain(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
-        for (int u = max(0, v_issued - 2); u < v_issued; ++u)
-          mbar_wait_drain(v_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
+        for (int u = max(0, k_issued - R); u < k_issued; ++u)
+          mbar_wait_drain(k_full + u % R, static_cast<uint32_t>(u / R) & 1u);
+        for (int u = max(0, v_issued - R); u < v_issued; ++u)
+          mbar_wait_drain(v_full + u % R, static_cast<uint32_t>(u / R) & 1u);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -309,9 +328,11 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
       // k steps, and commits s_full.
       auto issue_s = [&](int u) -> bool {
         const uint32_t d = tmem + static_cast<uint32_t>((u & 1) * BN);
-        const uint32_t k_base = (u & 1) ? (C::kKInQ ? C::kQOff : C::kKOff + C::kKBytes) : C::kKOff;
+        const int ks = u % R;
+        const uint32_t k_base =
+            ks == 0 ? C::kKOff : ((ks == 2 || C::kKInQ) ? C::kQOff : C::kKOff + C::kKBytes);
         const uint32_t b0 = lo(smem_base + k_base, 16);
-        if (!mbar_wait_warp(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab)) return false;
+        if (!mbar_wait_warp(k_full + ks, static_cast<uint32_t>(u / R) & 1u, ab)) return false;
         tc_fence_after();
         constexpr int kSteps = DK / 16;
 #pragma unroll
@@ -331,13 +352,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
         // the producer once it needs that K stage again, run out)
         if (u == 0) return true;
 #endif
-        mma_commit_warp(s_full + (u & 1));
+        mma_commit_warp(s_full + ks);
         return true;
       };
       auto issue_pv = [&](int u) {
         const uint32_t pa = tmem + static_cast<uint32_t>((u & 1) * BN);
-        const int stage = C::kVStages == 1 ? 0 : (u & 1);
-        const uint32_t b0 = lo(smem_base + C::kVOff + stage * C::kVBytes, C::kKVBox);
+        const int stage = C::kVStages == 1 ? 0 : u % R;
+        const uint32_t v_base = stage == 2 ? C::kQOff + C::kKBytes : C::kVOff + stage * C::kVBytes;
+        const uint32_t b0 = lo(smem_base + v_base, C::kKVBox);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k) {
           mma_bf16_ts_warp(tmem + C::kOCol, pa + static_cast<uint32_t>(k * 8),
@@ -354,14 +376,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
         // S(u+1) into the buffer of P(u-1): PV(u-1) was issued before it.
         const bool next = u + 1 < n_kv;
         if (next && !(ok = issue_s(u + 1))) break;
-        const uint32_t vs = C::kVStages == 1 ? 0u : static_cast<uint32_t>(u & 1);
-        const uint32_t vph = static_cast<uint32_t>(C::kVStages == 1 ? u : (u >> 1)) & 1u;
+        const uint32_t vs = C::kVStages == 1 ? 0u : static_cast<uint32_t>(u % R);
+        const uint32_t vph = static_cast<uint32_t>(C::kVStages == 1 ? u : u / R) & 1u;
         ok = mbar_wait_warp(p_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab) &&
              mbar_wait_warp(v_full + vs, vph, ab);
         if (!ok) break;
         tc_fence_after();
         issue_pv(u);
-        mma_commit_warp(o_full + (u & 1));
+        mma_commit_warp(o_full + u % R);
         if (u + 1 == n_kv) mma_commit_warp(o_last);
       }
       mma_commit_warp(drain);
@@ -408,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
     }
     for (int u = 0; ok && u < n_kv; ++u) {
       const uint32_t s_col = static_cast<uint32_t>((u & 1) * BN);
-      ok = mbar_wait_warp(s_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u, ab);
+      ok = mbar_wait_warp(s_full + u % R, static_cast<uint32_t>(u / R) & 1u, ab);
       if (!ok) break;
       tc_fence_after();
       float s[BN];
@@ -455,13 +477,14 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           l *= alpha;
         }
         // Only a rescale touches O, and it must follow O += P(u-1) V(u-1),
-        // whose barrier is o_full[(u-1) & 1].  Holding S(u) means
+        // whose barrier is o_full[(u-1) % R].  Holding S(u) means
         // O += P(u-2) V(u-2) has landed (S(u) was issued after it), so the
-        // barrier's previous phase, u-3, is complete; and O += P(u+1) V(u+1)
-        // needs this softmax's next P.  Its parity wait for the phase of u-1
-        // is therefore exact even though earlier phases were not waited on.
+        // barrier's previous phase, u-1-R, is complete; and its next one,
+        // u-1+R, is at least O += P(u+1) V(u+1), which needs this softmax's
+        // next P.  Its parity wait for the phase of u-1 is therefore exact
+        // even though earlier phases were not waited on.
         if (rescale_warp) {
-          ok = mbar_wait_warp(o_full + ((u - 1) & 1), static_cast<uint32_t>((u - 1) >> 1) & 1u, ab);
+          ok = mbar_wait_warp(o_full + (u - 1) % R, static_cast<uint32_t>((u - 1) / R) & 1u, ab);
           if (!ok) break;
           tc_fence_after();
         }
