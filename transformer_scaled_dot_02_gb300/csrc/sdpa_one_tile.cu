@@ -283,29 +283,36 @@ __global__ void __launch_bounds__(kThreads, OCfg<DK, KT>::kMinBlocks)
           mbar_wait_drain(k_full + (u & 1), static_cast<uint32_t>(u >> 1) & 1u);
         if (v_issued > 0) mbar_wait_drain(v_full, static_cast<uint32_t>(v_issued - 1) & 1u);
       } else {
-        for (int u = 0; u < n_kv; ++u) {
-          const int j0 = key_base + u * BN;   // first key of the tile
+        // K_{u+1} goes ahead of V_u: its stage is free once S(u+1-R) is done,
+        // which comes before O += P(u-R) V_{u-R}, the product that frees V_u's.
+        auto load_ring_k = [&](int u) -> bool {
           const int s = u % R;
-          const uint32_t use = static_cast<uint32_t>(u / R);
           // S(u-R) read this stage last.  s_full[s] cannot be two phases
-          // ahead: S(u) needs the K_u loaded below.
-          if (u >= R && !mbar_wait(s_full + s, (use - 1) & 1u, ab)) break;
+          // ahead: S(u) needs the K_u loaded here.
+          if (u >= R && !mbar_wait(s_full + s, static_cast<uint32_t>(u / R - 1) & 1u, ab)) return false;
           // the stage over Q: free once the softmax warps have copied Q into
           // tensor memory (the scores never read Q from shared memory here)
-          if (C::kKVOverQ && u == 2 && !mbar_wait(q_tmem, 0, ab)) break;
+          if (C::kKVOverQ && u == 2 && !mbar_wait(q_tmem, 0, ab)) return false;
           uint8_t* kdst = s == 2 ? smem + C::kQOff : smem + C::kKOff + s * C::kKBytes;
           mbar_arrive_expect_tx(k_full + s, C::kKBytes);
           for (int c = 0; c < DK / C::kBoxCols; ++c)
-            tma_load_4d(&p.tm_k, k_full + s, kdst + c * C::kKVBox, c * C::kBoxCols, j0, hi, bi);
+            tma_load_4d(&p.tm_k, k_full + s, kdst + c * C::kKVBox, c * C::kBoxCols, key_base + u * BN,
+                        hi, bi);
           k_issued = u + 1;
+          return true;
+        };
+        bool go = load_ring_k(0);
+        for (int u = 0; go && u < n_kv; ++u) {
+          if (u + 1 < n_kv && !(go = load_ring_k(u + 1))) break;
+          const int s = u % R;
           // O += P(u-R) V(u-R) read this stage last; o_full[s] cannot be two
           // phases ahead either (O += P(u) V_u needs V_u).
-          if (u >= R && !mbar_wait(o_full + s, (use - 1) & 1u, ab)) break;
+          if (u >= R && !mbar_wait(o_full + s, static_cast<uint32_t>(u / R - 1) & 1u, ab)) break;
           uint8_t* vdst = s == 2 ? smem + C::kQOff + C::kKBytes : smem + C::kVOff + s * C::kVBytes;
           mbar_arrive_expect_tx(v_full + s, C::kVBytes);
           for (int c = 0; c < C::kDvc / C::kBoxCols; ++c)
             tma_load_4d(&p.tm_v, v_full + s, vdst + c * C::kKVBox, chunk * C::kDvc + c * C::kBoxCols,
-                        j0, hi, bi);
+                        key_base + u * BN, hi, bi);
           v_issued = u + 1;
         }
         mbar_wait_drain(q_full, 0);
