@@ -110,9 +110,9 @@ struct Cfg {
   // head.  K and V stay resident (128 KB), which leaves room for one stage
   // of Q and dO and one dS^T buffer.  The stage's boxes come in four parts
   // with barriers of their own: Q's and dO's boxes of the other chunk, free
-  // once the step's scores have read them, and of this CTA's chunk, free
-  // once dV and dK have; so the next step's loads run while this step's
-  // softmax and products do.
+  // once the step's scores have read them, and this CTA's chunk of Q, free
+  // once dK has read it, and of dO, once dV has; so the next step's loads
+  // run while this step's softmax and products do.
   static constexpr bool kWide = DK > 128;
   static constexpr int kColsK = kWide ? 128 : DK;           // dK / dQ columns of a CTA
   static constexpr int kColsV = kWide ? 128 : DV;           // dV columns of a CTA
