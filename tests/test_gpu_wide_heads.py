@@ -61,6 +61,20 @@ def test_wide_ragged_causal(d, n):
 
 
 @pytest.mark.parametrize("d", [256, 512])
+@pytest.mark.parametrize("n_k", [1, 63, 64, 65, 128, 191, 192, 193, 256, 320, 385, 448, 449, 512])
+def test_wide_key_walk_lengths(d, n_k):
+    """Key walks of 1 to 8 tiles of 64, whole and ragged, through the K and V
+    stages (three of each at d = 256, the third in Q's shared memory; two of
+    K and one of V at d = 512): cross-attention without a mask, then with
+    key padding that ends the walk inside a tile."""
+    rng = np.random.default_rng(11300 + d + n_k)
+    b, h, n_q = 2, 1, 130
+    q, k, v = _rand(rng, (b, h, n_q, d)), _rand(rng, (b, h, n_k, d)), _rand(rng, (b, h, n_k, d))
+    _check(q, k, v, 0, None)
+    _check(q, k, v, 2, np.array([n_k, max(0, n_k - 37)], np.int32))
+
+
+@pytest.mark.parametrize("d", [256, 512])
 @pytest.mark.parametrize("r", [1, 2, 63, 64, 200])
 def test_wide_restricted(d, r):
     rng = np.random.default_rng(11200 + d + r)
